@@ -1,0 +1,108 @@
+"""Seeded synthetic workloads for the FlashAttention-2 forward pass.
+
+This module is shared by the CUDA path's tests/bench and by the CPU oracle's
+tests. It draws inputs and counts work; it holds none of the attention
+arithmetic itself.
+
+Workloads follow the shapes named for this path (all tensors [B, H, N, D],
+Q/K/V i.i.d. normal, cast to the 16-bit type with round-to-nearest-even):
+
+  tiny      B=1  H=1  N=128    D=64   fp16  non-causal   seed 0
+  pages     B=1  H=8  N=8192   D=64   fp16  non-causal   seed 1
+            (the shape of the RTX 4090 table on the "FlashAttention-2 MMA
+            代码学习" page, performance table at the top of the page)
+  causal128 B=4  H=16 N=4096   D=128  bf16  causal       seed 2
+  ragged    B=2  H=12 N=1000   D=64   fp16  non-causal   seed 3, Q/K ~ N(0, 3^2)
+  long      B=1  H=4  N=32768  D=128  bf16  causal       seed 4
+  target    B=1  H=8  N=8192   D=128  bf16  non-causal   seed 5
+            (the N=8192, D=128 non-causal case the throughput goal is stated on)
+  target_f16  same shape as target in fp16, seed 5
+  target_b4   B=4 H=16 N=8192 D=128 bf16 non-causal, seed 6 (supplementary: more
+              units per SM, less wave-quantisation tail)
+
+Scale is 1/sqrt(D) everywhere. Draw order: Q, then K, then V, each
+``torch.randn(shape, dtype=float32, generator=g) * sigma`` from a CPU
+generator seeded with the workload's seed, then cast to the 16-bit dtype.
+"""
+from __future__ import annotations
+
+import math
+from dataclasses import dataclass, replace
+
+import torch
+
+
+@dataclass(frozen=True)
+class Workload:
+    name: str
+    B: int
+    H: int
+    N: int
+    D: int
+    dtype: str          # "f16" or "bf16"
+    causal: bool
+    seed: int
+    sigma_qk: float = 1.0
+    sigma_v: float = 1.0
+
+    @property
+    def scale(self) -> float:
+        return 1.0 / math.sqrt(self.D)
+
+    @property
+    def torch_dtype(self) -> torch.dtype:
+        return torch.float16 if self.dtype == "f16" else torch.bfloat16
+
+    def describe(self) -> str:
+        return (f"B{self.B}-H{self.H}-N{self.N}-D{self.D} {self.dtype} "
+                f"{'causal' if self.causal else 'non-causal'}")
+
+
+WORKLOADS = {
+    "tiny": Workload("tiny", 1, 1, 128, 64, "f16", False, 0),
+    "pages": Workload("pages", 1, 8, 8192, 64, "f16", False, 1),
+    "causal128": Workload("causal128", 4, 16, 4096, 128, "bf16", True, 2),
+    "ragged": Workload("ragged", 2, 12, 1000, 64, "f16", False, 3, sigma_qk=3.0),
+    "long": Workload("long", 1, 4, 32768, 128, "bf16", True, 4),
+    "target": Workload("target", 1, 8, 8192, 128, "bf16", False, 5),
+    "target_f16": Workload("target_f16", 1, 8, 8192, 128, "f16", False, 5),
+    "target_b4": Workload("target_b4", 4, 16, 8192, 128, "bf16", False, 6),
+}
+
+# The five workloads the parity contract names, in their stated order.
+CONTRACT = ("tiny", "pages", "causal128", "ragged", "long")
+
+
+def custom(B: int, H: int, N: int, D: int, dtype: str = "bf16", causal: bool = False,
+           seed: int = 0, sigma_qk: float = 1.0, sigma_v: float = 1.0) -> Workload:
+    """A workload of arbitrary shape (used by edge-case tests and sweeps)."""
+    return Workload(f"B{B}H{H}N{N}D{D}{dtype}{'c' if causal else ''}s{seed}",
+                    B, H, N, D, dtype, causal, seed, sigma_qk, sigma_v)
+
+
+def make_inputs(w: Workload):
+    """Return (q, k, v) as contiguous CPU tensors of the workload's 16-bit dtype."""
+    g = torch.Generator(device="cpu")
+    g.manual_seed(w.seed)
+    shape = (w.B, w.H, w.N, w.D)
+    q = torch.randn(shape, dtype=torch.float32, generator=g) * w.sigma_qk
+    k = torch.randn(shape, dtype=torch.float32, generator=g) * w.sigma_qk
+    v = torch.randn(shape, dtype=torch.float32, generator=g) * w.sigma_v
+    dt = w.torch_dtype
+    return q.to(dt).contiguous(), k.to(dt).contiguous(), v.to(dt).contiguous()
+
+
+def flops(w: Workload) -> float:
+    """Metric FLOPs of one forward: 4*B*H*N^2*D, halved under the causal mask."""
+    f = 4.0 * w.B * w.H * float(w.N) * w.N * w.D
+    return f / 2.0 if w.causal else f
+
+
+def algorithmic_bytes(w: Workload) -> int:
+    """Compulsory HBM bytes: read Q, K, V once, write O (16-bit) and LSE (fp32)."""
+    elems = w.B * w.H * w.N * w.D
+    return 4 * elems * 2 + w.B * w.H * w.N * 4
+
+
+def with_seed(w: Workload, seed: int) -> Workload:
+    return replace(w, seed=seed)
