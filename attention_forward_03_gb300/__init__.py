@@ -1,0 +1,14 @@
+"""GB300 (sm_103a) FlashAttention-2 forward: a C-ABI library plus a thin Python binding.
+
+    from attention_forward_03_gb300 import attention_forward
+    O, LSE = attention_forward(q, k, v, is_causal=True)
+
+The compute runs in libfa2_gb300.so (build it with
+``attention_forward_03_gb300.build.build()``); the binding fails loudly if it
+is missing.
+"""
+from .binding import (  # noqa: F401
+    FA2_BF16, FA2_ERR_ALIGN, FA2_ERR_CUDA, FA2_ERR_INVALID_ARG, FA2_ERR_TIMEOUT, FA2_ERR_UNSUPPORTED,
+    FA2_F16, FA2_OK, Fa2Error, attention_forward, error_text, fa2_device_status, fa2_fwd,
+    fa2_set_watchdog_ns, fa2_version, library,
+)

@@ -1,0 +1,139 @@
+"""Thin ctypes binding over the C ABI in include/fa2.h (argument marshalling only).
+
+Every step of the forward pass runs in the sm_103a kernels of
+libfa2_gb300.so. This module only turns tensors into pointers, sizes and a
+stream handle, and turns status codes into exceptions. There is no fallback:
+if the library is missing, importing the functions below raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+
+LIB_NAME = "libfa2_gb300.so"
+LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), LIB_NAME)
+
+FA2_F16 = 0
+FA2_BF16 = 1
+FA2_OK = 0
+FA2_ERR_INVALID_ARG = -1
+FA2_ERR_UNSUPPORTED = -2
+FA2_ERR_ALIGN = -3
+FA2_ERR_CUDA = -4
+FA2_ERR_TIMEOUT = -5
+
+# every symbol include/fa2.h declares, with its ctypes signature
+_VP = ctypes.c_void_p
+SIGNATURES = {
+    "fa2_fwd": (ctypes.c_int, [_VP, _VP, _VP, _VP, _VP, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                               ctypes.c_int, ctypes.c_float, ctypes.c_int, ctypes.c_int, _VP]),
+    "fa2_device_status": (ctypes.c_int, [_VP, ctypes.POINTER(ctypes.c_int), ctypes.c_int]),
+    "fa2_set_watchdog_ns": (ctypes.c_int, [ctypes.c_ulonglong]),
+    "fa2_error_string": (ctypes.c_char_p, [ctypes.c_int]),
+    "fa2_last_cuda_error": (ctypes.c_char_p, []),
+    "fa2_version": (ctypes.c_int, []),
+}
+
+_lib = None
+
+
+class Fa2Error(RuntimeError):
+    def __init__(self, code: int, what: str):
+        super().__init__(what)
+        self.code = code
+
+
+def library() -> ctypes.CDLL:
+    """Load libfa2_gb300.so (built in-tree by attention_forward_03_gb300.build)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise ImportError(f"{LIB_NAME} is not built (expected at {LIB_PATH}); "
+                              "run attention_forward_03_gb300.build.build()")
+        lib = ctypes.CDLL(LIB_PATH)
+        for name, (res, args) in SIGNATURES.items():
+            fn = getattr(lib, name)
+            fn.restype = res
+            fn.argtypes = args
+        _lib = lib
+    return _lib
+
+
+def error_text(code: int) -> str:
+    lib = library()
+    msg = lib.fa2_error_string(code).decode()
+    if code == FA2_ERR_CUDA:
+        msg += f" ({lib.fa2_last_cuda_error().decode()})"
+    return msg
+
+
+def _check(code: int, what: str) -> None:
+    if code != FA2_OK:
+        raise Fa2Error(code, f"{what}: {error_text(code)} [{code}]")
+
+
+def fa2_fwd(Q: int, K: int, V: int, O: int, LSE: int, B: int, H: int, N: int, D: int, scale: float,
+            is_causal: int, dtype: int, stream: int | None) -> int:
+    """Pointer-level call with the C ABI's argument list; returns the raw status code."""
+    return library().fa2_fwd(Q, K, V, O, LSE, B, H, N, D, float(scale), int(is_causal), int(dtype), stream)
+
+
+def fa2_device_status(stream: int | None = None, clear: bool = False) -> int:
+    v = ctypes.c_int(0)
+    _check(library().fa2_device_status(stream, ctypes.byref(v), int(bool(clear))), "fa2_device_status")
+    return v.value
+
+
+def fa2_set_watchdog_ns(ns: int) -> None:
+    _check(library().fa2_set_watchdog_ns(int(ns)), "fa2_set_watchdog_ns")
+
+
+def fa2_version() -> int:
+    return library().fa2_version()
+
+
+# ------------------------------------------------------------ tensor helpers
+def _dtype_code(t) -> int:
+    import torch
+    if t.dtype == torch.float16:
+        return FA2_F16
+    if t.dtype == torch.bfloat16:
+        return FA2_BF16
+    raise TypeError(f"unsupported dtype {t.dtype}; expected float16 or bfloat16")
+
+
+def attention_forward(q, k, v, scale: float | None = None, is_causal: bool = False, out=None, lse=None,
+                      stream=None):
+    """FlashAttention-2 forward over torch CUDA tensors [B, H, N, D] (fp16/bf16).
+
+    Returns (O, LSE): O like q, LSE float32 [B, H, N]. `out` / `lse` may be
+    passed to write into caller-owned buffers. Runs on `stream` (a
+    torch.cuda.Stream) or the current stream.
+    """
+    import torch
+    if not (q.is_cuda and k.is_cuda and v.is_cuda):
+        raise ValueError("q, k, v must be CUDA tensors")
+    if q.shape != k.shape or q.shape != v.shape or q.dim() != 4:
+        raise ValueError("q, k, v must share one [B, H, N, D] shape")
+    if q.dtype != k.dtype or q.dtype != v.dtype:
+        raise ValueError("q, k, v must share one dtype")
+    if not (q.is_contiguous() and k.is_contiguous() and v.is_contiguous()):
+        raise ValueError("q, k, v must be contiguous")
+    B, H, N, D = q.shape
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
+    if out.shape != q.shape or out.dtype != q.dtype or not out.is_contiguous():
+        raise ValueError("out must be a contiguous tensor like q")
+    if lse.shape != (B, H, N) or lse.dtype != torch.float32 or not lse.is_contiguous():
+        raise ValueError("lse must be a contiguous float32 [B, H, N] tensor")
+    s = stream if stream is not None else torch.cuda.current_stream(q.device)
+    with torch.cuda.device(q.device):
+        code = fa2_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(),
+                       B, H, N, D, scale, int(bool(is_causal)), _dtype_code(q), s.cuda_stream)
+    _check(code, "fa2_fwd")
+    return out, lse

@@ -1,0 +1,207 @@
+// C ABI of the forward library: argument validation, TMA descriptors, the
+// persistent launch and the device watchdog word. Declarations and the
+// contract of every entry point: include/fa2.h.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <cmath>
+#include <cstdint>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+
+#include "fa2.h"
+#include "fa2_launch.h"
+
+namespace fa2 {
+namespace {
+
+constexpr int kMaxDevices = 64;
+constexpr unsigned long long kDefaultWatchdogNs = 1000000000ull;
+
+__device__ int g_watchdog_word;  // 0 = no timeout since last clear
+
+std::atomic<unsigned long long> g_watchdog_ns{kDefaultWatchdogNs};
+thread_local char t_last_cuda_error[256] = "";
+
+struct DeviceInfo {
+  std::once_flag once;
+  cudaError_t err = cudaSuccess;
+  int sms = 0;
+  int cc_major = 0, cc_minor = 0;
+  int* status = nullptr;
+};
+DeviceInfo g_devices[kMaxDevices];
+
+int record_cuda(cudaError_t e) {
+  std::snprintf(t_last_cuda_error, sizeof(t_last_cuda_error), "%s: %s", cudaGetErrorName(e),
+                cudaGetErrorString(e));
+  return FA2_ERR_CUDA;
+}
+
+// Device properties and the watchdog word's device address, once per device,
+// queried with that device current.
+DeviceInfo* device_info(int dev) {
+  if (dev < 0 || dev >= kMaxDevices) return nullptr;
+  DeviceInfo& d = g_devices[dev];
+  std::call_once(d.once, [&] {
+    cudaError_t e = cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&d.cc_major, cudaDevAttrComputeCapabilityMajor, dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&d.cc_minor, cudaDevAttrComputeCapabilityMinor, dev);
+    if (e == cudaSuccess) e = cudaGetSymbolAddress(reinterpret_cast<void**>(&d.status), g_watchdog_word);
+    d.err = e;
+  });
+  return &d;
+}
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static std::once_flag once;
+  static EncodeTiledFn fn = nullptr;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+// [B*H, N, D] view of a [B,H,N,D] tensor; 128 rows x 64 elements per box,
+// 128-byte swizzle; rows past N read as zeros.
+bool make_map(CUtensorMap* map, const void* ptr, int bh, int n, int d, int dtype) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return false;
+  cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)n, (cuuint64_t)bh};
+  cuuint64_t strides[2] = {(cuuint64_t)d * 2, (cuuint64_t)n * d * 2};
+  cuuint32_t box[3] = {64, 128, 1};
+  cuuint32_t estride[3] = {1, 1, 1};
+  CUresult r = enc(map, dtype == FA2_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3,
+                   const_cast<void*>(ptr), dims, strides, box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                   CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
+  const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
+  return x < y + nb && y < x + na;
+}
+
+using LaunchFn = cudaError_t (*)(const CUtensorMap&, const CUtensorMap&, const CUtensorMap&, const Params&, int,
+                                 cudaStream_t);
+
+LaunchFn pick(int d, int dtype, int causal) {
+  const bool bf = dtype == FA2_BF16, c = causal != 0;
+  if (d == 64) {
+    if (bf) return c ? launch_fwd<64, true, true> : launch_fwd<64, true, false>;
+    return c ? launch_fwd<64, false, true> : launch_fwd<64, false, false>;
+  }
+  if (bf) return c ? launch_fwd<128, true, true> : launch_fwd<128, true, false>;
+  return c ? launch_fwd<128, false, true> : launch_fwd<128, false, false>;
+}
+
+}  // namespace
+}  // namespace fa2
+
+using namespace fa2;
+
+extern "C" int fa2_fwd(const void* Q, const void* K, const void* V, void* O, float* LSE, int B, int H, int N,
+                       int D, float scale, int is_causal, int dtype, struct CUstream_st* stream) {
+  if (B < 0 || H < 0 || N < 0) return FA2_ERR_INVALID_ARG;
+  if (D != 64 && D != 128) return FA2_ERR_UNSUPPORTED;
+  if (dtype != FA2_F16 && dtype != FA2_BF16) return FA2_ERR_UNSUPPORTED;
+  if (!std::isfinite(scale) || !(scale > 0.f)) return FA2_ERR_INVALID_ARG;
+  if (B == 0 || H == 0 || N == 0) return FA2_OK;
+  if (!Q || !K || !V || !O || !LSE) return FA2_ERR_INVALID_ARG;
+  const int64_t bh = static_cast<int64_t>(B) * H;
+  const int64_t n_qt = (static_cast<int64_t>(N) + kUnitRows - 1) / kUnitRows;
+  if (bh > INT32_MAX || bh * n_qt > INT32_MAX) return FA2_ERR_INVALID_ARG;
+  const uintptr_t mis = reinterpret_cast<uintptr_t>(Q) | reinterpret_cast<uintptr_t>(K) |
+                        reinterpret_cast<uintptr_t>(V) | reinterpret_cast<uintptr_t>(O) |
+                        reinterpret_cast<uintptr_t>(LSE);
+  if (mis & 15u) return FA2_ERR_ALIGN;
+  const size_t tbytes = static_cast<size_t>(bh) * N * D * 2;
+  const size_t lbytes = static_cast<size_t>(bh) * N * 4;
+  if (overlaps(O, tbytes, Q, tbytes) || overlaps(O, tbytes, K, tbytes) || overlaps(O, tbytes, V, tbytes) ||
+      overlaps(LSE, lbytes, Q, tbytes) || overlaps(LSE, lbytes, K, tbytes) || overlaps(LSE, lbytes, V, tbytes) ||
+      overlaps(LSE, lbytes, O, tbytes))
+    return FA2_ERR_INVALID_ARG;
+
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return record_cuda(e);
+  DeviceInfo* info = device_info(dev);
+  if (!info) return FA2_ERR_UNSUPPORTED;
+  if (info->err != cudaSuccess) return record_cuda(info->err);
+  if (info->cc_major != 10 || info->cc_minor != 3) return FA2_ERR_UNSUPPORTED;
+
+  CUtensorMap mq, mk, mv;
+  if (!make_map(&mq, Q, (int)bh, N, D, dtype) || !make_map(&mk, K, (int)bh, N, D, dtype) ||
+      !make_map(&mv, V, (int)bh, N, D, dtype)) {
+    std::snprintf(t_last_cuda_error, sizeof(t_last_cuda_error), "cuTensorMapEncodeTiled failed");
+    return FA2_ERR_CUDA;
+  }
+  Params p;
+  p.o = O;
+  p.lse = LSE;
+  p.status = info->status;
+  p.watchdog_ns = g_watchdog_ns.load(std::memory_order_relaxed);
+  p.N = N;
+  p.BH = (int)bh;
+  p.n_qt = (int)n_qt;
+  p.num_units = (int)(bh * n_qt);
+  p.scale_log2 = scale * 1.4426950408889634f;
+  const int grid = p.num_units < info->sms ? p.num_units : info->sms;
+  e = pick(D, dtype, is_causal)(mq, mk, mv, p, grid, reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return record_cuda(e);
+  return FA2_OK;
+}
+
+extern "C" int fa2_device_status(struct CUstream_st* stream, int* status, int clear) {
+  if (!status) return FA2_ERR_INVALID_ARG;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return record_cuda(e);
+  DeviceInfo* info = device_info(dev);
+  if (!info) return FA2_ERR_UNSUPPORTED;
+  if (info->err != cudaSuccess) return record_cuda(info->err);
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  int v = 0;
+  e = cudaMemcpyAsync(&v, info->status, sizeof(int), cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  if (e == cudaSuccess && clear) {
+    e = cudaMemsetAsync(info->status, 0, sizeof(int), s);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  }
+  if (e != cudaSuccess) return record_cuda(e);
+  *status = v;
+  return FA2_OK;
+}
+
+extern "C" int fa2_set_watchdog_ns(unsigned long long ns) {
+  g_watchdog_ns.store(ns ? ns : kDefaultWatchdogNs, std::memory_order_relaxed);
+  return FA2_OK;
+}
+
+extern "C" const char* fa2_error_string(int code) {
+  switch (code) {
+    case FA2_OK: return "ok";
+    case FA2_ERR_INVALID_ARG: return "invalid argument";
+    case FA2_ERR_UNSUPPORTED: return "unsupported head dimension, dtype or device";
+    case FA2_ERR_ALIGN: return "tensor pointer not 16-byte aligned";
+    case FA2_ERR_CUDA: return "CUDA call failed";
+    case FA2_ERR_TIMEOUT: return "device watchdog timeout";
+    default: return "unknown status";
+  }
+}
+
+extern "C" const char* fa2_last_cuda_error(void) { return t_last_cuda_error; }
+
+extern "C" int fa2_version(void) { return (1 << 16) | 0; }

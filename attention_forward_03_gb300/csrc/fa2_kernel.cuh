@@ -1,0 +1,500 @@
+// FlashAttention-2 forward for GB300 (sm_103a): persistent, warp-specialised,
+// TMA-fed, tcgen05 tensor cores accumulating in tensor memory (TMEM).
+//
+// What it computes is the FlashAttention-2 forward pass as the pages define it
+// ("FlashAttention-2 MMA 代码学习", steps 0-1: O = softmax(QK^T*scale) V with
+// the row-wise online (m, l) merge; yangyitao.com CUDA book ch. 15: outer loop
+// over query tiles and inner loop over K/V tiles (15.1, change 1), sequence
+// length as a grid axis (15.1, change 2), one thread of work per query row
+// with no cross-warp reduction (15.1, change 3, the split-Q idea), deferred
+// division by l and LSE = m + log l as the only statistic kept (15.1,
+// change 4), causal tile skip, column and row masking for ragged N and the
+// -inf guards (15.3)).
+//
+// Layout of one CTA (one per SM, persistent over work units):
+//   work unit  = 256 query rows of one (batch, head): two 128-row sub-tiles.
+//   warps 0-3  softmax warpgroup for sub-tile 0 (thread = query row = TMEM lane)
+//   warps 4-7  softmax warpgroup for sub-tile 1
+//   warp  8    tcgen05 MMA issuer (one thread) and TMEM owner
+//   warp  9    TMA producer (one thread)
+// Tensor memory (512 columns x 128 lanes of 32 bits):
+//   [0,128)    S0: scores of sub-tile 0 (fp32); P0 (16-bit pairs) is written
+//              back over its first 64 columns
+//   [128,256)  S1 / P1 likewise for sub-tile 1
+//   [256,256+D)       O0 accumulator (fp32)
+//   [256+D,256+2D)    O1 accumulator
+// Shared memory: Q (2 sub-tiles, resident for the unit) and a ring of K/V
+// tiles (K_j, V_j, K_j+1, ...), all 128-byte swizzled by TMA in 128-row x
+// 64-element panels, which is also the operand layout the MMAs read.
+//
+// Per K/V tile j the MMA thread issues, for each sub-tile t in turn:
+//   O_t (+)= P_t(j) V_j      once softmax t has published P_t(j)
+//   S_t    = Q_t K_{j+1}^T   right after, into the same TMEM columns
+// Tensor-core ops issued by one thread run in issue order, so S_t(j+1) never
+// overwrites P_t(j) before the P.V product has read it, and the completion of
+// S_t(j+1) implies that of P_t(j).V_j: the softmax warpgroup may rescale O_t
+// as soon as it sees S_t(j+1).
+#pragma once
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <math_constants.h>
+#include <stdint.h>
+
+#include "fa2_launch.h"
+#include "sm103_ptx.cuh"
+#include "tmem_io.cuh"
+
+namespace fa2 {
+
+constexpr int kThreads = 320;
+constexpr int kMmaWarp = 8;
+constexpr int kLoadWarp = 9;
+constexpr int kPanelBytes = 128 * 128;  // 128 rows x 64 16-bit elements
+constexpr uint32_t kTmemCols = 512;
+
+// Watchdog codes written to the status word (site of the wait that gave up).
+enum : int {
+  kSiteLoadQEmpty = 1,
+  kSiteLoadRingEmpty = 2,
+  kSiteMmaQFull = 3,
+  kSiteMmaRingFull = 4,
+  kSiteMmaPFull = 5,
+  kSiteSoftmaxSFull = 6,
+  kSiteSoftmaxOFull = 7,
+  kSiteDrain = 8,
+};
+
+template <int D>
+struct Layout {
+  static constexpr int kPanels = D / 64;
+  static constexpr int kTileBytes = kPanels * kPanelBytes;
+  static constexpr int kStages = (D == 128) ? 5 : 8;
+  static constexpr int kQBytes = kSubTiles * kTileBytes;
+  static constexpr int kRingOffset = kQBytes;
+  static constexpr int kBarOffset = kRingOffset + kStages * kTileBytes;
+  // barriers: q_full, q_empty, ring full[S], ring empty[S], s_full[2], p_full[2], o_full[2], drain
+  static constexpr int kNumBars = 2 + 2 * kStages + 6 + 1;
+  static constexpr int kMiscOffset = kBarOffset + kNumBars * 8;
+  static constexpr int kSmemBytes = kMiscOffset + 16 + 1024;  // + slack for 1 KB alignment
+  static constexpr uint32_t kColO = 2 * kKeys;                 // O0 at 256, O1 at 256 + D
+  static_assert(kColO + 2 * D <= kTmemCols, "TMEM budget");
+  static_assert(kSmemBytes <= 232448, "shared memory budget");
+};
+
+struct Unit {
+  int bh;
+  int q0;
+  int nkv;
+};
+
+template <bool kCausal>
+__device__ __forceinline__ Unit decode_unit(int u, const Params& p) {
+  int qt, bh;
+  if (kCausal) {  // heaviest query tiles first
+    qt = p.n_qt - 1 - u / p.BH;
+    bh = u % p.BH;
+  } else {        // consecutive units share a head (K/V reuse in L2)
+    qt = u % p.n_qt;
+    bh = u / p.n_qt;
+  }
+  Unit w;
+  w.bh = bh;
+  w.q0 = qt * kUnitRows;
+  const int kend = kCausal ? min(p.N, w.q0 + kUnitRows) : p.N;
+  w.nkv = (kend + kKeys - 1) / kKeys;
+  return w;
+}
+
+// The r-th unit of this CTA; causal work is dealt in a zig-zag so that the
+// heavy and light ends of each round are spread over the CTAs.
+template <bool kCausal>
+__device__ __forceinline__ int unit_of_round(int r) {
+  const int g = gridDim.x, b = blockIdx.x;
+  return r * g + ((kCausal && (r & 1)) ? (g - 1 - b) : b);
+}
+
+struct Watchdog {
+  int* status;
+  volatile int* abort_flag;
+  unsigned long long limit_ns;
+};
+
+// Bounded wait. Returns false when the limit passes (recording `site` in the
+// status word and raising the CTA's abort flag) or when another role of the
+// CTA has already aborted. `honour_abort` = false is used while draining.
+__device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, const Watchdog& wd, int site,
+                                          bool honour_abort = true) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_timer_ns();
+  for (uint32_t it = 1;; ++it) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((it & 31u) == 0) {
+      if (honour_abort && *wd.abort_flag) return false;
+      if (global_timer_ns() - t0 > wd.limit_ns) {
+        *wd.abort_flag = 1;
+        atomicCAS(wd.status, 0, site);
+        return false;
+      }
+    }
+  }
+}
+
+__device__ __forceinline__ uint32_t pack2(float lo, float hi, bool bf16) {
+  if (bf16) {
+    __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&h);
+  } else {
+    __half2 h = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&h);
+  }
+}
+
+template <int D, bool kBf16, bool kCausal>
+__global__ void __launch_bounds__(kThreads, 1)
+    fa2_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                   const __grid_constant__ CUtensorMap tmV, const Params p) {
+  using L = Layout<D>;
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  const uint32_t raw = smem_addr(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t* smem = smem_raw + (base - raw);
+
+  const uint32_t sQ = base;
+  const uint32_t sRing = base + L::kRingOffset;
+  const uint32_t bars = base + L::kBarOffset;
+  const uint32_t bar_q_full = bars;
+  const uint32_t bar_q_empty = bars + 8;
+  auto bar_full = [&](int s) { return bars + 16 + 8u * s; };
+  auto bar_empty = [&](int s) { return bars + 16 + 8u * (L::kStages + s); };
+  const uint32_t bar_s_full0 = bars + 16 + 16u * L::kStages;
+  const uint32_t bar_p_full0 = bar_s_full0 + 16;
+  const uint32_t bar_o_full0 = bar_p_full0 + 16;
+  const uint32_t bar_drain = bar_o_full0 + 16;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kMiscOffset);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kMiscOffset + 4);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    mbar_init(bar_q_full, 1);
+    mbar_init(bar_q_empty, 1);
+    for (int s = 0; s < L::kStages; ++s) {
+      mbar_init(bar_full(s), 1);
+      mbar_init(bar_empty(s), 1);
+    }
+    for (int t = 0; t < 2; ++t) {
+      mbar_init(bar_s_full0 + 8 * t, 1);
+      mbar_init(bar_p_full0 + 8 * t, 4 * 32);
+      mbar_init(bar_o_full0 + 8 * t, 1);
+    }
+    mbar_init(bar_drain, 1);
+    *abort_flag = 0;
+    mbar_init_fence();
+  }
+  if (warp == kMmaWarp) {
+    tmem_alloc(smem_addr(tmem_slot), kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+  const uint32_t tmem = *tmem_slot;
+
+  Watchdog wd;
+  wd.status = p.status;
+  wd.abort_flag = abort_flag;
+  wd.limit_ns = p.watchdog_ns;
+
+  if (warp == kLoadWarp) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      tma_prefetch_map(&tmQ);
+      tma_prefetch_map(&tmK);
+      tma_prefetch_map(&tmV);
+      const uint64_t keep = l2_policy_evict_last();    // K/V: re-read by every query tile of the head
+      const uint64_t stream_once = l2_policy_evict_first();  // Q: read once
+      uint32_t it = 0;
+      uint32_t q_round = 0;
+      bool ok = true;
+      for (int r = 0; ok; ++r) {
+        const int u = unit_of_round<kCausal>(r);
+        if (u >= p.num_units) break;
+        const Unit w = decode_unit<kCausal>(u, p);
+        if (q_round > 0 && !wait_bounded(bar_q_empty, (q_round - 1) & 1u, wd, kSiteLoadQEmpty)) {
+          ok = false;
+          break;
+        }
+        mbar_arrive_expect_tx(bar_q_full, L::kQBytes);
+        for (int t = 0; t < kSubTiles; ++t)
+          for (int pn = 0; pn < L::kPanels; ++pn)
+            tma_load_3d_hint(sQ + t * L::kTileBytes + pn * kPanelBytes, &tmQ, bar_q_full, pn * 64,
+                             w.q0 + t * kRows, w.bh, stream_once);
+        ++q_round;
+        for (int j = 0; j < w.nkv && ok; ++j) {
+          for (int kv = 0; kv < 2; ++kv) {
+            const int slot = it % L::kStages;
+            const uint32_t ph = (it / L::kStages) & 1u;
+            if (!wait_bounded(bar_empty(slot), ph ^ 1u, wd, kSiteLoadRingEmpty)) {
+              ok = false;
+              break;
+            }
+            mbar_arrive_expect_tx(bar_full(slot), L::kTileBytes);
+            const CUtensorMap* map = kv ? &tmV : &tmK;
+            for (int pn = 0; pn < L::kPanels; ++pn)
+              tma_load_3d_hint(sRing + slot * L::kTileBytes + pn * kPanelBytes, map, bar_full(slot),
+                               pn * 64, j * kKeys, w.bh, keep);
+            ++it;
+          }
+        }
+      }
+      // Drain: every copy issued must have landed before the CTA may exit.
+      const uint32_t first = it > (uint32_t)L::kStages ? it - L::kStages : 0u;
+      for (uint32_t i = first; i < it; ++i)
+        wait_bounded(bar_full(i % L::kStages), (i / L::kStages) & 1u, wd, kSiteDrain, false);
+      if (q_round > 0) wait_bounded(bar_q_full, (q_round - 1) & 1u, wd, kSiteDrain, false);
+    }
+    __syncwarp();
+  } else if (warp == kMmaWarp) {
+    // ----------------------------------------------------------- MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idesc_s = make_idesc_f16(kBf16, kKeys, false);
+      constexpr uint32_t idesc_o = make_idesc_f16(kBf16, D, true);
+      const uint32_t tS[2] = {tmem + 0u, tmem + (uint32_t)kKeys};
+      const uint32_t tO[2] = {tmem + L::kColO, tmem + L::kColO + (uint32_t)D};
+
+      // S_t = Q_t K^T : D/16 steps of K=16 along the head dimension.
+      auto issue_s = [&](int t, int slot) {
+        const uint32_t qa = sQ + t * L::kTileBytes;
+        const uint32_t ka = sRing + slot * L::kTileBytes;
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * kPanelBytes + (kk & 3) * 32;
+          mma_ss(tS[t], smem_desc_sw128(qa + off, 16, 1024), smem_desc_sw128(ka + off, 16, 1024),
+                 idesc_s, kk > 0 ? 1u : 0u);
+        }
+      };
+      // O_t (+)= P_t V : P from TMEM (16-bit pairs), V from shared memory (MN-major).
+      auto issue_pv = [&](int t, int slot, bool acc) {
+        const uint32_t va = sRing + slot * L::kTileBytes;
+#pragma unroll
+        for (int kk = 0; kk < kKeys / 16; ++kk) {
+          mma_ts(tO[t], tS[t] + kk * 8, smem_desc_sw128(va + kk * 16 * 128, kPanelBytes, 1024),
+                 idesc_o, (acc || kk > 0) ? 1u : 0u);
+        }
+      };
+
+      uint32_t it = 0, q_round = 0;
+      uint32_t p_phase[2] = {0u, 0u};
+      bool ok = true;
+      for (int r = 0; ok; ++r) {
+        const int u = unit_of_round<kCausal>(r);
+        if (u >= p.num_units) break;
+        const Unit w = decode_unit<kCausal>(u, p);
+        if (!wait_bounded(bar_q_full, q_round & 1u, wd, kSiteMmaQFull)) { ok = false; break; }
+        ++q_round;
+        int slot_k = it % L::kStages;
+        if (!wait_bounded(bar_full(slot_k), (it / L::kStages) & 1u, wd, kSiteMmaRingFull)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after_sync();
+        issue_s(0, slot_k);
+        mma_commit(bar_s_full0);
+        issue_s(1, slot_k);
+        mma_commit(bar_s_full0 + 8);
+        mma_commit(bar_empty(slot_k));
+        ++it;
+        if (w.nkv == 1) mma_commit(bar_q_empty);
+
+        for (int j = 0; j < w.nkv; ++j) {
+          const int slot_v = it % L::kStages;
+          if (!wait_bounded(bar_full(slot_v), (it / L::kStages) & 1u, wd, kSiteMmaRingFull)) {
+            ok = false;
+            break;
+          }
+          ++it;
+          const bool next = j + 1 < w.nkv;
+          if (next) {
+            slot_k = it % L::kStages;
+            if (!wait_bounded(bar_full(slot_k), (it / L::kStages) & 1u, wd, kSiteMmaRingFull)) {
+              ok = false;
+              break;
+            }
+          }
+#pragma unroll
+          for (int t = 0; t < 2; ++t) {
+            if (!wait_bounded(bar_p_full0 + 8 * t, p_phase[t], wd, kSiteMmaPFull)) {
+              ok = false;
+              break;
+            }
+            p_phase[t] ^= 1u;
+            tc_fence_after_sync();
+            issue_pv(t, slot_v, j > 0);
+            if (!next) mma_commit(bar_o_full0 + 8 * t);
+            if (t == 1) mma_commit(bar_empty(slot_v));
+            if (next) {
+              issue_s(t, slot_k);
+              mma_commit(bar_s_full0 + 8 * t);
+            }
+          }
+          if (!ok) break;
+          if (next) {
+            mma_commit(bar_empty(slot_k));
+            ++it;
+            if (j + 2 == w.nkv) mma_commit(bar_q_empty);
+          }
+        }
+      }
+      // Drain: all issued tensor-core work completes before TMEM is released.
+      mma_commit(bar_drain);
+      wait_bounded(bar_drain, 0u, wd, kSiteDrain, false);
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------- softmax warpgroups
+    const int t = warp >> 2;                 // sub-tile
+    const int wr = warp & 3;                 // warp within the warpgroup: TMEM lanes 32*wr..
+    const uint32_t lane_off = static_cast<uint32_t>(wr * 32) << 16;
+    const uint32_t tS = tmem + lane_off + (uint32_t)(t * kKeys);
+    const uint32_t tO = tmem + lane_off + L::kColO + (uint32_t)(t * D);
+    const uint32_t bar_s = bar_s_full0 + 8 * t;
+    const uint32_t bar_p = bar_p_full0 + 8 * t;
+    const uint32_t bar_o = bar_o_full0 + 8 * t;
+    const float c = p.scale_log2;
+    uint32_t s_phase = 0, o_phase = 0;
+    bool ok = true;
+    for (int r = 0; ok; ++r) {
+      const int u = unit_of_round<kCausal>(r);
+      if (u >= p.num_units) break;
+      const Unit w = decode_unit<kCausal>(u, p);
+      const int row = w.q0 + t * kRows + wr * 32 + lane;
+      const int limit = kCausal ? min(p.N, row + 1) : p.N;  // allowed keys: [0, limit)
+      float m_raw = -CUDART_INF_F;   // running max of raw scores
+      float m_base = -CUDART_INF_F;  // exponent base in log2 units (m_raw * c, or 0 while -inf)
+      float l = 0.f;
+      for (int j = 0; j < w.nkv; ++j) {
+        bool got = wait_bounded(bar_s, s_phase, wd, kSiteSoftmaxSFull);
+        got = __all_sync(0xffffffffu, got);
+        if (!got) { ok = false; break; }
+        s_phase ^= 1u;
+        tc_fence_after_sync();
+        uint32_t sr[128];
+        tmem_ld32x128_wait(tS, sr);
+        float s[128];
+#pragma unroll
+        for (int i = 0; i < 128; ++i) s[i] = __uint_as_float(sr[i]);
+        const int kv0 = j * kKeys;
+        if (kv0 + kKeys > limit) {  // ragged tail and/or causal diagonal: mask disallowed keys
+#pragma unroll
+          for (int i = 0; i < 128; ++i)
+            if (kv0 + i >= limit) s[i] = -CUDART_INF_F;
+        }
+        float mx0 = s[0], mx1 = s[1], mx2 = s[2], mx3 = s[3];
+#pragma unroll
+        for (int i = 4; i < 128; i += 4) {
+          mx0 = fmaxf(mx0, s[i]);
+          mx1 = fmaxf(mx1, s[i + 1]);
+          mx2 = fmaxf(mx2, s[i + 2]);
+          mx3 = fmaxf(mx3, s[i + 3]);
+        }
+        const float m_new = fmaxf(fmaxf(m_raw, fmaxf(mx0, mx1)), fmaxf(mx2, mx3));
+        const float base_new = (m_new == -CUDART_INF_F) ? 0.f : m_new * c;
+        float alpha = 1.f;
+        if (m_new > m_raw) alpha = ex2_approx(m_base - base_new);
+        // Rescale the running O only when some row's max moved (and O holds data).
+        if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+#pragma unroll
+          for (int cc = 0; cc < D; cc += 32) {
+            uint32_t o[32];
+            tmem_ld32x32_wait(tO + cc, o);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+            tmem_st32x32(tO + cc, o);
+          }
+        }
+        const float nb = -base_new;
+        float l0 = 0.f, l1 = 0.f, l2 = 0.f, l3 = 0.f;
+#pragma unroll
+        for (int i = 0; i < 128; i += 4) {
+          s[i] = ex2_approx(fmaf(s[i], c, nb));
+          s[i + 1] = ex2_approx(fmaf(s[i + 1], c, nb));
+          s[i + 2] = ex2_approx(fmaf(s[i + 2], c, nb));
+          s[i + 3] = ex2_approx(fmaf(s[i + 3], c, nb));
+          l0 += s[i];
+          l1 += s[i + 1];
+          l2 += s[i + 2];
+          l3 += s[i + 3];
+        }
+        l = l * alpha + ((l0 + l1) + (l2 + l3));
+        m_raw = m_new;
+        m_base = base_new;
+        // P (16-bit pairs) over the first 64 columns of this sub-tile's S region.
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          uint32_t pk[32];
+#pragma unroll
+          for (int i = 0; i < 32; ++i) pk[i] = pack2(s[64 * h + 2 * i], s[64 * h + 2 * i + 1], kBf16);
+          tmem_st32x32(tS + 32 * h, pk);
+        }
+        tmem_wait_st();
+        tc_fence_before_sync();
+        mbar_arrive(bar_p);
+      }
+      if (!ok) break;
+      // -------------------------------------------------------- epilogue
+      bool got = wait_bounded(bar_o, o_phase, wd, kSiteSoftmaxOFull);
+      got = __all_sync(0xffffffffu, got);
+      if (!got) break;
+      o_phase ^= 1u;
+      tc_fence_after_sync();
+      const float inv = (l > 0.f) ? __frcp_rn(l) : 0.f;
+      const bool live = row < p.N;
+      uint8_t* orow = reinterpret_cast<uint8_t*>(p.o) +
+                      (static_cast<size_t>(w.bh) * p.N + (live ? row : 0)) * (D * 2);
+#pragma unroll
+      for (int cc = 0; cc < D; cc += 32) {
+        uint32_t o[32];
+        tmem_ld32x32_wait(tO + cc, o);
+        uint32_t pk[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i)
+          pk[i] = pack2(__uint_as_float(o[2 * i]) * inv, __uint_as_float(o[2 * i + 1]) * inv, kBf16);
+        if (live) {
+          uint4* dst = reinterpret_cast<uint4*>(orow + cc * 2);
+#pragma unroll
+          for (int q = 0; q < 4; ++q) dst[q] = make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+        }
+      }
+      if (live) {
+        p.lse[static_cast<size_t>(w.bh) * p.N + row] =
+            (l > 0.f) ? (m_base + __log2f(l)) * 0.69314718055994530942f : CUDART_INF_F;
+      }
+      // O_t is read out; the next unit's first P.V may overwrite it once this
+      // warpgroup publishes that unit's first P (ordered by bar_p).
+      tc_fence_before_sync();
+    }
+  }
+
+  tc_fence_before_sync();
+  __syncthreads();
+  if (warp == kMmaWarp) {
+    tc_fence_after_sync();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+template <int D, bool kBf16, bool kCausal>
+cudaError_t launch_fwd(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v, const Params& p,
+                       int grid, cudaStream_t stream) {
+  auto kern = fa2_fwd_kernel<D, kBf16, kCausal>;
+  const int smem = Layout<D>::kSmemBytes;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  kern<<<grid, kThreads, smem, stream>>>(q, k, v, p);
+  return cudaGetLastError();
+}
+
+}  // namespace fa2

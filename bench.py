@@ -1,0 +1,406 @@
+#!/usr/bin/env python3
+"""Benchmark of the GB300 FlashAttention-2 forward (one JSON line on stdout).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl gb300|reference]
+
+A step is one forward pass (one kernel launch) over the workload's [B,H,N,D]
+inputs, already resident in HBM. Timing uses CUDA events on the launching
+stream around exactly K steps, bracketed by a barrier and a device
+synchronise; the inputs rotate over enough copies that one pass over all of
+them is larger than twice the L2 cache, so no step finds its inputs in L2
+from the step before. Under torchrun each rank runs the same workload on its
+own GPU (weak scaling, no collective on the data path) and the slowest rank's
+time is reported.
+
+Metric: attention forward TFLOP/s = 4*B*H*N^2*D (halved when causal) / time.
+`--impl reference` times the CPU fp64 oracle (this path's reference
+implementation) on a bounded sample of the same workload instead.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import workloads  # noqa: E402
+
+METRIC = "attention forward TFLOPS (4·B·H·N²·D) and % of GB300 dense fp16/bf16 peak"
+UNIT = "TFLOP/s"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "traffic.json")
+KERNEL_SOURCES = os.path.join(ROOT, "attention_forward_03_gb300", "csrc")
+
+
+# ------------------------------------------------------------------ helpers
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for f in sorted(os.listdir(KERNEL_SOURCES)):
+        if f.endswith((".cu", ".cuh", ".h")):
+            with open(os.path.join(KERNEL_SOURCES, f), "rb") as fh:
+                h.update(f.encode() + b"\0" + fh.read())
+    return h.hexdigest()[:16]
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as fh:
+            p = json.load(fh)
+        return p, "measured"
+    except (OSError, ValueError):
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def traffic_per_launch(workload_name: str):
+    """DRAM bytes per launch from a committed ncu capture, if it matches the current kernel source."""
+    try:
+        with open(PROFILE_TRAFFIC) as fh:
+            t = json.load(fh)
+    except (OSError, ValueError):
+        return None
+    entry = t.get(workload_name)
+    if not entry or entry.get("kernel_source_hash") != kernel_source_hash():
+        return None
+    return entry.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons while the GPU is under load."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.dev = device_index
+        self.proc = None
+        self.lines = []
+        self.t_start = None
+        self.t_stop = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.dev), f"--query-gpu={self.QUERY}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self._reader = threading.Thread(target=self._read, daemon=True)
+        self._reader.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append((time.time(), line.strip()))
+
+    def mark_start(self):
+        self.t_start = time.time()
+
+    def mark_stop(self):
+        self.t_stop = time.time()
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self._reader.join(timeout=2)
+        rows = []
+        for ts, line in self.lines:
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                rows.append((ts, float(parts[1]), float(parts[2]), parts[4:]))
+            except ValueError:
+                continue
+        if not rows:
+            return None
+        inside = [r for r in rows if self.t_start and self.t_stop and self.t_start <= r[0] <= self.t_stop]
+        used = inside if inside else rows
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = set()
+        for r in used:
+            for name, flag in zip(names, r[3][1:]):
+                if flag.lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(r[1] for r in used), "sm_max_mhz": max(r[2] for r in used),
+                "reasons": sorted(reasons), "samples": len(used),
+                "window": "timed region" if inside else "warm-up and timed region"}
+
+
+# ------------------------------------------------------------- distributed
+def dist_setup():
+    """Return (rank, world, local_rank). Initialises torch.distributed under torchrun."""
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if backend == "nccl":
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+    return rank, world, local
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x: float, world: int, device=None) -> float:
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_tflops(flops_per_step: float, steps: int, world: int, max_seconds: float) -> float:
+    """Weak scaling: every rank runs the whole workload; the job finishes with the slowest rank."""
+    return flops_per_step * steps * world / max_seconds / 1e12
+
+
+# ------------------------------------------------------------- CPU oracle leg
+def oracle_sample(w: workloads.Workload, target_seconds: float, inputs=None):
+    """Time the fp64 oracle on a bounded sample of the workload's rows (one head).
+
+    Returns (tflops, seconds, rows, threads, description)."""
+    import numpy as np
+
+    import oracle
+    q, k, v = inputs if inputs is not None else workloads.make_inputs(
+        workloads.custom(1, 1, w.N, w.D, w.dtype, w.causal, w.seed, w.sigma_qk, w.sigma_v))
+    threads = oracle.default_threads()
+    N = w.N
+
+    def row_flops(rows):
+        if not w.causal:
+            return 4.0 * w.D * N * len(rows)
+        return float(sum(4.0 * w.D * (min(N, int(i) + 1)) for i in rows))
+
+    # calibrate on a small slice, then size the sample to the time budget
+    rng = np.random.default_rng(0)
+    probe = np.sort(rng.choice(N, size=min(N, 2 * threads), replace=False))
+    t0 = time.perf_counter()
+    oracle.attention_fwd(q[:1, :1], k[:1, :1], v[:1, :1], w.scale, w.causal, rows=probe, nthreads=threads)
+    dt = max(time.perf_counter() - t0, 1e-4)
+    rate = row_flops(probe) / dt
+    want_rows = int(min(N, max(threads, target_seconds * rate / max(row_flops([N // 2]), 1.0))))
+    rows = np.sort(rng.choice(N, size=want_rows, replace=False))
+    t0 = time.perf_counter()
+    oracle.attention_fwd(q[:1, :1], k[:1, :1], v[:1, :1], w.scale, w.causal, rows=rows, nthreads=threads)
+    secs = time.perf_counter() - t0
+    desc = (f"{len(rows)} query rows of one head of {w.describe()} "
+            f"(full key range of each row), fp64, {threads} threads")
+    return row_flops(rows) / secs / 1e12, secs, len(rows), threads, desc
+
+
+# -------------------------------------------------------------------- arms
+def run_reference(args, w, rank, world):
+    if rank != 0:
+        return None
+    import numpy as np  # noqa: F401
+    per_step = max(1.0, args.reference_seconds / max(1, args.steps + args.warmup))
+    small = workloads.custom(1, 1, w.N, w.D, w.dtype, w.causal, w.seed, w.sigma_qk, w.sigma_v)
+    inputs = workloads.make_inputs(small)
+    for _ in range(args.warmup):
+        oracle_sample(w, per_step, inputs)
+    vals, secs = [], []
+    desc, threads = "", 1
+    for _ in range(args.steps):
+        tf, s, rows, threads, desc = oracle_sample(w, per_step, inputs)
+        vals.append(tf)
+        secs.append(s)
+    value = statistics.median(vals)
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * statistics.median(secs),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded N(0, sigma^2) inputs, cast to the workload's 16-bit dtype)",
+        "config": {"workload": w.describe(), "B": w.B, "H": w.H, "N": w.N, "D": w.D, "causal": w.causal,
+                   "input_dtype": w.dtype, "l2": "host CPU run; no GPU L2 involved"},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle", "sample": desc},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    return line
+
+
+def run_gb300(args, w, rank, world, local):
+    import torch
+
+    import attention_forward_03_gb300 as fa2
+    if not torch.cuda.is_available():
+        raise RuntimeError("the gb300 arm needs a CUDA device")
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    fa2.library()
+    stream = torch.cuda.current_stream(dev)
+
+    q, k, v = workloads.make_inputs(w)
+    set_bytes = workloads.algorithmic_bytes(w)
+    l2 = getattr(torch.cuda.get_device_properties(dev), "L2_cache_size", 128 * 2 ** 20)
+    nsets = max(2, math.ceil(2 * l2 / set_bytes))
+    sets = []
+    for _ in range(nsets):
+        sets.append((q.to(dev), k.to(dev), v.to(dev), torch.empty_like(q, device=dev),
+                     torch.empty((w.B, w.H, w.N), dtype=torch.float32, device=dev)))
+    torch.cuda.synchronize(dev)
+
+    def step(i):
+        qd, kd, vd, od, ld = sets[i % nsets]
+        fa2.attention_forward(qd, kd, vd, scale=w.scale, is_causal=w.causal, out=od, lse=ld, stream=stream)
+
+    clocks = ClockSampler(local)
+    clocks.start()
+    for i in range(args.warmup):
+        step(i)
+    torch.cuda.synchronize(dev)
+    # keep the GPU busy for ~1 s before the timed region so clocks settle and get sampled
+    t0 = time.perf_counter()
+    i = 0
+    while time.perf_counter() - t0 < args.settle_seconds:
+        step(i)
+        i += 1
+        if i % 16 == 0:
+            torch.cuda.synchronize(dev)
+    torch.cuda.synchronize(dev)
+    fa2.fa2_device_status(clear=True)
+
+    ev0 = torch.cuda.Event(enable_timing=True)
+    ev1 = torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    clocks.mark_start()
+    ev0.record(stream)
+    for i in range(args.steps):
+        step(i)
+    ev1.record(stream)
+    torch.cuda.synchronize(dev)
+    clocks.mark_stop()
+    barrier(world)
+    elapsed = ev0.elapsed_time(ev1) / 1e3
+    clock_info = clocks.stop()
+    status = fa2.fa2_device_status(clear=True)
+    if status != 0:
+        raise RuntimeError(f"device watchdog fired during the timed region (code {status})")
+    t_max = max_over_ranks(elapsed, world, dev)
+    flops = workloads.flops(w)
+    value = whole_job_tflops(flops, args.steps, world, t_max)
+    per_launch = elapsed / args.steps
+
+    # end to end through the public API, host buffers in pinned memory
+    qh, kh, vh = (t.pin_memory() for t in (q, k, v))
+    oh = torch.empty_like(q).pin_memory()
+    lh = torch.empty((w.B, w.H, w.N), dtype=torch.float32).pin_memory()
+    qd, kd, vd, od, ld = sets[0]
+
+    def e2e_step():
+        qd.copy_(qh, non_blocking=True)
+        kd.copy_(kh, non_blocking=True)
+        vd.copy_(vh, non_blocking=True)
+        fa2.attention_forward(qd, kd, vd, scale=w.scale, is_causal=w.causal, out=od, lse=ld, stream=stream)
+        oh.copy_(od, non_blocking=True)
+        lh.copy_(ld, non_blocking=True)
+
+    for _ in range(2):
+        e2e_step()
+    torch.cuda.synchronize(dev)
+    e2e_steps = max(3, min(args.steps, 50))
+    barrier(world)
+    ev0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    ev1.record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_elapsed = max_over_ranks(ev0.elapsed_time(ev1) / 1e3, world, dev)
+    e2e_value = whole_job_tflops(flops, e2e_steps, world, e2e_elapsed)
+    h2d = 3 * q.numel() * q.element_size()
+    d2h = oh.numel() * oh.element_size() + lh.numel() * 4
+
+    if rank != 0:
+        return None
+    peaks, peak_src = load_peaks()
+    peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    achieved = flops / per_launch / 1e12
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": 1e3 * t_max / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": w.dtype,
+        "data": "synthetic (seeded N(0, sigma^2) inputs, cast to the workload's 16-bit dtype)",
+        "config": {"workload": w.describe(), "B": w.B, "H": w.H, "N": w.N, "D": w.D, "causal": w.causal,
+                   "scale": "1/sqrt(D)", "parallelism": f"weak x{world} (one independent replica per GPU)",
+                   "l2": f"inputs rotate over {nsets} copies ({nsets * set_bytes / 2**20:.0f} MiB > 2x L2)"},
+        "pct_of_peak": 100.0 * achieved / peak,
+        "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                     "frac": achieved / peak, "peak_source": f"{peak_src} bf16 dense (burst)",
+                     "traffic": traffic_per_launch(w.name),
+                     "algorithmic_bytes": workloads.algorithmic_bytes(w),
+                     "achieved_hbm_gbs": workloads.algorithmic_bytes(w) / per_launch / 1e9},
+        "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": args.steps,
+        "clocks": clock_info,
+    }
+    if not args.no_cpu_baseline:
+        tf, secs, rows, threads, desc = oracle_sample(w, args.cpu_seconds)
+        line["cpu_baseline"] = {"value": tf, "unit": UNIT, "cores": threads, "kind": "oracle", "sample": desc,
+                                "seconds": secs}
+    return line
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--workload", default="target", choices=sorted(workloads.WORKLOADS))
+    ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--settle-seconds", type=float, default=1.0)
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--reference-seconds", type=float, default=120.0,
+                    help="total CPU time budget of the reference arm")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    w = workloads.WORKLOADS[args.workload]
+    if args.impl == "reference":
+        # the CPU oracle runs on rank 0 only; other ranks exit without work
+        rank, world = int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1"))
+        line = run_reference(args, w, rank, world)
+        if line is not None:
+            print(json.dumps(line), flush=True)
+        return
+    rank, world, local = dist_setup()
+    if world != args.gpus and rank == 0:
+        print(f"note: --gpus {args.gpus} but WORLD_SIZE {world}", file=sys.stderr)
+    line = run_gb300(args, w, rank, world, local)
+    if rank == 0 and line is not None:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

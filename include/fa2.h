@@ -1,0 +1,108 @@
+/*
+ * fa2.h — C ABI of the GB300 (sm_103a) FlashAttention-2 forward library.
+ *
+ * The operation (FlashAttention-2 forward):
+ *   for every batch b, head h and query row i of an N-long sequence,
+ *     S_ij = scale * <Q[b,h,i,:], K[b,h,j,:]>      over the allowed keys j
+ *     O[b,h,i,:] = softmax_j(S_ij) V[b,h,j,:]
+ *     LSE[b,h,i] = ln sum_j exp(S_ij)              (natural log)
+ *   Allowed keys: 0 <= j < N, and j <= i when is_causal != 0 (top-left
+ *   aligned, query and key sequences have the same length N).
+ * Definition and the statistics kept: "FlashAttention-2 MMA 代码学习"
+ * (chuoer47 blog), step 0 (O = softmax(QK^T/sqrt(d)) V) and step 1 (the
+ * row-wise (m, l) merge); the yangyitao.com CUDA book, ch. 15, section 15.1
+ * (LSE = m + log l is the one statistic kept for the backward pass) and
+ * section 15.3 (the kernel signature Q, K, V, O, LSE, N, H, softmax_scale,
+ * is_causal; scale applied before the max; causal masking of col > row;
+ * padded columns >= N masked; rows >= N not written; an all-masked row
+ * gives O = 0 and LSE = +inf, which the masks supported here never produce).
+ *
+ * All entry points are thread-safe and may be called from several host
+ * threads at once.
+ */
+#ifndef FA2_GB300_H
+#define FA2_GB300_H
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+struct CUstream_st; /* the same type as cudaStream_t / CUstream */
+
+/* dtype codes */
+#define FA2_F16 0  /* IEEE binary16 inputs and output */
+#define FA2_BF16 1 /* bfloat16 inputs and output      */
+
+/* status codes (0 = success, negative = error) */
+#define FA2_OK 0
+#define FA2_ERR_INVALID_ARG (-1) /* null pointer, negative size, bad scale, overlapping O/LSE/inputs, size overflow */
+#define FA2_ERR_UNSUPPORTED (-2) /* head dim not 64 or 128, unknown dtype, device is not sm_103 */
+#define FA2_ERR_ALIGN (-3)       /* a tensor pointer is not 16-byte aligned */
+#define FA2_ERR_CUDA (-4)        /* a CUDA runtime/driver call failed (see fa2_last_cuda_error) */
+#define FA2_ERR_TIMEOUT (-5)     /* the device watchdog fired (reported by fa2_device_status) */
+
+/*
+ * fa2_fwd — enqueue the forward pass on `stream`.
+ *
+ * Q, K, V : device pointers, contiguous [B, H, N, D] tensors of `dtype`
+ *           (row-major, D fastest). Read only. 16-byte aligned.
+ * O       : device pointer, contiguous [B, H, N, D] of `dtype`. Fully
+ *           overwritten with the normalised output, rounded to nearest-even.
+ *           Must not overlap Q, K, V or LSE.
+ * LSE     : device pointer, contiguous [B, H, N] fp32. Fully overwritten with
+ *           the natural-log logsumexp of each row's scaled scores. 16-byte
+ *           aligned; must not overlap Q, K, V or O.
+ * B, H, N : batch, heads, sequence length (queries and keys), each >= 0. If
+ *           any is 0 the call does nothing and returns FA2_OK (pointers may
+ *           then be NULL).
+ * D       : head dimension; 64 or 128.
+ * scale   : multiplier on Q.K; finite and > 0 (the usual value is 1/sqrt(D)).
+ * is_causal: nonzero keeps only keys j <= i for query i.
+ * dtype   : FA2_F16 or FA2_BF16.
+ * stream  : CUDA stream (NULL = legacy default stream) of the current device;
+ *           all pointers must be device memory of that device.
+ *
+ * Ownership: the caller owns every buffer; the library never allocates,
+ * frees or retains them. Asynchronous: a return of FA2_OK means the kernel
+ * was enqueued, not that it finished; errors inside the kernel surface as a
+ * CUDA error on the stream or through fa2_device_status. Host-side argument
+ * errors are detected before anything is enqueued and leave O and LSE
+ * untouched.
+ */
+int fa2_fwd(const void* Q, const void* K, const void* V, void* O, float* LSE,
+            int B, int H, int N, int D, float scale, int is_causal, int dtype,
+            struct CUstream_st* stream);
+
+/*
+ * fa2_device_status — read the device-side watchdog word of the current
+ * device, synchronising `stream` first. *status receives 0 when no kernel of
+ * this library has timed out waiting on one of its internal barriers since
+ * the last clear, else a positive code identifying the wait that gave up.
+ * If `clear` is nonzero the word is reset to 0 afterwards. Returns FA2_OK,
+ * FA2_ERR_INVALID_ARG (status NULL) or FA2_ERR_CUDA.
+ */
+int fa2_device_status(struct CUstream_st* stream, int* status, int clear);
+
+/*
+ * fa2_set_watchdog_ns — set the time (in nanoseconds) a kernel waits on any
+ * one internal barrier before it records a timeout in the watchdog word and
+ * winds down. Applies to launches made after the call, process-wide. 0
+ * restores the default (1 s). Returns FA2_OK.
+ */
+int fa2_set_watchdog_ns(unsigned long long ns);
+
+/* Human-readable text for a status code (static storage, never NULL). */
+const char* fa2_error_string(int code);
+
+/* Text of the last CUDA error seen by this library on the calling thread
+ * (static thread-local storage, never NULL; "" if none). */
+const char* fa2_last_cuda_error(void);
+
+/* Library ABI version: (major << 16) | minor. */
+int fa2_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FA2_GB300_H */

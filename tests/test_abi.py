@@ -1,0 +1,121 @@
+"""Host-side checks of the C ABI: the library loads, exports what include/fa2.h
+declares, and rejects bad arguments before touching a GPU. No kernel runs here."""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+
+import pytest
+import torch
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "fa2.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from attention_forward_03_gb300 import build
+    build.build()
+    from attention_forward_03_gb300 import binding
+    return binding
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(fa2_[a-z_]+)\s*\(", text)))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    assert "fa2_fwd" in names and "fa2_device_status" in names
+    assert len(names) >= 6
+
+
+def test_every_declared_symbol_is_exported(lib):
+    so = ctypes.CDLL(lib.LIB_PATH)
+    for name in declared_functions():
+        assert hasattr(so, name), f"{name} declared in fa2.h but not exported"
+    assert set(declared_functions()) == set(lib.SIGNATURES), "binding signatures out of sync with fa2.h"
+
+
+def test_codes_match_header(lib):
+    text = open(HEADER).read()
+    for name in ("FA2_F16", "FA2_BF16", "FA2_OK", "FA2_ERR_INVALID_ARG", "FA2_ERR_UNSUPPORTED",
+                 "FA2_ERR_ALIGN", "FA2_ERR_CUDA", "FA2_ERR_TIMEOUT"):
+        m = re.search(rf"#define {name} \(?(-?\d+)\)?", text)
+        assert m and int(m.group(1)) == getattr(lib, name), name
+
+
+def test_version_and_strings(lib):
+    assert lib.fa2_version() >> 16 == 1
+    for code in (0, -1, -2, -3, -4, -5, 17):
+        assert isinstance(lib.library().fa2_error_string(code), bytes)
+    assert lib.library().fa2_last_cuda_error() is not None
+    lib.fa2_set_watchdog_ns(0)
+
+
+A = 0x10000  # 16-byte aligned fake addresses, far apart; never dereferenced by these tests
+GOOD = dict(Q=A, K=A * 16, V=A * 32, O=A * 48, LSE=A * 64, B=1, H=2, N=64, D=64, scale=0.125, is_causal=0,
+            dtype=0, stream=None)
+
+
+def call(lib, **over):
+    a = dict(GOOD)
+    a.update(over)
+    return lib.fa2_fwd(a["Q"], a["K"], a["V"], a["O"], a["LSE"], a["B"], a["H"], a["N"], a["D"], a["scale"],
+                       a["is_causal"], a["dtype"], a["stream"])
+
+
+@pytest.mark.parametrize("over,code", [
+    (dict(B=-1), -1), (dict(H=-3), -1), (dict(N=-1), -1),
+    (dict(D=96), -2), (dict(D=256), -2), (dict(D=0), -2),
+    (dict(dtype=2), -2), (dict(dtype=-1), -2),
+    (dict(scale=0.0), -1), (dict(scale=-0.5), -1), (dict(scale=float("nan")), -1), (dict(scale=float("inf")), -1),
+    (dict(Q=None), -1), (dict(K=None), -1), (dict(V=None), -1), (dict(O=None), -1), (dict(LSE=None), -1),
+    (dict(Q=A + 8), -3), (dict(V=A * 32 + 2), -3), (dict(O=A * 48 + 4), -3), (dict(LSE=A * 64 + 12), -3),
+    (dict(O=A + 64), -1),            # O overlaps Q
+    (dict(LSE=A * 48 + 128), -1),    # LSE overlaps O
+    (dict(B=1 << 16, H=1 << 16), -1),  # B*H overflows int32
+])
+def test_bad_arguments_are_rejected_before_any_gpu_work(lib, over, code):
+    assert call(lib, **over) == code
+
+
+@pytest.mark.parametrize("over", [dict(B=0), dict(H=0), dict(N=0),
+                                  dict(B=0, Q=None, K=None, V=None, O=None, LSE=None)])
+def test_empty_problem_is_a_no_op(lib, over):
+    assert call(lib, **over) == lib.FA2_OK
+
+
+@pytest.mark.skipif(torch.cuda.is_available(), reason="only meaningful on a host without a GPU")
+def test_valid_call_without_a_gpu_fails_loudly(lib):
+    assert call(lib) == lib.FA2_ERR_CUDA
+    assert lib.library().fa2_last_cuda_error().decode() != ""
+    with pytest.raises(lib.Fa2Error):
+        lib._check(call(lib), "fa2_fwd")
+
+
+def test_binding_refuses_cpu_tensors(lib):
+    q = torch.zeros(1, 1, 8, 64, dtype=torch.float16)
+    with pytest.raises(ValueError):
+        lib.attention_forward(q, q, q)
+
+
+def test_missing_library_raises(lib, monkeypatch, tmp_path):
+    import attention_forward_03_gb300.binding as b
+    monkeypatch.setattr(b, "_lib", None)
+    monkeypatch.setattr(b, "LIB_PATH", str(tmp_path / "missing.so"))
+    with pytest.raises(ImportError):
+        b.library()
+
+
+def test_product_never_imports_the_oracle():
+    pkg = os.path.join(ROOT, "attention_forward_03_gb300")
+    for dirpath, _, files in os.walk(pkg):
+        for f in files:
+            if f.endswith((".py", ".cu", ".cuh", ".h")):
+                text = open(os.path.join(dirpath, f), encoding="utf-8").read()
+                assert not re.search(r"^\s*(import|from)\s+oracle\b", text, flags=re.M), f
+                assert "fa2_oracle" not in text, f
