@@ -183,37 +183,43 @@ def whole_job_tflops(flops_per_step: float, steps: int, world: int, max_seconds:
 
 # ------------------------------------------------------------- CPU oracle leg
 def oracle_sample(w: workloads.Workload, target_seconds: float, inputs=None):
-    """Time the fp64 oracle on a bounded sample of the workload's rows (one head).
+    """Time the fp64 oracle on a bounded sample of the workload's rows.
 
+    The sample is a uniform random subset of all B*H*N query rows (each row
+    over its full allowed key range), sized from a short calibration run so
+    that it takes about `target_seconds`; if the whole workload fits in that
+    time, the sample is the whole workload.
     Returns (tflops, seconds, rows, threads, description)."""
     import numpy as np
 
     import oracle
-    q, k, v = inputs if inputs is not None else workloads.make_inputs(
-        workloads.custom(1, 1, w.N, w.D, w.dtype, w.causal, w.seed, w.sigma_qk, w.sigma_v))
+    q, k, v = inputs if inputs is not None else workloads.make_inputs(w)
     threads = oracle.default_threads()
     N = w.N
+    total = w.B * w.H * N
 
     def row_flops(rows):
+        rows = np.asarray(rows)
         if not w.causal:
             return 4.0 * w.D * N * len(rows)
-        return float(sum(4.0 * w.D * (min(N, int(i) + 1)) for i in rows))
+        return float(np.sum(4.0 * w.D * np.minimum(N, rows % N + 1)))
 
-    # calibrate on a small slice, then size the sample to the time budget
     rng = np.random.default_rng(0)
-    probe = np.sort(rng.choice(N, size=min(N, 2 * threads), replace=False))
+    probe = np.sort(rng.choice(total, size=min(total, 2 * threads), replace=False))
     t0 = time.perf_counter()
-    oracle.attention_fwd(q[:1, :1], k[:1, :1], v[:1, :1], w.scale, w.causal, rows=probe, nthreads=threads)
-    dt = max(time.perf_counter() - t0, 1e-4)
-    rate = row_flops(probe) / dt
-    want_rows = int(min(N, max(threads, target_seconds * rate / max(row_flops([N // 2]), 1.0))))
-    rows = np.sort(rng.choice(N, size=want_rows, replace=False))
+    oracle.attention_fwd(q, k, v, w.scale, w.causal, rows=probe, nthreads=threads)
+    rate = row_flops(probe) / max(time.perf_counter() - t0, 1e-4)
+    per_row = workloads.flops(w) / total
+    want = int(min(total, max(threads, target_seconds * rate / per_row)))
+    rows = np.sort(rng.choice(total, size=want, replace=False)) if want < total else None
     t0 = time.perf_counter()
-    oracle.attention_fwd(q[:1, :1], k[:1, :1], v[:1, :1], w.scale, w.causal, rows=rows, nthreads=threads)
+    oracle.attention_fwd(q, k, v, w.scale, w.causal, rows=rows, nthreads=threads)
     secs = time.perf_counter() - t0
-    desc = (f"{len(rows)} query rows of one head of {w.describe()} "
-            f"(full key range of each row), fp64, {threads} threads")
-    return row_flops(rows) / secs / 1e12, secs, len(rows), threads, desc
+    n = total if rows is None else len(rows)
+    fl = workloads.flops(w) if rows is None else row_flops(rows)
+    what = "the whole workload" if rows is None else f"{n} of its {total} query rows, drawn uniformly"
+    desc = f"{what} ({w.describe()}, each row over its full allowed key range), fp64, {threads} threads"
+    return fl / secs / 1e12, secs, n, threads, desc
 
 
 # -------------------------------------------------------------------- arms
@@ -222,8 +228,7 @@ def run_reference(args, w, rank, world):
         return None
     import numpy as np  # noqa: F401
     per_step = max(1.0, args.reference_seconds / max(1, args.steps + args.warmup))
-    small = workloads.custom(1, 1, w.N, w.D, w.dtype, w.causal, w.seed, w.sigma_qk, w.sigma_v)
-    inputs = workloads.make_inputs(small)
+    inputs = workloads.make_inputs(w)
     for _ in range(args.warmup):
         oracle_sample(w, per_step, inputs)
     vals, secs = [], []
