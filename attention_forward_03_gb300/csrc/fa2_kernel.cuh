@@ -53,6 +53,10 @@ constexpr int kMmaWarp = 8;
 constexpr int kLoadWarp = 9;
 constexpr int kPanelBytes = 128 * 128;  // 128 rows x 64 16-bit elements
 constexpr uint32_t kTmemCols = 512;
+// The exponent base of a row moves only when its max exceeds the base by more
+// than this many powers of two (so p <= 2^8 = 256, exact in the 16-bit P and
+// far from overflow in the fp32 sums).
+constexpr float kRescaleLog2 = 8.0f;
 
 // Watchdog codes written to the status word (site of the wait that gave up).
 enum : int {
@@ -74,8 +78,8 @@ struct Layout {
   static constexpr int kQBytes = kSubTiles * kTileBytes;
   static constexpr int kRingOffset = kQBytes;
   static constexpr int kBarOffset = kRingOffset + kStages * kTileBytes;
-  // barriers: q_full, q_empty, ring full[S], ring empty[S], s_full[2], p_full[2], o_full[2], drain
-  static constexpr int kNumBars = 2 + 2 * kStages + 6 + 1;
+  // barriers: q_full, q_empty, ring full[S], ring empty[S], s_full[2], p_full[2][2 halves], o_full[2], drain
+  static constexpr int kNumBars = 2 + 2 * kStages + 8 + 1;
   static constexpr int kMiscOffset = kBarOffset + kNumBars * 8;
   static constexpr int kSmemBytes = kMiscOffset + 16 + 1024;  // + slack for 1 KB alignment
   static constexpr uint32_t kColO = 2 * kKeys;                 // O0 at 256, O1 at 256 + D
@@ -141,6 +145,10 @@ __device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, cons
   }
 }
 
+__device__ __forceinline__ float round16(float x, bool bf16) {
+  return bf16 ? __bfloat162float(__float2bfloat16_rn(x)) : __half2float(__float2half_rn(x));
+}
+
 __device__ __forceinline__ uint32_t pack2(float lo, float hi, bool bf16) {
   if (bf16) {
     __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
@@ -169,8 +177,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto bar_full = [&](int s) { return bars + 16 + 8u * s; };
   auto bar_empty = [&](int s) { return bars + 16 + 8u * (L::kStages + s); };
   const uint32_t bar_s_full0 = bars + 16 + 16u * L::kStages;
-  const uint32_t bar_p_full0 = bar_s_full0 + 16;
-  const uint32_t bar_o_full0 = bar_p_full0 + 16;
+  const uint32_t bar_p_full0 = bar_s_full0 + 16;  // [sub-tile][half] at + 16*t + 8*h
+  const uint32_t bar_o_full0 = bar_p_full0 + 32;
   const uint32_t bar_drain = bar_o_full0 + 16;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kMiscOffset);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kMiscOffset + 4);
@@ -187,7 +195,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int t = 0; t < 2; ++t) {
       mbar_init(bar_s_full0 + 8 * t, 1);
-      mbar_init(bar_p_full0 + 8 * t, 4 * 32);
+      mbar_init(bar_p_full0 + 16 * t, 4 * 32);
+      mbar_init(bar_p_full0 + 16 * t + 8, 4 * 32);
       mbar_init(bar_o_full0 + 8 * t, 1);
     }
     mbar_init(bar_drain, 1);
@@ -276,18 +285,20 @@ __global__ void __launch_bounds__(kThreads, 1)
                  idesc_s, kk > 0 ? 1u : 0u);
         }
       };
-      // O_t (+)= P_t V : P from TMEM (16-bit pairs), V from shared memory (MN-major).
-      auto issue_pv = [&](int t, int slot, bool acc) {
+      // O_t (+)= P_t V over keys [64h, 64h+64): P from TMEM (16-bit pairs), V from
+      // shared memory (MN-major).
+      auto issue_pv_half = [&](int t, int slot, int h, bool acc) {
         const uint32_t va = sRing + slot * L::kTileBytes;
 #pragma unroll
-        for (int kk = 0; kk < kKeys / 16; ++kk) {
+        for (int k4 = 0; k4 < kKeys / 32; ++k4) {
+          const int kk = h * (kKeys / 32) + k4;
           mma_ts(tO[t], tS[t] + kk * 8, smem_desc_sw128(va + kk * 16 * 128, kPanelBytes, 1024),
                  idesc_o, (acc || kk > 0) ? 1u : 0u);
         }
       };
 
       uint32_t it = 0, q_round = 0;
-      uint32_t p_phase[2] = {0u, 0u};
+      uint32_t p_phase[2] = {0u, 0u};  // both halves of a sub-tile flip together
       bool ok = true;
       for (int r = 0; ok; ++r) {
         const int u = unit_of_round<kCausal>(r);
@@ -326,13 +337,19 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
 #pragma unroll
           for (int t = 0; t < 2; ++t) {
-            if (!wait_bounded(bar_p_full0 + 8 * t, p_phase[t], wd, kSiteMmaPFull)) {
+            if (!wait_bounded(bar_p_full0 + 16 * t, p_phase[t], wd, kSiteMmaPFull)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after_sync();
+            issue_pv_half(t, slot_v, 0, j > 0);
+            if (!wait_bounded(bar_p_full0 + 16 * t + 8, p_phase[t], wd, kSiteMmaPFull)) {
               ok = false;
               break;
             }
             p_phase[t] ^= 1u;
             tc_fence_after_sync();
-            issue_pv(t, slot_v, j > 0);
+            issue_pv_half(t, slot_v, 1, true);
             if (!next) mma_commit(bar_o_full0 + 8 * t);
             if (t == 1) mma_commit(bar_empty(slot_v));
             if (next) {
@@ -361,7 +378,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tS = tmem + lane_off + (uint32_t)(t * kKeys);
     const uint32_t tO = tmem + lane_off + L::kColO + (uint32_t)(t * D);
     const uint32_t bar_s = bar_s_full0 + 8 * t;
-    const uint32_t bar_p = bar_p_full0 + 8 * t;
+    const uint32_t bar_p = bar_p_full0 + 16 * t;  // + 8 for the second half
     const uint32_t bar_o = bar_o_full0 + 8 * t;
     const float c = p.scale_log2;
     uint32_t s_phase = 0, o_phase = 0;
@@ -372,9 +389,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       const Unit w = decode_unit<kCausal>(u, p);
       const int row = w.q0 + t * kRows + wr * 32 + lane;
       const int limit = kCausal ? min(p.N, row + 1) : p.N;  // allowed keys: [0, limit)
-      float m_raw = -CUDART_INF_F;   // running max of raw scores
-      float m_base = -CUDART_INF_F;  // exponent base in log2 units (m_raw * c, or 0 while -inf)
-      float l = 0.f;
+      float m_raw = -CUDART_INF_F;  // running max of the raw scores seen so far
+      float base = -CUDART_INF_F;   // exponent base (log2 units) that l and O are relative to
+      float l = 0.f;    // sum of p (unrounded): LSE
+      float l_o = 0.f;  // normaliser of O (see below)
       for (int j = 0; j < w.nkv; ++j) {
         bool got = wait_bounded(bar_s, s_phase, wd, kSiteSoftmaxSFull);
         got = __all_sync(0xffffffffu, got);
@@ -392,19 +410,28 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int i = 0; i < 128; ++i)
             if (kv0 + i >= limit) s[i] = -CUDART_INF_F;
         }
-        float mx0 = s[0], mx1 = s[1], mx2 = s[2], mx3 = s[3];
+        // row max: four independent chains of 3-input maxima
+        float mx[4];
 #pragma unroll
-        for (int i = 4; i < 128; i += 4) {
-          mx0 = fmaxf(mx0, s[i]);
-          mx1 = fmaxf(mx1, s[i + 1]);
-          mx2 = fmaxf(mx2, s[i + 2]);
-          mx3 = fmaxf(mx3, s[i + 3]);
+        for (int q = 0; q < 4; ++q) {
+          mx[q] = fmax3(s[32 * q], s[32 * q + 1], s[32 * q + 2]);
+#pragma unroll
+          for (int i = 3; i < 31; i += 2) mx[q] = fmax3(mx[q], s[32 * q + i], s[32 * q + i + 1]);
+          mx[q] = fmaxf(mx[q], s[32 * q + 31]);
         }
-        const float m_new = fmaxf(fmaxf(m_raw, fmaxf(mx0, mx1)), fmaxf(mx2, mx3));
-        const float base_new = (m_new == -CUDART_INF_F) ? 0.f : m_new * c;
+        const float m_tile = fmaxf(fmax3(mx[0], mx[1], mx[2]), mx[3]);
+        m_raw = fmaxf(m_raw, m_tile);
+        // Move the exponent base only when the max has grown by more than
+        // kRescaleLog2 (or on the first tile); otherwise keep the old base, so
+        // every p stays below 2^kRescaleLog2 and O, l need no rescale.
+        // While a row has seen no allowed key its base stays -inf and every p
+        // is 0 (exponent offset 0 instead of -inf, so no inf - inf).
+        const float cand = m_raw * c;
         float alpha = 1.f;
-        if (m_new > m_raw) alpha = ex2_approx(m_base - base_new);
-        // Rescale the running O only when some row's max moved (and O holds data).
+        if (m_raw != -CUDART_INF_F && (base == -CUDART_INF_F || cand - base > kRescaleLog2)) {
+          alpha = ex2_approx(base - cand);  // 0 on the first tile with an allowed key
+          base = cand;
+        }
         if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
 #pragma unroll
           for (int cc = 0; cc < D; cc += 32) {
@@ -415,33 +442,42 @@ __global__ void __launch_bounds__(kThreads, 1)
             tmem_st32x32(tO + cc, o);
           }
         }
-        const float nb = -base_new;
-        float l0 = 0.f, l1 = 0.f, l2 = 0.f, l3 = 0.f;
-#pragma unroll
-        for (int i = 0; i < 128; i += 4) {
-          s[i] = ex2_approx(fmaf(s[i], c, nb));
-          s[i + 1] = ex2_approx(fmaf(s[i + 1], c, nb));
-          s[i + 2] = ex2_approx(fmaf(s[i + 2], c, nb));
-          s[i + 3] = ex2_approx(fmaf(s[i + 3], c, nb));
-          l0 += s[i];
-          l1 += s[i + 1];
-          l2 += s[i + 2];
-          l3 += s[i + 3];
-        }
-        l = l * alpha + ((l0 + l1) + (l2 + l3));
-        m_raw = m_new;
-        m_base = base_new;
-        // P (16-bit pairs) over the first 64 columns of this sub-tile's S region.
+        const float nb = (base == -CUDART_INF_F) ? 0.f : -base;
+        float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+        // P (16-bit pairs) over the first 64 columns of this sub-tile's S
+        // region, published in two halves so that P.V can start on the
+        // first 64 keys while the second half is exponentiated.
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
           uint32_t pk[32];
 #pragma unroll
-          for (int i = 0; i < 32; ++i) pk[i] = pack2(s[64 * h + 2 * i], s[64 * h + 2 * i + 1], kBf16);
+          for (int i = 0; i < 32; ++i) {
+            float x0, x1;
+            ffma2_bcast(x0, x1, s[64 * h + 2 * i], s[64 * h + 2 * i + 1], c, nb);
+            const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
+            fadd2_acc(acc[2 * (i & 3)], acc[2 * (i & 3) + 1], p0, p1);
+            pk[i] = pack2(p0, p1, kBf16);
+          }
           tmem_st32x32(tS + 32 * h, pk);
+          tmem_wait_st();
+          tc_fence_before_sync();
+          mbar_arrive(bar_p + 8 * h);
         }
-        tmem_wait_st();
-        tc_fence_before_sync();
-        mbar_arrive(bar_p);
+        const float lt = ((acc[0] + acc[1]) + (acc[2] + acc[3])) + ((acc[4] + acc[5]) + (acc[6] + acc[7]));
+        // P.V uses p rounded to 16 bits. With the base lagging the max, the
+        // tile's largest p is not a power of two, so its rounding would leave
+        // the dominant weight unnormalised; the O normaliser carries the
+        // rounded value of that element (recomputed exactly as above) while
+        // the LSE keeps the unrounded sum.
+        float px, pxr;
+        {
+          float x0, x1;
+          ffma2_bcast(x0, x1, m_tile, m_tile, c, nb);
+          px = ex2_approx(x0);
+          pxr = round16(px, kBf16);
+        }
+        l = l * alpha + lt;
+        l_o = l_o * alpha + (lt + (pxr - px));
       }
       if (!ok) break;
       // -------------------------------------------------------- epilogue
@@ -450,7 +486,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!got) break;
       o_phase ^= 1u;
       tc_fence_after_sync();
-      const float inv = (l > 0.f) ? __frcp_rn(l) : 0.f;
+      const float inv = (l > 0.f) ? __frcp_rn(l_o) : 0.f;
       const bool live = row < p.N;
       uint8_t* orow = reinterpret_cast<uint8_t*>(p.o) +
                       (static_cast<size_t>(w.bh) * p.N + (live ? row : 0)) * (D * 2);
@@ -470,7 +506,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (live) {
         p.lse[static_cast<size_t>(w.bh) * p.N + row] =
-            (l > 0.f) ? (m_base + __log2f(l)) * 0.69314718055994530942f : CUDART_INF_F;
+            (l > 0.f) ? (base + __log2f(l)) * 0.69314718055994530942f : CUDART_INF_F;
       }
       // O_t is read out; the next unit's first P.V may overwrite it once this
       // warpgroup publishes that unit's first P (ordered by bar_p).

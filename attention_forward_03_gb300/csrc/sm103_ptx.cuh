@@ -178,4 +178,38 @@ __device__ __forceinline__ float ex2_approx(float x) {
   return y;
 }
 
+// three-input maximum (one instruction on sm_100 and later)
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+
+// (d0, d1) = (a0, a1) * (b, b) + (c, c) as one packed f32x2 FMA
+__device__ __forceinline__ void ffma2_bcast(float& d0, float& d1, float a0, float a1, float b, float c) {
+  asm("{\n"
+      ".reg .b64 A, B, C, D;\n"
+      "mov.b64 A, {%2, %3};\n"
+      "mov.b64 B, {%4, %4};\n"
+      "mov.b64 C, {%5, %5};\n"
+      "fma.rn.f32x2 D, A, B, C;\n"
+      "mov.b64 {%0, %1}, D;\n"
+      "}\n"
+      : "=f"(d0), "=f"(d1)
+      : "f"(a0), "f"(a1), "f"(b), "f"(c));
+}
+
+// (s0, s1) += (a0, a1) as one packed f32x2 add
+__device__ __forceinline__ void fadd2_acc(float& s0, float& s1, float a0, float a1) {
+  asm("{\n"
+      ".reg .b64 A, S;\n"
+      "mov.b64 S, {%0, %1};\n"
+      "mov.b64 A, {%2, %3};\n"
+      "add.rn.f32x2 S, S, A;\n"
+      "mov.b64 {%0, %1}, S;\n"
+      "}\n"
+      : "+f"(s0), "+f"(s1)
+      : "f"(a0), "f"(a1));
+}
+
 }  // namespace fa2
