@@ -28,6 +28,10 @@ _VP = ctypes.c_void_p
 SIGNATURES = {
     "fa2_fwd": (ctypes.c_int, [_VP, _VP, _VP, _VP, _VP, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                ctypes.c_int, ctypes.c_float, ctypes.c_int, ctypes.c_int, _VP]),
+    "fa2_fwd_workspace_bytes": (ctypes.c_int, [ctypes.c_int, ctypes.POINTER(ctypes.c_size_t)]),
+    "fa2_fwd_ws": (ctypes.c_int, [_VP, _VP, _VP, _VP, _VP, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                  ctypes.c_int, ctypes.c_float, ctypes.c_int, ctypes.c_int, _VP, ctypes.c_size_t,
+                                  _VP]),
     "fa2_device_status": (ctypes.c_int, [_VP, ctypes.POINTER(ctypes.c_int), ctypes.c_int]),
     "fa2_set_watchdog_ns": (ctypes.c_int, [ctypes.c_ulonglong]),
     "fa2_error_string": (ctypes.c_char_p, [ctypes.c_int]),
@@ -79,6 +83,19 @@ def fa2_fwd(Q: int, K: int, V: int, O: int, LSE: int, B: int, H: int, N: int, D:
     return library().fa2_fwd(Q, K, V, O, LSE, B, H, N, D, float(scale), int(is_causal), int(dtype), stream)
 
 
+def fa2_fwd_ws(Q: int, K: int, V: int, O: int, LSE: int, B: int, H: int, N: int, D: int, scale: float,
+               is_causal: int, dtype: int, workspace: int | None, workspace_bytes: int, stream: int | None) -> int:
+    """Pointer-level call of the workspace variant; returns the raw status code."""
+    return library().fa2_fwd_ws(Q, K, V, O, LSE, B, H, N, D, float(scale), int(is_causal), int(dtype), workspace,
+                                int(workspace_bytes), stream)
+
+
+def fa2_fwd_workspace_bytes(D: int) -> int:
+    n = ctypes.c_size_t(0)
+    _check(library().fa2_fwd_workspace_bytes(int(D), ctypes.byref(n)), "fa2_fwd_workspace_bytes")
+    return n.value
+
+
 def fa2_device_status(stream: int | None = None, clear: bool = False) -> int:
     v = ctypes.c_int(0)
     _check(library().fa2_device_status(stream, ctypes.byref(v), int(bool(clear))), "fa2_device_status")
@@ -103,13 +120,34 @@ def _dtype_code(t) -> int:
     raise TypeError(f"unsupported dtype {t.dtype}; expected float16 or bfloat16")
 
 
+_workspaces = {}
+
+
+def workspace_for(device, D: int):
+    """A cached caller-side workspace (torch uint8 tensor) for fa2_fwd_ws on `device`."""
+    import torch
+    dev = torch.device(device)
+    key = (dev.index, D)
+    ws = _workspaces.get(key)
+    if ws is None:
+        with torch.cuda.device(dev):
+            n = fa2_fwd_workspace_bytes(D)
+        ws = torch.empty(n, dtype=torch.uint8, device=dev)
+        _workspaces[key] = ws
+    return ws
+
+
 def attention_forward(q, k, v, scale: float | None = None, is_causal: bool = False, out=None, lse=None,
-                      stream=None):
+                      stream=None, schedule: str = "balanced", workspace=None):
     """FlashAttention-2 forward over torch CUDA tensors [B, H, N, D] (fp16/bf16).
 
     Returns (O, LSE): O like q, LSE float32 [B, H, N]. `out` / `lse` may be
     passed to write into caller-owned buffers. Runs on `stream` (a
     torch.cuda.Stream) or the current stream.
+    schedule: "balanced" (fa2_fwd_ws with a workspace: equal work per SM) or
+    "units" (fa2_fwd: whole query tiles per CTA, no workspace).
+    workspace: optional uint8 CUDA tensor for the balanced schedule; by default
+    a cached one per device is used.
     """
     import torch
     if not (q.is_cuda and k.is_cuda and v.is_cuda):
@@ -120,6 +158,8 @@ def attention_forward(q, k, v, scale: float | None = None, is_causal: bool = Fal
         raise ValueError("q, k, v must share one dtype")
     if not (q.is_contiguous() and k.is_contiguous() and v.is_contiguous()):
         raise ValueError("q, k, v must be contiguous")
+    if schedule not in ("balanced", "units"):
+        raise ValueError("schedule must be 'balanced' or 'units'")
     B, H, N, D = q.shape
     if scale is None:
         scale = 1.0 / math.sqrt(D)
@@ -133,7 +173,14 @@ def attention_forward(q, k, v, scale: float | None = None, is_causal: bool = Fal
         raise ValueError("lse must be a contiguous float32 [B, H, N] tensor")
     s = stream if stream is not None else torch.cuda.current_stream(q.device)
     with torch.cuda.device(q.device):
-        code = fa2_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(),
-                       B, H, N, D, scale, int(bool(is_causal)), _dtype_code(q), s.cuda_stream)
-    _check(code, "fa2_fwd")
+        if schedule == "units":
+            code = fa2_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(),
+                           B, H, N, D, scale, int(bool(is_causal)), _dtype_code(q), s.cuda_stream)
+            _check(code, "fa2_fwd")
+        else:
+            ws = workspace if workspace is not None else workspace_for(q.device, D)
+            code = fa2_fwd_ws(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(),
+                              B, H, N, D, scale, int(bool(is_causal)), _dtype_code(q), ws.data_ptr(),
+                              ws.numel() * ws.element_size(), s.cuda_stream)
+            _check(code, "fa2_fwd_ws")
     return out, lse

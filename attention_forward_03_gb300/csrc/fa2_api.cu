@@ -4,7 +4,11 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <unistd.h>
+
+#include <algorithm>
 #include <atomic>
+#include <chrono>
 #include <cmath>
 #include <cstdint>
 #include <cstdio>
@@ -112,8 +116,26 @@ LaunchFn pick(int d, int dtype, int causal) {
 
 using namespace fa2;
 
-extern "C" int fa2_fwd(const void* Q, const void* K, const void* V, void* O, float* LSE, int B, int H, int N,
-                       int D, float scale, int is_causal, int dtype, struct CUstream_st* stream) {
+namespace {
+
+std::atomic<unsigned long long> g_epoch{0};
+
+// Launch tags: a per-process random high half and a counter, so a workspace
+// flag left by any earlier launch (of this or another process) never matches.
+unsigned long long next_epoch() {
+  static const unsigned long long salt = [] {
+    unsigned long long x = static_cast<unsigned long long>(std::chrono::steady_clock::now().time_since_epoch().count());
+    x ^= static_cast<unsigned long long>(getpid()) << 21;
+    x ^= reinterpret_cast<uintptr_t>(&g_epoch);
+    x = (x ^ (x >> 30)) * 0xbf58476d1ce4e5b9ull;
+    x = (x ^ (x >> 27)) * 0x94d049bb133111ebull;
+    return (x ^ (x >> 31)) << 32;
+  }();
+  return salt | ((g_epoch.fetch_add(1, std::memory_order_relaxed) + 1) & 0xffffffffull);
+}
+
+int launch(const void* Q, const void* K, const void* V, void* O, float* LSE, int B, int H, int N, int D,
+           float scale, int is_causal, int dtype, void* workspace, size_t workspace_bytes, cudaStream_t stream) {
   if (B < 0 || H < 0 || N < 0) return FA2_ERR_INVALID_ARG;
   if (D != 64 && D != 128) return FA2_ERR_UNSUPPORTED;
   if (dtype != FA2_F16 && dtype != FA2_BF16) return FA2_ERR_UNSUPPORTED;
@@ -125,13 +147,17 @@ extern "C" int fa2_fwd(const void* Q, const void* K, const void* V, void* O, flo
   if (bh > INT32_MAX || bh * n_qt > INT32_MAX) return FA2_ERR_INVALID_ARG;
   const uintptr_t mis = reinterpret_cast<uintptr_t>(Q) | reinterpret_cast<uintptr_t>(K) |
                         reinterpret_cast<uintptr_t>(V) | reinterpret_cast<uintptr_t>(O) |
-                        reinterpret_cast<uintptr_t>(LSE);
+                        reinterpret_cast<uintptr_t>(LSE) | reinterpret_cast<uintptr_t>(workspace);
   if (mis & 15u) return FA2_ERR_ALIGN;
   const size_t tbytes = static_cast<size_t>(bh) * N * D * 2;
   const size_t lbytes = static_cast<size_t>(bh) * N * 4;
   if (overlaps(O, tbytes, Q, tbytes) || overlaps(O, tbytes, K, tbytes) || overlaps(O, tbytes, V, tbytes) ||
       overlaps(LSE, lbytes, Q, tbytes) || overlaps(LSE, lbytes, K, tbytes) || overlaps(LSE, lbytes, V, tbytes) ||
       overlaps(LSE, lbytes, O, tbytes))
+    return FA2_ERR_INVALID_ARG;
+  if (workspace && (overlaps(workspace, workspace_bytes, Q, tbytes) || overlaps(workspace, workspace_bytes, K, tbytes) ||
+                    overlaps(workspace, workspace_bytes, V, tbytes) || overlaps(workspace, workspace_bytes, O, tbytes) ||
+                    overlaps(workspace, workspace_bytes, LSE, lbytes)))
     return FA2_ERR_INVALID_ARG;
 
   int dev = 0;
@@ -141,6 +167,7 @@ extern "C" int fa2_fwd(const void* Q, const void* K, const void* V, void* O, flo
   if (!info) return FA2_ERR_UNSUPPORTED;
   if (info->err != cudaSuccess) return record_cuda(info->err);
   if (info->cc_major != 10 || info->cc_minor != 3) return FA2_ERR_UNSUPPORTED;
+  if (workspace && workspace_bytes < stream_k_workspace_bytes(info->sms, D)) return FA2_ERR_INVALID_ARG;
 
   CUtensorMap mq, mk, mv;
   if (!make_map(&mq, Q, (int)bh, N, D, dtype) || !make_map(&mk, K, (int)bh, N, D, dtype) ||
@@ -148,7 +175,7 @@ extern "C" int fa2_fwd(const void* Q, const void* K, const void* V, void* O, flo
     std::snprintf(t_last_cuda_error, sizeof(t_last_cuda_error), "cuTensorMapEncodeTiled failed");
     return FA2_ERR_CUDA;
   }
-  Params p;
+  Params p = {};
   p.o = O;
   p.lse = LSE;
   p.status = info->status;
@@ -157,11 +184,64 @@ extern "C" int fa2_fwd(const void* Q, const void* K, const void* V, void* O, flo
   p.BH = (int)bh;
   p.n_qt = (int)n_qt;
   p.num_units = (int)(bh * n_qt);
+  p.nkv_full = (N + kKeys - 1) / kKeys;
   p.scale_log2 = scale * 1.4426950408889634f;
-  const int grid = p.num_units < info->sms ? p.num_units : info->sms;
-  e = pick(D, dtype, is_causal)(mq, mk, mv, p, grid, reinterpret_cast<cudaStream_t>(stream));
+  // K/V-tile steps of one head: non-causal n_qt * nkv_full; causal sum of
+  // min(2qt+2, nkv_full) over the head's query units.
+  long long per_head = 0;
+  if (is_causal) {
+    for (int64_t qt = 0; qt < n_qt; ++qt) per_head += std::min<long long>(2 * qt + 2, p.nkv_full);
+  } else {
+    per_head = n_qt * static_cast<long long>(p.nkv_full);
+  }
+  p.steps_per_head = per_head;
+  p.total_steps = per_head * bh;
+  int grid;
+  if (workspace) {
+    p.stream_k = 1;
+    grid = static_cast<int>(std::min<long long>(info->sms, p.total_steps));
+    const size_t slots = static_cast<size_t>(info->sms) * 2;
+    char* ws = static_cast<char*>(workspace);
+    p.ws_o = reinterpret_cast<float*>(ws);
+    p.ws_stats = p.ws_o + slots * D * 128;
+    const size_t fbytes = (slots * (static_cast<size_t>(D) * 128 + 3 * 128) * sizeof(float) + 255) / 256 * 256;
+    p.ws_flags = reinterpret_cast<unsigned long long*>(ws + fbytes);
+    p.epoch = next_epoch();
+  } else {
+    p.stream_k = 0;
+    grid = p.num_units < info->sms ? p.num_units : info->sms;
+  }
+  e = pick(D, dtype, is_causal)(mq, mk, mv, p, grid, stream);
   if (e != cudaSuccess) return record_cuda(e);
   return FA2_OK;
+}
+
+}  // namespace
+
+extern "C" int fa2_fwd(const void* Q, const void* K, const void* V, void* O, float* LSE, int B, int H, int N,
+                       int D, float scale, int is_causal, int dtype, struct CUstream_st* stream) {
+  return launch(Q, K, V, O, LSE, B, H, N, D, scale, is_causal, dtype, nullptr, 0,
+                reinterpret_cast<cudaStream_t>(stream));
+}
+
+extern "C" int fa2_fwd_workspace_bytes(int D, size_t* bytes) {
+  if (!bytes) return FA2_ERR_INVALID_ARG;
+  if (D != 64 && D != 128) return FA2_ERR_UNSUPPORTED;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return record_cuda(e);
+  DeviceInfo* info = device_info(dev);
+  if (!info) return FA2_ERR_UNSUPPORTED;
+  if (info->err != cudaSuccess) return record_cuda(info->err);
+  *bytes = stream_k_workspace_bytes(info->sms, D);
+  return FA2_OK;
+}
+
+extern "C" int fa2_fwd_ws(const void* Q, const void* K, const void* V, void* O, float* LSE, int B, int H, int N,
+                          int D, float scale, int is_causal, int dtype, void* workspace, size_t workspace_bytes,
+                          struct CUstream_st* stream) {
+  return launch(Q, K, V, O, LSE, B, H, N, D, scale, is_causal, dtype, workspace, workspace_bytes,
+                reinterpret_cast<cudaStream_t>(stream));
 }
 
 extern "C" int fa2_device_status(struct CUstream_st* stream, int* status, int clear) {

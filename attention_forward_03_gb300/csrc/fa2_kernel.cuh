@@ -27,6 +27,15 @@
 // tiles (K_j, V_j, K_j+1, ...), all 128-byte swizzled by TMA in 128-row x
 // 64-element panels, which is also the operand layout the MMAs read.
 //
+// Schedules. Work is a sequence of segments: K/V tiles [kv_begin, kv_end) of
+// one unit. With the round schedule every segment is a whole unit. With the
+// stream-K schedule each CTA takes an equal share of all K/V-tile steps, so a
+// unit may be cut between consecutive CTAs: the CTA holding the unit's first
+// tiles ("owner", the last segment of its share) merges the fp32 partial
+// results the following CTAs wrote for the rest of the unit (each as the
+// first segment of its share) before writing O and LSE. Partials carry their
+// own exponent base and are combined with the usual (m, l) merge.
+//
 // Per K/V tile j the MMA thread issues, for each sub-tile t in turn:
 //   O_t (+)= P_t(j) V_j      once softmax t has published P_t(j)
 //   S_t    = Q_t K_{j+1}^T   right after, into the same TMEM columns
@@ -68,6 +77,8 @@ enum : int {
   kSiteSoftmaxSFull = 6,
   kSiteSoftmaxOFull = 7,
   kSiteDrain = 8,
+  kSitePartialWrite = 9,
+  kSitePartialFlag = 10,
 };
 
 template <int D>
@@ -78,8 +89,9 @@ struct Layout {
   static constexpr int kQBytes = kSubTiles * kTileBytes;
   static constexpr int kRingOffset = kQBytes;
   static constexpr int kBarOffset = kRingOffset + kStages * kTileBytes;
-  // barriers: q_full, q_empty, ring full[S], ring empty[S], s_full[2], p_full[2][2 halves], o_full[2], drain
-  static constexpr int kNumBars = 2 + 2 * kStages + 8 + 1;
+  // barriers: q_full, q_empty, ring full[S], ring empty[S], s_full[2], p_full[2][2 halves], o_full[2],
+  // drain, part_done[2]
+  static constexpr int kNumBars = 2 + 2 * kStages + 8 + 1 + 2;
   static constexpr int kMiscOffset = kBarOffset + kNumBars * 8;
   static constexpr int kSmemBytes = kMiscOffset + 16 + 1024;  // + slack for 1 KB alignment
   static constexpr uint32_t kColO = 2 * kKeys;                 // O0 at 256, O1 at 256 + D
@@ -87,36 +99,88 @@ struct Layout {
   static_assert(kSmemBytes <= 232448, "shared memory budget");
 };
 
-struct Unit {
-  int bh;
-  int q0;
-  int nkv;
-};
-
+// K/V tiles of query unit qt (two 128-row sub-tiles from row 256*qt).
 template <bool kCausal>
-__device__ __forceinline__ Unit decode_unit(int u, const Params& p) {
-  int qt, bh;
-  if (kCausal) {  // heaviest query tiles first
-    qt = p.n_qt - 1 - u / p.BH;
-    bh = u % p.BH;
-  } else {        // consecutive units share a head (K/V reuse in L2)
-    qt = u % p.n_qt;
-    bh = u / p.n_qt;
-  }
-  Unit w;
-  w.bh = bh;
-  w.q0 = qt * kUnitRows;
-  const int kend = kCausal ? min(p.N, w.q0 + kUnitRows) : p.N;
-  w.nkv = (kend + kKeys - 1) / kKeys;
-  return w;
+__device__ __forceinline__ int unit_nkv(int qt, const Params& p) {
+  return kCausal ? min(2 * qt + 2, p.nkv_full) : p.nkv_full;
 }
 
-// The r-th unit of this CTA; causal work is dealt in a zig-zag so that the
-// heavy and light ends of each round are spread over the CTAs.
+struct Segment {
+  int bh;
+  int q0;                // first query row of the unit
+  int kv_begin, kv_end;  // K/V tiles processed in this segment
+  int nkv;               // K/V tiles of the whole unit
+  long long unit_end;    // stream-K: step one past the unit's last step
+};
+
+struct SegCursor {
+  int round;             // round schedule
+  long long step, end;   // stream-K schedule
+};
+
+__device__ __forceinline__ long long stream_k_begin(const Params& p, int b) {
+  return p.total_steps * b / gridDim.x;
+}
+
+__device__ __forceinline__ SegCursor first_cursor(const Params& p) {
+  SegCursor c;
+  c.round = 0;
+  c.step = p.stream_k ? stream_k_begin(p, blockIdx.x) : 0;
+  c.end = p.stream_k ? stream_k_begin(p, blockIdx.x + 1) : 0;
+  return c;
+}
+
+// Next segment of this CTA. Every role walks the same sequence.
 template <bool kCausal>
-__device__ __forceinline__ int unit_of_round(int r) {
-  const int g = gridDim.x, b = blockIdx.x;
-  return r * g + ((kCausal && (r & 1)) ? (g - 1 - b) : b);
+__device__ __forceinline__ bool next_segment(SegCursor& c, Segment& s, const Params& p) {
+  if (!p.stream_k) {
+    // Rounds of whole units. Non-causal: consecutive units share a head (K/V
+    // reuse in L2). Causal: heaviest query tiles first, dealt in a zig-zag so
+    // heavy and light ends of each round spread over the CTAs.
+    const int g = gridDim.x, b = blockIdx.x, r = c.round++;
+    const int u = r * g + ((kCausal && (r & 1)) ? (g - 1 - b) : b);
+    if (u >= p.num_units) return false;
+    int qt, bh;
+    if (kCausal) {
+      qt = p.n_qt - 1 - u / p.BH;
+      bh = u % p.BH;
+    } else {
+      qt = u % p.n_qt;
+      bh = u / p.n_qt;
+    }
+    s.bh = bh;
+    s.q0 = qt * kUnitRows;
+    s.nkv = unit_nkv<kCausal>(qt, p);
+    s.kv_begin = 0;
+    s.kv_end = s.nkv;
+    s.unit_end = 0;
+    return true;
+  }
+  if (c.step >= c.end) return false;
+  // Units in order (head, query tile ascending); unit qt of a head starts at
+  // step qt*nkv_full (non-causal) or qt*(qt+1) (causal: nkv = 2qt+2).
+  const long long bh = c.step / p.steps_per_head;
+  const int r = static_cast<int>(c.step - bh * p.steps_per_head);
+  int qt, start;
+  if (kCausal) {
+    qt = static_cast<int>((sqrtf(4.f * r + 1.f) - 1.f) * 0.5f);
+    qt = min(max(qt, 0), p.n_qt - 1);
+    while (qt > 0 && qt * (qt + 1) > r) --qt;
+    while (qt + 1 < p.n_qt && (qt + 1) * (qt + 2) <= r) ++qt;
+    start = qt * (qt + 1);
+  } else {
+    qt = r / p.nkv_full;
+    start = qt * p.nkv_full;
+  }
+  s.bh = static_cast<int>(bh);
+  s.q0 = qt * kUnitRows;
+  s.nkv = unit_nkv<kCausal>(qt, p);
+  s.kv_begin = r - start;
+  const long long left = c.end - c.step;
+  s.kv_end = static_cast<int>(min(static_cast<long long>(s.nkv), s.kv_begin + left));
+  s.unit_end = c.step - s.kv_begin + s.nkv;
+  c.step += s.kv_end - s.kv_begin;
+  return true;
 }
 
 struct Watchdog {
@@ -143,6 +207,30 @@ __device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, cons
       }
     }
   }
+}
+
+// Bounded wait for a global flag to carry this launch's epoch (acquire).
+__device__ __forceinline__ bool wait_flag(const unsigned long long* f, unsigned long long epoch, const Watchdog& wd,
+                                          int site) {
+  uint64_t t0 = 0;
+  for (uint32_t it = 0;; ++it) {
+    unsigned long long v;
+    asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(f) : "memory");
+    if (v == epoch) return true;
+    if (it == 0) t0 = global_timer_ns();
+    if ((it & 15u) == 15u) {
+      if (*wd.abort_flag) return false;
+      if (global_timer_ns() - t0 > wd.limit_ns) {
+        *wd.abort_flag = 1;
+        atomicCAS(wd.status, 0, site);
+        return false;
+      }
+    }
+  }
+}
+
+__device__ __forceinline__ void store_release(unsigned long long* f, unsigned long long v) {
+  asm volatile("st.release.gpu.global.u64 [%0], %1;" ::"l"(f), "l"(v) : "memory");
 }
 
 __device__ __forceinline__ float round16(float x, bool bf16) {
@@ -180,6 +268,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t bar_p_full0 = bar_s_full0 + 16;  // [sub-tile][half] at + 16*t + 8*h
   const uint32_t bar_o_full0 = bar_p_full0 + 32;
   const uint32_t bar_drain = bar_o_full0 + 16;
+  const uint32_t bar_part0 = bar_drain + 8;  // [sub-tile]
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kMiscOffset);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kMiscOffset + 4);
 
@@ -200,6 +289,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(bar_o_full0 + 8 * t, 1);
     }
     mbar_init(bar_drain, 1);
+    mbar_init(bar_part0, 4 * 32);
+    mbar_init(bar_part0 + 8, 4 * 32);
     *abort_flag = 0;
     mbar_init_fence();
   }
@@ -228,10 +319,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t it = 0;
       uint32_t q_round = 0;
       bool ok = true;
-      for (int r = 0; ok; ++r) {
-        const int u = unit_of_round<kCausal>(r);
-        if (u >= p.num_units) break;
-        const Unit w = decode_unit<kCausal>(u, p);
+      SegCursor cur = first_cursor(p);
+      Segment w;
+      while (ok && next_segment<kCausal>(cur, w, p)) {
         if (q_round > 0 && !wait_bounded(bar_q_empty, (q_round - 1) & 1u, wd, kSiteLoadQEmpty)) {
           ok = false;
           break;
@@ -242,7 +332,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             tma_load_3d_hint(sQ + t * L::kTileBytes + pn * kPanelBytes, &tmQ, bar_q_full, pn * 64,
                              w.q0 + t * kRows, w.bh, stream_once);
         ++q_round;
-        for (int j = 0; j < w.nkv && ok; ++j) {
+        for (int j = w.kv_begin; j < w.kv_end && ok; ++j) {
           for (int kv = 0; kv < 2; ++kv) {
             const int slot = it % L::kStages;
             const uint32_t ph = (it / L::kStages) & 1u;
@@ -300,10 +390,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t it = 0, q_round = 0;
       uint32_t p_phase[2] = {0u, 0u};  // both halves of a sub-tile flip together
       bool ok = true;
-      for (int r = 0; ok; ++r) {
-        const int u = unit_of_round<kCausal>(r);
-        if (u >= p.num_units) break;
-        const Unit w = decode_unit<kCausal>(u, p);
+      SegCursor cur = first_cursor(p);
+      Segment w;
+      while (ok && next_segment<kCausal>(cur, w, p)) {
         if (!wait_bounded(bar_q_full, q_round & 1u, wd, kSiteMmaQFull)) { ok = false; break; }
         ++q_round;
         int slot_k = it % L::kStages;
@@ -318,16 +407,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         mma_commit(bar_s_full0 + 8);
         mma_commit(bar_empty(slot_k));
         ++it;
-        if (w.nkv == 1) mma_commit(bar_q_empty);
+        if (w.kv_end - w.kv_begin == 1) mma_commit(bar_q_empty);
 
-        for (int j = 0; j < w.nkv; ++j) {
+        for (int j = w.kv_begin; j < w.kv_end; ++j) {
           const int slot_v = it % L::kStages;
           if (!wait_bounded(bar_full(slot_v), (it / L::kStages) & 1u, wd, kSiteMmaRingFull)) {
             ok = false;
             break;
           }
           ++it;
-          const bool next = j + 1 < w.nkv;
+          const bool next = j + 1 < w.kv_end;
           if (next) {
             slot_k = it % L::kStages;
             if (!wait_bounded(bar_full(slot_k), (it / L::kStages) & 1u, wd, kSiteMmaRingFull)) {
@@ -342,7 +431,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               break;
             }
             tc_fence_after_sync();
-            issue_pv_half(t, slot_v, 0, j > 0);
+            issue_pv_half(t, slot_v, 0, j > w.kv_begin);
             if (!wait_bounded(bar_p_full0 + 16 * t + 8, p_phase[t], wd, kSiteMmaPFull)) {
               ok = false;
               break;
@@ -361,7 +450,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (next) {
             mma_commit(bar_empty(slot_k));
             ++it;
-            if (j + 2 == w.nkv) mma_commit(bar_q_empty);
+            if (j + 2 == w.kv_end) mma_commit(bar_q_empty);
           }
         }
       }
@@ -381,19 +470,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t bar_p = bar_p_full0 + 16 * t;  // + 8 for the second half
     const uint32_t bar_o = bar_o_full0 + 8 * t;
     const float c = p.scale_log2;
-    uint32_t s_phase = 0, o_phase = 0;
+    const int rr = wr * 32 + lane;           // row within the sub-tile
+    uint32_t s_phase = 0, o_phase = 0, part_phase = 0;
     bool ok = true;
-    for (int r = 0; ok; ++r) {
-      const int u = unit_of_round<kCausal>(r);
-      if (u >= p.num_units) break;
-      const Unit w = decode_unit<kCausal>(u, p);
-      const int row = w.q0 + t * kRows + wr * 32 + lane;
+    SegCursor cur = first_cursor(p);
+    Segment w;
+    while (ok && next_segment<kCausal>(cur, w, p)) {
+      const int row = w.q0 + t * kRows + rr;
       const int limit = kCausal ? min(p.N, row + 1) : p.N;  // allowed keys: [0, limit)
       float m_raw = -CUDART_INF_F;  // running max of the raw scores seen so far
       float base = -CUDART_INF_F;   // exponent base (log2 units) that l and O are relative to
       float l = 0.f;    // sum of p (unrounded): LSE
       float l_o = 0.f;  // normaliser of O (see below)
-      for (int j = 0; j < w.nkv; ++j) {
+      for (int j = w.kv_begin; j < w.kv_end; ++j) {
         bool got = wait_bounded(bar_s, s_phase, wd, kSiteSoftmaxSFull);
         got = __all_sync(0xffffffffu, got);
         if (!got) { ok = false; break; }
@@ -432,7 +521,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           alpha = ex2_approx(base - cand);  // 0 on the first tile with an allowed key
           base = cand;
         }
-        if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+        if (j > w.kv_begin && __any_sync(0xffffffffu, alpha != 1.f)) {
 #pragma unroll
           for (int cc = 0; cc < D; cc += 32) {
             uint32_t o[32];
@@ -486,6 +575,56 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!got) break;
       o_phase ^= 1u;
       tc_fence_after_sync();
+      if (w.kv_begin > 0) {
+        // Not the unit's first tiles: hand the unnormalised partial (O, base,
+        // l, l_o) to the owner through this CTA's workspace slot.
+        const size_t slot = static_cast<size_t>(blockIdx.x) * 2 + t;
+        float* po = p.ws_o + slot * D * 128;
+        float* ps = p.ws_stats + slot * 3 * 128;
+#pragma unroll
+        for (int cc = 0; cc < D; cc += 32) {
+          uint32_t o[32];
+          tmem_ld32x32_wait(tO + cc, o);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) __stcg(po + (cc + i) * 128 + rr, __uint_as_float(o[i]));
+        }
+        __stcg(ps + rr, base);
+        __stcg(ps + 128 + rr, l);
+        __stcg(ps + 256 + rr, l_o);
+        __threadfence();
+        mbar_arrive(bar_part0 + 8 * t);
+        if (rr == 0) {
+          if (!wait_bounded(bar_part0 + 8 * t, part_phase, wd, kSitePartialWrite)) break;
+          store_release(p.ws_flags + slot, p.epoch);
+        }
+        part_phase ^= 1u;
+        tc_fence_before_sync();
+        continue;
+      }
+      // Owner (or whole unit): fold in the partials of the CTAs that took the
+      // rest of this unit, if any, then normalise and write O and LSE.
+      float a_own = 1.f, nbase = base;
+      int first_c = blockIdx.x + 1, last_c = blockIdx.x;  // partial holders [first_c, last_c]
+      if (p.stream_k && w.kv_end < w.nkv) {
+        while (last_c + 1 < static_cast<int>(gridDim.x) && stream_k_begin(p, last_c + 1) < w.unit_end) ++last_c;
+        bool fine = true;
+        for (int cb = first_c; cb <= last_c && fine; ++cb)
+          fine = wait_flag(p.ws_flags + static_cast<size_t>(cb) * 2 + t, p.epoch, wd, kSitePartialFlag);
+        fine = __all_sync(0xffffffffu, fine);
+        if (!fine) break;
+        for (int cb = first_c; cb <= last_c; ++cb)
+          nbase = fmaxf(nbase, __ldcg(p.ws_stats + (static_cast<size_t>(cb) * 2 + t) * 3 * 128 + rr));
+        a_own = ex2_approx(base - nbase);
+        l *= a_own;
+        l_o *= a_own;
+        for (int cb = first_c; cb <= last_c; ++cb) {
+          const float* ps = p.ws_stats + (static_cast<size_t>(cb) * 2 + t) * 3 * 128;
+          const float a = ex2_approx(__ldcg(ps + rr) - nbase);  // 0 for a partial that saw no key
+          l += a * __ldcg(ps + 128 + rr);
+          l_o += a * __ldcg(ps + 256 + rr);
+        }
+        base = nbase;
+      }
       const float inv = (l > 0.f) ? __frcp_rn(l_o) : 0.f;
       const bool live = row < p.N;
       uint8_t* orow = reinterpret_cast<uint8_t*>(p.o) +
@@ -494,10 +633,19 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int cc = 0; cc < D; cc += 32) {
         uint32_t o[32];
         tmem_ld32x32_wait(tO + cc, o);
+        float of[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) of[i] = __uint_as_float(o[i]) * a_own;
+        for (int cb = first_c; cb <= last_c; ++cb) {
+          const size_t slot = static_cast<size_t>(cb) * 2 + t;
+          const float a = ex2_approx(__ldcg(p.ws_stats + slot * 3 * 128 + rr) - nbase);
+          const float* po = p.ws_o + slot * D * 128;
+#pragma unroll
+          for (int i = 0; i < 32; ++i) of[i] = fmaf(a, __ldcg(po + (cc + i) * 128 + rr), of[i]);
+        }
         uint32_t pk[16];
 #pragma unroll
-        for (int i = 0; i < 16; ++i)
-          pk[i] = pack2(__uint_as_float(o[2 * i]) * inv, __uint_as_float(o[2 * i + 1]) * inv, kBf16);
+        for (int i = 0; i < 16; ++i) pk[i] = pack2(of[2 * i] * inv, of[2 * i + 1] * inv, kBf16);
         if (live) {
           uint4* dst = reinterpret_cast<uint4*>(orow + cc * 2);
 #pragma unroll
@@ -508,8 +656,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         p.lse[static_cast<size_t>(w.bh) * p.N + row] =
             (l > 0.f) ? (base + __log2f(l)) * 0.69314718055994530942f : CUDART_INF_F;
       }
-      // O_t is read out; the next unit's first P.V may overwrite it once this
-      // warpgroup publishes that unit's first P (ordered by bar_p).
+      // O_t is read out; the next segment's first P.V may overwrite it once
+      // this warpgroup publishes that segment's first P (ordered by bar_p).
       tc_fence_before_sync();
     }
   }
@@ -522,6 +670,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
+// The stream-K schedule waits across CTAs, so it is launched cooperatively
+// (the whole grid resident at once, or the launch fails).
 template <int D, bool kBf16, bool kCausal>
 cudaError_t launch_fwd(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v, const Params& p,
                        int grid, cudaStream_t stream) {
@@ -529,8 +679,17 @@ cudaError_t launch_fwd(const CUtensorMap& q, const CUtensorMap& k, const CUtenso
   const int smem = Layout<D>::kSmemBytes;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  kern<<<grid, kThreads, smem, stream>>>(q, k, v, p);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = p.stream_k ? 1 : 0;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, q, k, v, p);
 }
 
 }  // namespace fa2

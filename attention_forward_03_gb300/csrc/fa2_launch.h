@@ -4,6 +4,7 @@
 #pragma once
 #include <cuda.h>
 #include <cuda_runtime.h>
+#include <stddef.h>
 
 namespace fa2 {
 
@@ -21,8 +22,25 @@ struct Params {
   int BH;
   int n_qt;                 // query work units per head = ceil(N / 256)
   int num_units;            // BH * n_qt
+  int nkv_full;             // K/V tiles of a full row = ceil(N / 128)
   float scale_log2;         // scale * log2(e)
+  // Schedule. 0: whole units dealt to CTAs in rounds. 1 (stream-K): CTA b
+  // takes K/V-tile steps [total*b/G, total*(b+1)/G) of the unit sequence;
+  // units cut between CTAs are merged through the workspace below.
+  int stream_k;
+  long long steps_per_head; // K/V-tile steps of all units of one head
+  long long total_steps;    // BH * steps_per_head
+  float* ws_o;              // [G][2][D][128] fp32 partial O (unnormalised)
+  float* ws_stats;          // [G][2][3][128] base, l, l_o of each partial row
+  unsigned long long* ws_flags;  // [G][2] = epoch once that partial is written
+  unsigned long long epoch; // unique tag of this launch
 };
+
+// Bytes of stream-K workspace for `grid` CTAs at head dimension d.
+inline size_t stream_k_workspace_bytes(int grid, int d) {
+  const size_t per = 2ull * (static_cast<size_t>(d) * 128 + 3 * 128) * sizeof(float);
+  return (static_cast<size_t>(grid) * per + 255) / 256 * 256 + static_cast<size_t>(grid) * 2 * 8;
+}
 
 template <int D, bool kBf16, bool kCausal>
 cudaError_t launch_fwd(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v, const Params& p,

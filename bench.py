@@ -274,7 +274,8 @@ def run_gb300(args, w, rank, world, local):
 
     def step(i):
         qd, kd, vd, od, ld = sets[i % nsets]
-        fa2.attention_forward(qd, kd, vd, scale=w.scale, is_causal=w.causal, out=od, lse=ld, stream=stream)
+        fa2.attention_forward(qd, kd, vd, scale=w.scale, is_causal=w.causal, out=od, lse=ld, stream=stream,
+                              schedule=args.schedule)
 
     clocks = ClockSampler(local)
     clocks.start()
@@ -324,7 +325,8 @@ def run_gb300(args, w, rank, world, local):
         qd.copy_(qh, non_blocking=True)
         kd.copy_(kh, non_blocking=True)
         vd.copy_(vh, non_blocking=True)
-        fa2.attention_forward(qd, kd, vd, scale=w.scale, is_causal=w.causal, out=od, lse=ld, stream=stream)
+        fa2.attention_forward(qd, kd, vd, scale=w.scale, is_causal=w.causal, out=od, lse=ld, stream=stream,
+                              schedule=args.schedule)
         oh.copy_(od, non_blocking=True)
         lh.copy_(ld, non_blocking=True)
 
@@ -354,7 +356,8 @@ def run_gb300(args, w, rank, world, local):
         "scaling": "weak", "vs_baseline": None, "dtype": w.dtype,
         "data": "synthetic (seeded N(0, sigma^2) inputs, cast to the workload's 16-bit dtype)",
         "config": {"workload": w.describe(), "B": w.B, "H": w.H, "N": w.N, "D": w.D, "causal": w.causal,
-                   "scale": "1/sqrt(D)", "parallelism": f"weak x{world} (one independent replica per GPU)",
+                   "scale": "1/sqrt(D)", "schedule": args.schedule,
+                   "parallelism": f"weak x{world} (one independent replica per GPU)",
                    "l2": f"inputs rotate over {nsets} copies ({nsets * set_bytes / 2**20:.0f} MiB > 2x L2)"},
         "pct_of_peak": 100.0 * achieved / peak,
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
@@ -380,6 +383,8 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--workload", default="target", choices=sorted(workloads.WORKLOADS))
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--schedule", default="balanced", choices=["balanced", "units"],
+                    help="balanced: fa2_fwd_ws (equal K/V-tile steps per SM); units: fa2_fwd")
     ap.add_argument("--settle-seconds", type=float, default=1.0)
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--reference-seconds", type=float, default=120.0,

@@ -23,6 +23,8 @@
 #ifndef FA2_GB300_H
 #define FA2_GB300_H
 
+#include <stddef.h>
+
 #ifdef __cplusplus
 extern "C" {
 #endif
@@ -72,6 +74,37 @@ struct CUstream_st; /* the same type as cudaStream_t / CUstream */
 int fa2_fwd(const void* Q, const void* K, const void* V, void* O, float* LSE,
             int B, int H, int N, int D, float scale, int is_causal, int dtype,
             struct CUstream_st* stream);
+
+/*
+ * fa2_fwd_workspace_bytes — bytes of device workspace fa2_fwd_ws needs on the
+ * current device for head dimension D (64 or 128): one fp32 partial result of
+ * a 256-row work unit per SM plus one 8-byte flag per 128-row half. It does
+ * not depend on B, H or N. Returns FA2_OK, FA2_ERR_INVALID_ARG (bytes NULL),
+ * FA2_ERR_UNSUPPORTED (D) or FA2_ERR_CUDA.
+ */
+int fa2_fwd_workspace_bytes(int D, size_t* bytes);
+
+/*
+ * fa2_fwd_ws — the same operation, arguments and results as fa2_fwd, with a
+ * caller-owned device workspace that lets the kernel balance work exactly
+ * across the SMs: each persistent CTA takes an equal share of all
+ * (query tile, K/V tile) steps, and a query tile whose K/V range is cut
+ * between CTAs is finished by merging fp32 partial results with the online
+ * (m, l) rule of "FlashAttention-2 MMA 代码学习", step 1 (the merge the
+ * pages apply across K/V blocks, here applied across CTAs).
+ *
+ * workspace: NULL (then this is exactly fa2_fwd), or a 16-byte aligned
+ *   device buffer of at least fa2_fwd_workspace_bytes(D) bytes that overlaps
+ *   no tensor. Its contents need no initialisation and are scratch after the
+ *   call; calls that share a workspace must not run concurrently on the GPU.
+ * The launch is cooperative (all CTAs resident); if that cannot be arranged
+ * the call returns FA2_ERR_CUDA.
+ * Errors as fa2_fwd, plus FA2_ERR_INVALID_ARG for a workspace that is too
+ * small or overlaps a tensor, FA2_ERR_ALIGN for a misaligned workspace.
+ */
+int fa2_fwd_ws(const void* Q, const void* K, const void* V, void* O, float* LSE,
+               int B, int H, int N, int D, float scale, int is_causal, int dtype,
+               void* workspace, size_t workspace_bytes, struct CUstream_st* stream);
 
 /*
  * fa2_device_status — read the device-side watchdog word of the current

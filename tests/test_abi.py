@@ -83,6 +83,23 @@ def test_bad_arguments_are_rejected_before_any_gpu_work(lib, over, code):
     assert call(lib, **over) == code
 
 
+def call_ws(lib, ws, ws_bytes, **over):
+    a = dict(GOOD)
+    a.update(over)
+    return lib.fa2_fwd_ws(a["Q"], a["K"], a["V"], a["O"], a["LSE"], a["B"], a["H"], a["N"], a["D"], a["scale"],
+                          a["is_causal"], a["dtype"], ws, ws_bytes, a["stream"])
+
+
+def test_workspace_variant_checks_its_arguments(lib):
+    assert call_ws(lib, A * 80 + 8, 1 << 20) == lib.FA2_ERR_ALIGN           # misaligned workspace
+    assert call_ws(lib, A * 48 + 256, 1 << 20) == lib.FA2_ERR_INVALID_ARG   # workspace overlaps O
+    assert call_ws(lib, A * 80, 1 << 20, D=96) == lib.FA2_ERR_UNSUPPORTED
+    assert call_ws(lib, None, 0, B=0) == lib.FA2_OK
+    n = ctypes.c_size_t(0)
+    assert lib.library().fa2_fwd_workspace_bytes(96, ctypes.byref(n)) == lib.FA2_ERR_UNSUPPORTED
+    assert lib.library().fa2_fwd_workspace_bytes(64, None) == lib.FA2_ERR_INVALID_ARG
+
+
 @pytest.mark.parametrize("over", [dict(B=0), dict(H=0), dict(N=0),
                                   dict(B=0, Q=None, K=None, V=None, O=None, LSE=None)])
 def test_empty_problem_is_a_no_op(lib, over):

@@ -31,18 +31,21 @@ def fa2():
     return m
 
 
-def run_gpu(fa2, q, k, v, w, out=None, lse=None, stream=None):
+SCHEDULES = ("units", "balanced")
+
+
+def run_gpu(fa2, q, k, v, w, out=None, lse=None, stream=None, schedule="balanced"):
     qd, kd, vd = (t.cuda() for t in (q, k, v))
     O, L = fa2.attention_forward(qd, kd, vd, scale=w.scale, is_causal=w.causal, out=out, lse=lse,
-                                 stream=stream)
+                                 stream=stream, schedule=schedule)
     torch.cuda.synchronize()
     assert fa2.fa2_device_status(clear=True) == 0, "device watchdog fired"
     return O, L
 
 
-def compare(fa2, oracle_mod, w, rows=None, sample=None):
+def compare(fa2, oracle_mod, w, rows=None, sample=None, schedule="balanced"):
     q, k, v = workloads.make_inputs(w)
-    O, L = run_gpu(fa2, q, k, v, w)
+    O, L = run_gpu(fa2, q, k, v, w, schedule=schedule)
     assert torch.isfinite(O).all().item(), "non-finite output"
     assert torch.isfinite(L).all().item(), "non-finite LSE"
     if sample is not None:
@@ -60,8 +63,9 @@ def compare(fa2, oracle_mod, w, rows=None, sample=None):
     return err_o, err_l
 
 
-def test_tiny_every_element(fa2, oracle_mod):
-    compare(fa2, oracle_mod, workloads.WORKLOADS["tiny"])
+@pytest.mark.parametrize("schedule", SCHEDULES)
+def test_tiny_every_element(fa2, oracle_mod, schedule):
+    compare(fa2, oracle_mod, workloads.WORKLOADS["tiny"], schedule=schedule)
 
 
 EDGE_N = [1, 7, 63, 64, 65, 127, 128, 129, 255, 256, 257, 383, 1000]
@@ -71,40 +75,56 @@ EDGE_N = [1, 7, 63, 64, 65, 127, 128, 129, 255, 256, 257, 383, 1000]
 @pytest.mark.parametrize("D", [64, 128])
 @pytest.mark.parametrize("dtype", ["f16", "bf16"])
 @pytest.mark.parametrize("causal", [False, True])
-def test_edge_shapes_every_element(fa2, oracle_mod, N, D, dtype, causal):
+@pytest.mark.parametrize("schedule", SCHEDULES)
+def test_edge_shapes_every_element(fa2, oracle_mod, N, D, dtype, causal, schedule):
     w = workloads.custom(1, 2, N, D, dtype, causal, seed=N * 7 + D)
-    compare(fa2, oracle_mod, w)
+    compare(fa2, oracle_mod, w, schedule=schedule)
 
 
-def test_ragged_tail_does_not_read_the_next_head(fa2, oracle_mod):
+@pytest.mark.parametrize("schedule", SCHEDULES)
+def test_ragged_tail_does_not_read_the_next_head(fa2, oracle_mod, schedule):
     # Rows past N of one head must read as zeros, never as the next head's rows.
     w = workloads.custom(2, 3, 65, 64, "f16", False, seed=99)
-    compare(fa2, oracle_mod, w)
+    compare(fa2, oracle_mod, w, schedule=schedule)
     w = workloads.custom(2, 3, 200, 128, "bf16", True, seed=98)
-    compare(fa2, oracle_mod, w)
+    compare(fa2, oracle_mod, w, schedule=schedule)
 
 
-def test_many_units_per_cta(fa2, oracle_mod):
+@pytest.mark.parametrize("schedule", SCHEDULES)
+def test_many_units_per_cta(fa2, oracle_mod, schedule):
     # More work units than SMs: each persistent CTA loops over several units.
     w = workloads.custom(4, 40, 512, 64, "bf16", False, seed=5)
-    compare(fa2, oracle_mod, w, sample=400)
+    compare(fa2, oracle_mod, w, sample=400, schedule=schedule)
     w = workloads.custom(3, 50, 700, 128, "f16", True, seed=6)
-    compare(fa2, oracle_mod, w, sample=400)
+    compare(fa2, oracle_mod, w, sample=400, schedule=schedule)
 
 
+@pytest.mark.parametrize("shape", [(1, 1, 4096, 128, False), (1, 1, 4096, 64, True), (1, 2, 3000, 128, True),
+                                   (1, 3, 2049, 64, False), (2, 1, 8192, 128, False)])
+def test_units_cut_across_many_ctas(fa2, oracle_mod, shape):
+    # Few K/V-tile steps per CTA: one query tile's K/V range is split over
+    # several CTAs and its owner merges several partials (every row checked).
+    B, H, N, D, causal = shape
+    w = workloads.custom(B, H, N, D, "bf16", causal, seed=N + D)
+    compare(fa2, oracle_mod, w, schedule="balanced")
+
+
+@pytest.mark.parametrize("schedule", SCHEDULES)
 @pytest.mark.parametrize("name", workloads.CONTRACT + ("target", "target_f16"))
-def test_contract_workloads_full_size(fa2, oracle_mod, name):
+def test_contract_workloads_full_size(fa2, oracle_mod, name, schedule):
     w = workloads.WORKLOADS[name]
     if w.B * w.H * w.N <= 4096:
-        compare(fa2, oracle_mod, w)
+        compare(fa2, oracle_mod, w, schedule=schedule)
     else:
-        compare(fa2, oracle_mod, w, sample=600)
+        compare(fa2, oracle_mod, w, sample=600, schedule=schedule)
 
 
-def test_peaked_logits_every_element(fa2, oracle_mod):
+@pytest.mark.parametrize("schedule", SCHEDULES)
+def test_peaked_logits_every_element(fa2, oracle_mod, schedule):
     # The ragged workload's Q/K ~ N(0, 3^2): sharply peaked rows, checked on every row.
     w = workloads.WORKLOADS["ragged"]
-    compare(fa2, oracle_mod, workloads.custom(w.B, 2, w.N, w.D, w.dtype, w.causal, w.seed, sigma_qk=3.0))
+    compare(fa2, oracle_mod, workloads.custom(w.B, 2, w.N, w.D, w.dtype, w.causal, w.seed, sigma_qk=3.0),
+            schedule=schedule)
 
 
 def test_outputs_fully_overwritten_and_deterministic(fa2, oracle_mod):
@@ -117,6 +137,9 @@ def test_outputs_fully_overwritten_and_deterministic(fa2, oracle_mod):
     assert torch.isfinite(O1).all().item() and torch.isfinite(L1).all().item()
     O2, L2 = run_gpu(fa2, q, k, v, w)
     assert torch.equal(O1, O2) and torch.equal(L1, L2)
+    O3, L3 = run_gpu(fa2, q, k, v, w, schedule="units")
+    O4, L4 = run_gpu(fa2, q, k, v, w, schedule="units")
+    assert torch.equal(O3, O4) and torch.equal(L3, L4)
 
 
 def test_runs_on_a_side_stream(fa2, oracle_mod):
