@@ -488,27 +488,38 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!got) { ok = false; break; }
         s_phase ^= 1u;
         tc_fence_after_sync();
-        uint32_t sr[128];
-        tmem_ld32x128_wait(tS, sr);
-        float s[128];
-#pragma unroll
-        for (int i = 0; i < 128; ++i) s[i] = __uint_as_float(sr[i]);
+        // Two passes over the S row in TMEM keep only two 32-column chunks in
+        // registers: pass 1 takes the row max, pass 2 re-reads each chunk,
+        // exponentiates it and writes P behind itself (P chunk c lands on
+        // columns [16c, 16c+16), which pass 2 has already read).
         const int kv0 = j * kKeys;
-        if (kv0 + kKeys > limit) {  // ragged tail and/or causal diagonal: mask disallowed keys
+        const bool masked = kv0 + kKeys > limit;  // ragged tail and/or causal diagonal
+        auto mask_chunk = [&](uint32_t (&v)[32], int c0) {
 #pragma unroll
-          for (int i = 0; i < 128; ++i)
-            if (kv0 + i >= limit) s[i] = -CUDART_INF_F;
+          for (int i = 0; i < 32; ++i)
+            if (kv0 + c0 + i >= limit) v[i] = __float_as_uint(-CUDART_INF_F);
+        };
+        float m_tile = -CUDART_INF_F;
+#pragma unroll
+        for (int c2 = 0; c2 < 4; c2 += 2) {
+          uint32_t va[32], vb[32];
+          tmem_ld32x32(tS + 32 * c2, va);
+          tmem_ld32x32(tS + 32 * (c2 + 1), vb);
+          tmem_wait_ld32(va);
+          tmem_wait_ld32(vb);
+          if (masked) {
+            mask_chunk(va, 32 * c2);
+            mask_chunk(vb, 32 * (c2 + 1));
+          }
+          float m0 = fmax3(__uint_as_float(va[0]), __uint_as_float(va[1]), __uint_as_float(va[2]));
+          float m1 = fmax3(__uint_as_float(vb[0]), __uint_as_float(vb[1]), __uint_as_float(vb[2]));
+#pragma unroll
+          for (int i = 3; i < 31; i += 2) {
+            m0 = fmax3(m0, __uint_as_float(va[i]), __uint_as_float(va[i + 1]));
+            m1 = fmax3(m1, __uint_as_float(vb[i]), __uint_as_float(vb[i + 1]));
+          }
+          m_tile = fmax3(m_tile, fmaxf(m0, __uint_as_float(va[31])), fmaxf(m1, __uint_as_float(vb[31])));
         }
-        // row max: four independent chains of 3-input maxima
-        float mx[4];
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          mx[q] = fmax3(s[32 * q], s[32 * q + 1], s[32 * q + 2]);
-#pragma unroll
-          for (int i = 3; i < 31; i += 2) mx[q] = fmax3(mx[q], s[32 * q + i], s[32 * q + i + 1]);
-          mx[q] = fmaxf(mx[q], s[32 * q + 31]);
-        }
-        const float m_tile = fmaxf(fmax3(mx[0], mx[1], mx[2]), mx[3]);
         m_raw = fmaxf(m_raw, m_tile);
         // Move the exponent base only when the max has grown by more than
         // kRescaleLog2 (or on the first tile); otherwise keep the old base, so
@@ -538,16 +549,34 @@ __global__ void __launch_bounds__(kThreads, 1)
         // first 64 keys while the second half is exponentiated.
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
-          uint32_t pk[32];
+          uint32_t va[32], vb[32];
+          tmem_ld32x32(tS + 64 * h, va);
+          tmem_ld32x32(tS + 64 * h + 32, vb);
+          tmem_wait_ld32(va);
+          tmem_wait_ld32(vb);
+          if (masked) {
+            mask_chunk(va, 64 * h);
+            mask_chunk(vb, 64 * h + 32);
+          }
+          uint32_t pk[16];
 #pragma unroll
-          for (int i = 0; i < 32; ++i) {
+          for (int i = 0; i < 16; ++i) {
             float x0, x1;
-            ffma2_bcast(x0, x1, s[64 * h + 2 * i], s[64 * h + 2 * i + 1], c, nb);
+            ffma2_bcast(x0, x1, __uint_as_float(va[2 * i]), __uint_as_float(va[2 * i + 1]), c, nb);
             const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
             fadd2_acc(acc[2 * (i & 3)], acc[2 * (i & 3) + 1], p0, p1);
             pk[i] = pack2(p0, p1, kBf16);
           }
-          tmem_st32x32(tS + 32 * h, pk);
+          tmem_st32x16(tS + 32 * h, pk);
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            float x0, x1;
+            ffma2_bcast(x0, x1, __uint_as_float(vb[2 * i]), __uint_as_float(vb[2 * i + 1]), c, nb);
+            const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
+            fadd2_acc(acc[2 * (i & 3)], acc[2 * (i & 3) + 1], p0, p1);
+            pk[i] = pack2(p0, p1, kBf16);
+          }
+          tmem_st32x16(tS + 32 * h + 16, pk);
           tmem_wait_st();
           tc_fence_before_sync();
           mbar_arrive(bar_p + 8 * h);
