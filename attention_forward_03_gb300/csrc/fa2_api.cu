@@ -218,6 +218,14 @@ int launch(const void* Q, const void* K, const void* V, void* O, float* LSE, int
 
 }  // namespace
 
+namespace fa2 {
+int launch_forward(const void* Q, const void* K, const void* V, void* O, float* LSE, int B, int H, int N, int D,
+                   float scale, int is_causal, int dtype, void* workspace, size_t workspace_bytes,
+                   cudaStream_t stream) {
+  return ::launch(Q, K, V, O, LSE, B, H, N, D, scale, is_causal, dtype, workspace, workspace_bytes, stream);
+}
+}  // namespace fa2
+
 extern "C" int fa2_fwd(const void* Q, const void* K, const void* V, void* O, float* LSE, int B, int H, int N,
                        int D, float scale, int is_causal, int dtype, struct CUstream_st* stream) {
   return launch(Q, K, V, O, LSE, B, H, N, D, scale, is_causal, dtype, nullptr, 0,

@@ -37,10 +37,17 @@ struct Params {
 };
 
 // Bytes of stream-K workspace for `grid` CTAs at head dimension d.
-inline size_t stream_k_workspace_bytes(int grid, int d) {
-  const size_t per = 2ull * (static_cast<size_t>(d) * 128 + 3 * 128) * sizeof(float);
-  return (static_cast<size_t>(grid) * per + 255) / 256 * 256 + static_cast<size_t>(grid) * 2 * 8;
+constexpr size_t stream_k_workspace_bytes(int grid, int d) {
+  return (static_cast<size_t>(grid) * (2ull * (static_cast<size_t>(d) * 128 + 3 * 128) * sizeof(float)) + 255) /
+             256 * 256 +
+         static_cast<size_t>(grid) * 2 * 8;
 }
+
+// The full forward call (validation, tensor maps, launch) with an optional
+// stream-K workspace; the C entry points are thin wrappers around it.
+int launch_forward(const void* Q, const void* K, const void* V, void* O, float* LSE, int B, int H, int N, int D,
+                   float scale, int is_causal, int dtype, void* workspace, size_t workspace_bytes,
+                   cudaStream_t stream);
 
 template <int D, bool kBf16, bool kCausal>
 cudaError_t launch_fwd(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v, const Params& p,

@@ -107,6 +107,33 @@ int fa2_fwd_ws(const void* Q, const void* K, const void* V, void* O, float* LSE,
                void* workspace, size_t workspace_bytes, struct CUstream_st* stream);
 
 /*
+ * fa2_fwd_noalloc — the same operation, arguments and results as fa2_fwd,
+ * with the balanced (stream-K) schedule of fa2_fwd_ws, for callers that
+ * cannot allocate device memory: code that must not call cudaMalloc, for
+ * instance because its host application owns all device memory through a
+ * fixed pool or arena and allows no other allocation, or because it runs on a
+ * latency-critical path where an allocation and the device synchronisation
+ * it implies are not acceptable. It calls no allocation routine. The pages
+ * have no counterpart to this entry point.
+ *
+ * Its scratch is one static device array of this library, 21,465,600 bytes,
+ * held on every GPU that loads the library until the process exits. It
+ * covers devices of up to 160 SMs at head dimension 64 or 128; a device with
+ * more SMs is refused with FA2_ERR_UNSUPPORTED.
+ * The first call on each device looks up the array's device address (with
+ * that device current); make that first call before any stream capture.
+ * All calls share the array and it keeps the last call's contents. Nothing
+ * in it has to start at zero: each launch tags its partial results with a
+ * unique value, so leftovers of earlier calls are never read. Calls that
+ * overlap on the GPU (on different streams, or on different host threads
+ * without ordering) race on the array and must not be made.
+ * Errors as fa2_fwd.
+ */
+int fa2_fwd_noalloc(const void* Q, const void* K, const void* V, void* O, float* LSE,
+                    int B, int H, int N, int D, float scale, int is_causal, int dtype,
+                    struct CUstream_st* stream);
+
+/*
  * fa2_device_status — read the device-side watchdog word of the current
  * device, synchronising `stream` first. *status receives 0 when no kernel of
  * this library has timed out waiting on one of its internal barriers since

@@ -100,6 +100,17 @@ def test_workspace_variant_checks_its_arguments(lib):
     assert lib.library().fa2_fwd_workspace_bytes(64, None) == lib.FA2_ERR_INVALID_ARG
 
 
+def test_no_alloc_entry_point_checks_arguments_first(lib):
+    so = lib.library()
+    a = dict(GOOD)
+    args = lambda **o: [dict(a, **o)[x] for x in ("Q", "K", "V", "O", "LSE", "B", "H", "N", "D", "scale",
+                                                   "is_causal", "dtype", "stream")]  # noqa: E731
+    assert so.fa2_fwd_noalloc(*args(B=-1)) == lib.FA2_ERR_INVALID_ARG
+    assert so.fa2_fwd_noalloc(*args(D=96)) == lib.FA2_ERR_UNSUPPORTED
+    assert so.fa2_fwd_noalloc(*args(dtype=5)) == lib.FA2_ERR_UNSUPPORTED
+    assert so.fa2_fwd_noalloc(*args(N=0)) == lib.FA2_OK
+
+
 @pytest.mark.parametrize("over", [dict(B=0), dict(H=0), dict(N=0),
                                   dict(B=0, Q=None, K=None, V=None, O=None, LSE=None)])
 def test_empty_problem_is_a_no_op(lib, over):
