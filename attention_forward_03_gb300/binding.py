@@ -36,6 +36,7 @@ SIGNATURES = {
                                        ctypes.c_int, ctypes.c_float, ctypes.c_int, ctypes.c_int, _VP]),
     "fa2_device_status": (ctypes.c_int, [_VP, ctypes.POINTER(ctypes.c_int), ctypes.c_int]),
     "fa2_set_watchdog_ns": (ctypes.c_int, [ctypes.c_ulonglong]),
+    "fa2_test_withhold_next_load": (ctypes.c_int, [ctypes.c_int]),
     "fa2_error_string": (ctypes.c_char_p, [ctypes.c_int]),
     "fa2_last_cuda_error": (ctypes.c_char_p, []),
     "fa2_version": (ctypes.c_int, []),
@@ -139,15 +140,36 @@ def workspace_for(device, D: int):
     return ws
 
 
+UNIT_ROWS = 256  # query rows per work unit of the kernel
+
+
+def choose_schedule(B: int, H: int, N: int, is_causal: bool, sms: int) -> str:
+    """Pick the kernel schedule for a problem (a choice between two C entry points).
+
+    The balanced schedule (fa2_fwd_ws) splits work exactly across the SMs at the
+    cost of a partial-result merge per CTA; it pays off only for non-causal work
+    of at least one unit per SM whose last round of whole units would leave more
+    than 8% of the SMs idle. Causal work is already balanced by the round
+    schedule's heaviest-first zig-zag, and small problems are dominated by the
+    fixed per-segment cost, so both use the round schedule (fa2_fwd).
+    """
+    units = B * H * -(-N // UNIT_ROWS)
+    if is_causal or units < sms:
+        return "units"
+    rounds = -(-units // sms)
+    return "balanced" if units / (rounds * sms) < 0.92 else "units"
+
+
 def attention_forward(q, k, v, scale: float | None = None, is_causal: bool = False, out=None, lse=None,
-                      stream=None, schedule: str = "balanced", workspace=None):
+                      stream=None, schedule: str = "auto", workspace=None):
     """FlashAttention-2 forward over torch CUDA tensors [B, H, N, D] (fp16/bf16).
 
     Returns (O, LSE): O like q, LSE float32 [B, H, N]. `out` / `lse` may be
     passed to write into caller-owned buffers. Runs on `stream` (a
     torch.cuda.Stream) or the current stream.
-    schedule: "balanced" (fa2_fwd_ws with a workspace: equal work per SM) or
-    "units" (fa2_fwd: whole query tiles per CTA, no workspace).
+    schedule: "auto" (choose_schedule), "balanced" (fa2_fwd_ws with a
+    workspace: equal work per SM) or "units" (fa2_fwd: whole query tiles per
+    CTA, no workspace).
     workspace: optional uint8 CUDA tensor for the balanced schedule; by default
     a cached one per device is used.
     """
@@ -160,9 +182,12 @@ def attention_forward(q, k, v, scale: float | None = None, is_causal: bool = Fal
         raise ValueError("q, k, v must share one dtype")
     if not (q.is_contiguous() and k.is_contiguous() and v.is_contiguous()):
         raise ValueError("q, k, v must be contiguous")
-    if schedule not in ("balanced", "units"):
-        raise ValueError("schedule must be 'balanced' or 'units'")
+    if schedule not in ("auto", "balanced", "units"):
+        raise ValueError("schedule must be 'auto', 'balanced' or 'units'")
     B, H, N, D = q.shape
+    if schedule == "auto":
+        sms = torch.cuda.get_device_properties(q.device).multi_processor_count
+        schedule = choose_schedule(B, H, N, is_causal, sms)
     if scale is None:
         scale = 1.0 / math.sqrt(D)
     if out is None:

@@ -27,6 +27,7 @@ constexpr unsigned long long kDefaultWatchdogNs = 1000000000ull;
 __device__ int g_watchdog_word;  // 0 = no timeout since last clear
 
 std::atomic<unsigned long long> g_watchdog_ns{kDefaultWatchdogNs};
+std::atomic<int> g_test_withhold{0};
 thread_local char t_last_cuda_error[256] = "";
 
 struct DeviceInfo {
@@ -186,6 +187,7 @@ int launch(const void* Q, const void* K, const void* V, void* O, float* LSE, int
   p.num_units = (int)(bh * n_qt);
   p.nkv_full = (N + kKeys - 1) / kKeys;
   p.scale_log2 = scale * 1.4426950408889634f;
+  p.test_withhold = g_test_withhold.exchange(0, std::memory_order_relaxed);
   // K/V-tile steps of one head: non-causal n_qt * nkv_full; causal sum of
   // min(2qt+2, nkv_full) over the head's query units.
   long long per_head = 0;
@@ -275,6 +277,11 @@ extern "C" int fa2_device_status(struct CUstream_st* stream, int* status, int cl
 
 extern "C" int fa2_set_watchdog_ns(unsigned long long ns) {
   g_watchdog_ns.store(ns ? ns : kDefaultWatchdogNs, std::memory_order_relaxed);
+  return FA2_OK;
+}
+
+extern "C" int fa2_test_withhold_next_load(int enable) {
+  g_test_withhold.store(enable ? 1 : 0, std::memory_order_relaxed);
   return FA2_OK;
 }
 

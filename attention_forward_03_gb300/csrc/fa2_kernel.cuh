@@ -340,6 +340,10 @@ __global__ void __launch_bounds__(kThreads, 1)
               ok = false;
               break;
             }
+            if (p.test_withhold && it == 0) {  // test hook: this tile never arrives
+              ++it;
+              continue;
+            }
             mbar_arrive_expect_tx(bar_full(slot), L::kTileBytes);
             const CUtensorMap* map = kv ? &tmV : &tmK;
             for (int pn = 0; pn < L::kPanels; ++pn)

@@ -34,6 +34,7 @@ struct Params {
   float* ws_stats;          // [G][2][3][128] base, l, l_o of each partial row
   unsigned long long* ws_flags;  // [G][2] = epoch once that partial is written
   unsigned long long epoch; // unique tag of this launch
+  int test_withhold;        // test hook: the producer withholds its first K/V tile
 };
 
 // Bytes of stream-K workspace for `grid` CTAs at head dimension d.

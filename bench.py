@@ -263,6 +263,10 @@ def run_gb300(args, w, rank, world, local):
     stream = torch.cuda.current_stream(dev)
 
     q, k, v = workloads.make_inputs(w)
+    resolved_schedule = args.schedule
+    if resolved_schedule == "auto":
+        resolved_schedule = fa2.binding.choose_schedule(w.B, w.H, w.N, w.causal,
+                                                        torch.cuda.get_device_properties(dev).multi_processor_count)
     set_bytes = workloads.algorithmic_bytes(w)
     l2 = getattr(torch.cuda.get_device_properties(dev), "L2_cache_size", 128 * 2 ** 20)
     nsets = max(2, math.ceil(2 * l2 / set_bytes))
@@ -356,7 +360,7 @@ def run_gb300(args, w, rank, world, local):
         "scaling": "weak", "vs_baseline": None, "dtype": w.dtype,
         "data": "synthetic (seeded N(0, sigma^2) inputs, cast to the workload's 16-bit dtype)",
         "config": {"workload": w.describe(), "B": w.B, "H": w.H, "N": w.N, "D": w.D, "causal": w.causal,
-                   "scale": "1/sqrt(D)", "schedule": args.schedule,
+                   "scale": "1/sqrt(D)", "schedule": resolved_schedule,
                    "parallelism": f"weak x{world} (one independent replica per GPU)",
                    "l2": f"inputs rotate over {nsets} copies ({nsets * set_bytes / 2**20:.0f} MiB > 2x L2)"},
         "pct_of_peak": 100.0 * achieved / peak,
@@ -383,8 +387,9 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--workload", default="target", choices=sorted(workloads.WORKLOADS))
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
-    ap.add_argument("--schedule", default="balanced", choices=["balanced", "units"],
-                    help="balanced: fa2_fwd_ws (equal K/V-tile steps per SM); units: fa2_fwd")
+    ap.add_argument("--schedule", default="auto", choices=["auto", "balanced", "units"],
+                    help="auto: the binding's choice; balanced: fa2_fwd_ws (equal K/V-tile steps per SM); "
+                         "units: fa2_fwd")
     ap.add_argument("--settle-seconds", type=float, default=1.0)
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--reference-seconds", type=float, default=120.0,

@@ -151,6 +151,16 @@ int fa2_device_status(struct CUstream_st* stream, int* status, int clear);
  */
 int fa2_set_watchdog_ns(unsigned long long ns);
 
+/*
+ * fa2_test_withhold_next_load — test hook for the watchdog. When enable is
+ * nonzero, the next launch of this library (process-wide, one launch only)
+ * withholds its first K/V tile: the waits for that tile run out after the
+ * watchdog time, the kernel records the wait site in the watchdog word,
+ * winds down without leaving work in flight, and O/LSE are left unspecified.
+ * No GPU fault, trap or hang is involved. Returns FA2_OK.
+ */
+int fa2_test_withhold_next_load(int enable);
+
 /* Human-readable text for a status code (static storage, never NULL). */
 const char* fa2_error_string(int code);
 

@@ -147,3 +147,12 @@ def test_product_never_imports_the_oracle():
                 text = open(os.path.join(dirpath, f), encoding="utf-8").read()
                 assert not re.search(r"^\s*(import|from)\s+oracle\b", text, flags=re.M), f
                 assert "fa2_oracle" not in text, f
+
+
+def test_schedule_choice():
+    from attention_forward_03_gb300.binding import choose_schedule
+    assert choose_schedule(1, 8, 8192, False, 152) == "balanced"   # 256 units: last round 68% busy
+    assert choose_schedule(4, 16, 8192, False, 152) == "units"     # 2048 units: 96% of rounds busy
+    assert choose_schedule(1, 8, 8192, True, 152) == "units"       # causal: zig-zag rounds
+    assert choose_schedule(2, 12, 1000, False, 152) == "units"     # fewer units than SMs
+    assert choose_schedule(1, 152, 256, False, 152) == "units"     # exactly one full round

@@ -1,0 +1,50 @@
+"""The device watchdog, exercised without any GPU fault.
+
+A test hook makes the next launch withhold its first K/V tile, so the waits
+for it run out after a short watchdog time. The kernel must record the wait
+site in the status word, wind down, and leave the context usable: a normal
+launch right after must still match the oracle.
+"""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+import torch
+
+import workloads
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def fa2():
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    from attention_forward_03_gb300 import build
+    build.build()
+    import attention_forward_03_gb300 as m
+    m.fa2_device_status(clear=True)
+    return m
+
+
+def test_withheld_tile_times_out_and_the_context_stays_usable(fa2, oracle_mod):
+    w = workloads.custom(1, 4, 512, 128, "bf16", False, seed=77)
+    q, k, v = (t.cuda() for t in workloads.make_inputs(w))
+    lib = fa2.library()
+    try:
+        fa2.fa2_set_watchdog_ns(20_000_000)  # 20 ms
+        assert lib.fa2_test_withhold_next_load(1) == fa2.FA2_OK
+        fa2.attention_forward(q, k, v, scale=w.scale, schedule="units")
+        torch.cuda.synchronize()  # returns: every wait in the kernel is bounded
+        status = fa2.fa2_device_status(clear=True)
+        assert status != 0, "the withheld tile should have made a wait run out"
+        assert fa2.fa2_device_status() == 0  # cleared
+    finally:
+        lib.fa2_test_withhold_next_load(0)
+        fa2.fa2_set_watchdog_ns(0)
+    # the hook applied to one launch only; the next one is normal and right
+    O, L = fa2.attention_forward(q, k, v, scale=w.scale, schedule="units")
+    torch.cuda.synchronize()
+    assert fa2.fa2_device_status(clear=True) == 0
+    Oref, Lref = oracle_mod.attention_fwd(q.cpu(), k.cpu(), v.cpu(), w.scale, False)
+    assert np.abs(O.float().cpu().numpy() - Oref).max() <= 1e-2
+    assert np.abs(L.cpu().numpy() - Lref).max() <= 1e-3
