@@ -365,33 +365,49 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       constexpr uint32_t idesc_s = make_idesc_f16(kBf16, kKeys, false);
       constexpr uint32_t idesc_o = make_idesc_f16(kBf16, D, true);
-      const uint32_t tS[2] = {tmem + 0u, tmem + (uint32_t)kKeys};
-      const uint32_t tO[2] = {tmem + L::kColO, tmem + L::kColO + (uint32_t)D};
+      // Descriptor low words advance by compile-time offsets (the start
+      // address field never carries: shared memory stays below 256 KB); the
+      // high words are constants.
+      constexpr uint32_t kHi = desc_hi_sw128(1024);  // 8-row (K-major) / 8-key (MN-major) groups 1 KB apart
+      const uint32_t q_lo = desc_lo_sw128(sQ, 16);
+      const uint32_t ring_lo = desc_lo_sw128(sRing, 16);
+      const uint32_t ring_lo_v = desc_lo_sw128(sRing, kPanelBytes);  // V: 64-column panels 16 KB apart
 
       // S_t = Q_t K^T : D/16 steps of K=16 along the head dimension.
       auto issue_s = [&](int t, int slot) {
-        const uint32_t qa = sQ + t * L::kTileBytes;
-        const uint32_t ka = sRing + slot * L::kTileBytes;
+        const uint32_t qa = q_lo + static_cast<uint32_t>((t * L::kTileBytes) >> 4);
+        const uint32_t ka = ring_lo + static_cast<uint32_t>(slot * (L::kTileBytes >> 4));
+        const uint32_t dt = tmem + static_cast<uint32_t>(t * kKeys);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * kPanelBytes + (kk & 3) * 32;
-          mma_ss(tS[t], smem_desc_sw128(qa + off, 16, 1024), smem_desc_sw128(ka + off, 16, 1024),
-                 idesc_s, kk > 0 ? 1u : 0u);
+          const uint32_t off = static_cast<uint32_t>(((kk >> 2) * kPanelBytes + (kk & 3) * 32) >> 4);
+          mma_ss_w(dt, qa + off, kHi, ka + off, kHi, idesc_s, kk > 0 ? 1u : 0u);
         }
       };
       // O_t (+)= P_t V over keys [64h, 64h+64): P from TMEM (16-bit pairs), V from
       // shared memory (MN-major).
       auto issue_pv_half = [&](int t, int slot, int h, bool acc) {
-        const uint32_t va = sRing + slot * L::kTileBytes;
+        const uint32_t va = ring_lo_v + static_cast<uint32_t>(slot * (L::kTileBytes >> 4));
+        const uint32_t dt = tmem + L::kColO + static_cast<uint32_t>(t * D);
+        const uint32_t pt = tmem + static_cast<uint32_t>(t * kKeys);
 #pragma unroll
         for (int k4 = 0; k4 < kKeys / 32; ++k4) {
           const int kk = h * (kKeys / 32) + k4;
-          mma_ts(tO[t], tS[t] + kk * 8, smem_desc_sw128(va + kk * 16 * 128, kPanelBytes, 1024),
-                 idesc_o, (acc || kk > 0) ? 1u : 0u);
+          mma_ts_w(dt, pt + kk * 8, va + static_cast<uint32_t>((kk * 16 * 128) >> 4), kHi, idesc_o,
+                   (acc || kk > 0) ? 1u : 0u);
         }
       };
 
-      uint32_t it = 0, q_round = 0;
+      // ring position: slot and the parity of its current use
+      int slot = 0;
+      uint32_t ring_ph = 0;
+      auto advance = [&]() {
+        if (++slot == L::kStages) {
+          slot = 0;
+          ring_ph ^= 1u;
+        }
+      };
+      uint32_t q_round = 0;
       uint32_t p_phase[2] = {0u, 0u};  // both halves of a sub-tile flip together
       bool ok = true;
       SegCursor cur = first_cursor(p);
@@ -399,34 +415,35 @@ __global__ void __launch_bounds__(kThreads, 1)
       while (ok && next_segment<kCausal>(cur, w, p)) {
         if (!wait_bounded(bar_q_full, q_round & 1u, wd, kSiteMmaQFull)) { ok = false; break; }
         ++q_round;
-        int slot_k = it % L::kStages;
-        if (!wait_bounded(bar_full(slot_k), (it / L::kStages) & 1u, wd, kSiteMmaRingFull)) {
+        int slot_k = slot;
+        if (!wait_bounded(bar_full(slot_k), ring_ph, wd, kSiteMmaRingFull)) {
           ok = false;
           break;
         }
+        advance();
         tc_fence_after_sync();
         issue_s(0, slot_k);
         mma_commit(bar_s_full0);
         issue_s(1, slot_k);
         mma_commit(bar_s_full0 + 8);
         mma_commit(bar_empty(slot_k));
-        ++it;
         if (w.kv_end - w.kv_begin == 1) mma_commit(bar_q_empty);
 
         for (int j = w.kv_begin; j < w.kv_end; ++j) {
-          const int slot_v = it % L::kStages;
-          if (!wait_bounded(bar_full(slot_v), (it / L::kStages) & 1u, wd, kSiteMmaRingFull)) {
+          const int slot_v = slot;
+          if (!wait_bounded(bar_full(slot_v), ring_ph, wd, kSiteMmaRingFull)) {
             ok = false;
             break;
           }
-          ++it;
+          advance();
           const bool next = j + 1 < w.kv_end;
           if (next) {
-            slot_k = it % L::kStages;
-            if (!wait_bounded(bar_full(slot_k), (it / L::kStages) & 1u, wd, kSiteMmaRingFull)) {
+            slot_k = slot;
+            if (!wait_bounded(bar_full(slot_k), ring_ph, wd, kSiteMmaRingFull)) {
               ok = false;
               break;
             }
+            advance();
           }
 #pragma unroll
           for (int t = 0; t < 2; ++t) {
@@ -434,14 +451,9 @@ __global__ void __launch_bounds__(kThreads, 1)
               ok = false;
               break;
             }
-            tc_fence_after_sync();
-            issue_pv_half(t, slot_v, 0, j > w.kv_begin);
-            if (!wait_bounded(bar_p_full0 + 16 * t + 8, p_phase[t], wd, kSiteMmaPFull)) {
-              ok = false;
-              break;
-            }
             p_phase[t] ^= 1u;
             tc_fence_after_sync();
+            issue_pv_half(t, slot_v, 0, j > w.kv_begin);
             issue_pv_half(t, slot_v, 1, true);
             if (!next) mma_commit(bar_o_full0 + 8 * t);
             if (t == 1) mma_commit(bar_empty(slot_v));
@@ -453,7 +465,6 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (!ok) break;
           if (next) {
             mma_commit(bar_empty(slot_k));
-            ++it;
             if (j + 2 == w.kv_end) mma_commit(bar_q_empty);
           }
         }
@@ -581,10 +592,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             pk[i] = pack2(p0, p1, kBf16);
           }
           tmem_st32x16(tS + 32 * h + 16, pk);
-          tmem_wait_st();
-          tc_fence_before_sync();
-          mbar_arrive(bar_p + 8 * h);
         }
+        tmem_wait_st();
+        tc_fence_before_sync();
+        mbar_arrive(bar_p);
         const float lt = ((acc[0] + acc[1]) + (acc[2] + acc[3])) + ((acc[4] + acc[5]) + (acc[6] + acc[7]));
         // P.V uses p rounded to 16 bits. With the base lagging the max, the
         // tile's largest p is not a power of two, so its rounding would leave
