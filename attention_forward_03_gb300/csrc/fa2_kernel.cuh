@@ -15,17 +15,26 @@
 //   work unit  = 256 query rows of one (batch, head): two 128-row sub-tiles.
 //   warps 0-3  softmax warpgroup for sub-tile 0 (thread = query row = TMEM lane)
 //   warps 4-7  softmax warpgroup for sub-tile 1
-//   warp  8    tcgen05 MMA issuer (one thread) and TMEM owner
-//   warp  9    TMA producer (one thread)
+//   warps 8-9  tcgen05 MMA issuers: with two issuers warp 8 + t drives
+//              sub-tile t, with one issuer warp 8 drives both; warp 8 also
+//              owns the TMEM allocation
+//   warp  10   TMA producer (one thread); warp 11 idle. Warps 8-11 form the
+//              third warpgroup, which gives registers to the softmax ones.
 // Tensor memory (512 columns x 128 lanes of 32 bits):
-//   [0,128)    S0: scores of sub-tile 0 (fp32); P0 (16-bit pairs) is written
-//              back over its first 64 columns
-//   [128,256)  S1 / P1 likewise for sub-tile 1
-//   [256,256+D)       O0 accumulator (fp32)
-//   [256+D,256+2D)    O1 accumulator
-// Shared memory: Q (2 sub-tiles, resident for the unit) and a ring of K/V
-// tiles (K_j, V_j, K_j+1, ...), all 128-byte swizzled by TMA in 128-row x
-// 64-element panels, which is also the operand layout the MMAs read.
+//   [128t, 128t+128)      S of sub-tile t (fp32 scores)
+//   [256+tD, 256+tD+D)    O accumulator of sub-tile t (fp32)
+// Shared memory: Q (2 sub-tiles, resident for the segment), P (2 sub-tiles,
+// 16-bit), and a ring of K/V tiles; all 128-byte swizzled in 64-element-wide
+// panels, the operand layout the MMAs read (TMA writes Q/K/V that way; the
+// softmax threads write P that way).
+//
+// Per K/V tile j the MMA issuer of sub-tile t issues:
+//   S_t(j+1) = Q_t K_{j+1}^T   once softmax t has loaded S_t(j) into registers
+//   O_t (+)= P_t(j) V_j        once softmax t has written P_t(j) to shared memory
+// P lives in shared memory, so the next scores are computed while the softmax
+// of the current tile runs: each softmax warpgroup works tile after tile
+// without waiting for a P.V product. Rescaling O (rare: the exponent base
+// lags the row max by up to 2^8) waits for the previous P.V explicitly.
 //
 // Schedules. Work is a sequence of segments: K/V tiles [kv_begin, kv_end) of
 // one unit. With the round schedule every segment is a whole unit. With the
@@ -35,14 +44,6 @@
 // results the following CTAs wrote for the rest of the unit (each as the
 // first segment of its share) before writing O and LSE. Partials carry their
 // own exponent base and are combined with the usual (m, l) merge.
-//
-// Per K/V tile j the MMA thread issues, for each sub-tile t in turn:
-//   O_t (+)= P_t(j) V_j      once softmax t has published P_t(j)
-//   S_t    = Q_t K_{j+1}^T   right after, into the same TMEM columns
-// Tensor-core ops issued by one thread run in issue order, so S_t(j+1) never
-// overwrites P_t(j) before the P.V product has read it, and the completion of
-// S_t(j+1) implies that of P_t(j).V_j: the softmax warpgroup may rescale O_t
-// as soon as it sees S_t(j+1).
 #pragma once
 #include <cuda.h>
 #include <cuda_bf16.h>
@@ -57,10 +58,22 @@
 
 namespace fa2 {
 
-constexpr int kThreads = 320;
-constexpr int kMmaWarp = 8;
-constexpr int kLoadWarp = 9;
+constexpr int kThreads = 384;     // 3 warpgroups
+constexpr int kMmaWarp = 8;       // first MMA issuer warp
+constexpr int kLoadWarp = 10;
+// Two MMA issuers, one per sub-tile: a thread issuing tcgen05.mma is held
+// until the tensor core takes each instruction (~90-110 cycles for these
+// M=128 x N=128 x K=16 steps), so one thread cannot keep the tensor core busy.
+constexpr int kIssuers = 2;
+// Registers: the launch gives every thread kLaunchRegs (= 65536 / 384 rounded
+// down to 8); the softmax warpgroups then take kSoftmaxRegs and the third
+// warpgroup gives back down to kControlRegs. The split must add up exactly.
+constexpr int kLaunchRegs = 168;
+constexpr int kSoftmaxRegs = 224;
+constexpr int kControlRegs = 56;
+static_assert(2 * kSoftmaxRegs + kControlRegs == 3 * kLaunchRegs, "register split must match the launch");
 constexpr int kPanelBytes = 128 * 128;  // 128 rows x 64 16-bit elements
+constexpr int kPTileBytes = 2 * kPanelBytes;  // P of one sub-tile: 128 rows x 128 keys
 constexpr uint32_t kTmemCols = 512;
 // The exponent base of a row moves only when its max exceeds the base by more
 // than this many powers of two (so p <= 2^8 = 256, exact in the 16-bit P and
@@ -79,19 +92,22 @@ enum : int {
   kSiteDrain = 8,
   kSitePartialWrite = 9,
   kSitePartialFlag = 10,
+  kSiteMmaSFree = 11,
+  kSiteSoftmaxPFree = 12,
 };
 
 template <int D>
 struct Layout {
   static constexpr int kPanels = D / 64;
-  static constexpr int kTileBytes = kPanels * kPanelBytes;
-  static constexpr int kStages = (D == 128) ? 5 : 8;
+  static constexpr int kTileBytes = kPanels * kPanelBytes;  // 128 rows x D (Q sub-tile, K or V tile)
+  static constexpr int kStages = (D == 128) ? 3 : 8;
   static constexpr int kQBytes = kSubTiles * kTileBytes;
-  static constexpr int kRingOffset = kQBytes;
+  static constexpr int kPOffset = kQBytes;
+  static constexpr int kRingOffset = kPOffset + kSubTiles * kPTileBytes;
   static constexpr int kBarOffset = kRingOffset + kStages * kTileBytes;
-  // barriers: q_full, q_empty, ring full[S], ring empty[S], s_full[2], p_full[2][2 halves], o_full[2],
-  // drain, part_done[2]
-  static constexpr int kNumBars = 2 + 2 * kStages + 8 + 1 + 2;
+  // barriers: q_full, q_empty, ring full[S], ring empty[S], s_full[2], s_free[2], p_full[2], p_free[2],
+  // o_full[2], drain[2], part_done[2]
+  static constexpr int kNumBars = 2 + 2 * kStages + 2 * 7;
   static constexpr int kMiscOffset = kBarOffset + kNumBars * 8;
   static constexpr int kSmemBytes = kMiscOffset + 16 + 1024;  // + slack for 1 KB alignment
   static constexpr uint32_t kColO = 2 * kKeys;                 // O0 at 256, O1 at 256 + D
@@ -247,6 +263,7 @@ __device__ __forceinline__ uint32_t pack2(float lo, float hi, bool bf16) {
   }
 }
 
+
 template <int D, bool kBf16, bool kCausal>
 __global__ void __launch_bounds__(kThreads, 1)
     fa2_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
@@ -258,17 +275,20 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* smem = smem_raw + (base - raw);
 
   const uint32_t sQ = base;
+  const uint32_t sP = base + L::kPOffset;
   const uint32_t sRing = base + L::kRingOffset;
   const uint32_t bars = base + L::kBarOffset;
   const uint32_t bar_q_full = bars;
   const uint32_t bar_q_empty = bars + 8;
   auto bar_full = [&](int s) { return bars + 16 + 8u * s; };
   auto bar_empty = [&](int s) { return bars + 16 + 8u * (L::kStages + s); };
-  const uint32_t bar_s_full0 = bars + 16 + 16u * L::kStages;
-  const uint32_t bar_p_full0 = bar_s_full0 + 16;  // [sub-tile][half] at + 16*t + 8*h
-  const uint32_t bar_o_full0 = bar_p_full0 + 32;
-  const uint32_t bar_drain = bar_o_full0 + 16;
-  const uint32_t bar_part0 = bar_drain + 8;  // [sub-tile]
+  const uint32_t bar_s_full0 = bars + 16 + 16u * L::kStages;  // [sub-tile]
+  const uint32_t bar_s_free0 = bar_s_full0 + 16;              // [sub-tile]
+  const uint32_t bar_p_full0 = bar_s_free0 + 16;              // [sub-tile]
+  const uint32_t bar_p_free0 = bar_p_full0 + 16;              // [sub-tile]
+  const uint32_t bar_o_full0 = bar_p_free0 + 16;              // [sub-tile]
+  const uint32_t bar_drain = bar_o_full0 + 16;                // [issuer]
+  const uint32_t bar_part0 = bar_drain + 16;                  // [sub-tile]
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kMiscOffset);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kMiscOffset + 4);
 
@@ -277,20 +297,20 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (threadIdx.x == 0) {
     mbar_init(bar_q_full, 1);
-    mbar_init(bar_q_empty, 1);
+    mbar_init(bar_q_empty, kIssuers);
     for (int s = 0; s < L::kStages; ++s) {
       mbar_init(bar_full(s), 1);
-      mbar_init(bar_empty(s), 1);
+      mbar_init(bar_empty(s), kIssuers);
     }
     for (int t = 0; t < 2; ++t) {
       mbar_init(bar_s_full0 + 8 * t, 1);
-      mbar_init(bar_p_full0 + 16 * t, 4 * 32);
-      mbar_init(bar_p_full0 + 16 * t + 8, 4 * 32);
+      mbar_init(bar_s_free0 + 8 * t, 4 * 32);
+      mbar_init(bar_p_full0 + 8 * t, 4 * 32);
+      mbar_init(bar_p_free0 + 8 * t, 1);
       mbar_init(bar_o_full0 + 8 * t, 1);
+      mbar_init(bar_drain + 8 * t, 1);
+      mbar_init(bar_part0 + 8 * t, 4 * 32);
     }
-    mbar_init(bar_drain, 1);
-    mbar_init(bar_part0, 4 * 32);
-    mbar_init(bar_part0 + 8, 4 * 32);
     *abort_flag = 0;
     mbar_init_fence();
   }
@@ -308,185 +328,193 @@ __global__ void __launch_bounds__(kThreads, 1)
   wd.abort_flag = abort_flag;
   wd.limit_ns = p.watchdog_ns;
 
-  if (warp == kLoadWarp) {
-    // ------------------------------------------------------------ producer
-    if (lane == 0) {
-      tma_prefetch_map(&tmQ);
-      tma_prefetch_map(&tmK);
-      tma_prefetch_map(&tmV);
-      const uint64_t keep = l2_policy_evict_last();    // K/V: re-read by every query tile of the head
-      const uint64_t stream_once = l2_policy_evict_first();  // Q: read once
-      uint32_t it = 0;
-      uint32_t q_round = 0;
-      bool ok = true;
-      SegCursor cur = first_cursor(p);
-      Segment w;
-      while (ok && next_segment<kCausal>(cur, w, p)) {
-        if (q_round > 0 && !wait_bounded(bar_q_empty, (q_round - 1) & 1u, wd, kSiteLoadQEmpty)) {
-          ok = false;
-          break;
-        }
-        mbar_arrive_expect_tx(bar_q_full, L::kQBytes);
-        for (int t = 0; t < kSubTiles; ++t)
-          for (int pn = 0; pn < L::kPanels; ++pn)
-            tma_load_3d_hint(sQ + t * L::kTileBytes + pn * kPanelBytes, &tmQ, bar_q_full, pn * 64,
-                             w.q0 + t * kRows, w.bh, stream_once);
-        ++q_round;
-        for (int j = w.kv_begin; j < w.kv_end && ok; ++j) {
-          for (int kv = 0; kv < 2; ++kv) {
-            const int slot = it % L::kStages;
-            const uint32_t ph = (it / L::kStages) & 1u;
-            if (!wait_bounded(bar_empty(slot), ph ^ 1u, wd, kSiteLoadRingEmpty)) {
-              ok = false;
-              break;
-            }
-            if (p.test_withhold && it == 0) {  // test hook: this tile never arrives
-              ++it;
-              continue;
-            }
+  if (warp >= 8) {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kControlRegs));
+    if (warp == kLoadWarp) {
+      // ---------------------------------------------------------- producer
+      // Ring order per segment [b, e): K_b, then for each j: K_{j+1}, V_j —
+      // the order the MMA issuers consume and release them.
+      if (lane == 0) {
+        tma_prefetch_map(&tmQ);
+        tma_prefetch_map(&tmK);
+        tma_prefetch_map(&tmV);
+        const uint64_t keep = l2_policy_evict_last();          // K/V: re-read by every query tile of the head
+        const uint64_t stream_once = l2_policy_evict_first();  // Q: read once
+        int slot = 0;
+        uint32_t ring_ph = 0, issued = 0, q_round = 0;
+        bool ok = true;
+        SegCursor cur = first_cursor(p);
+        Segment w;
+        auto load_tile = [&](const CUtensorMap* map, int j) -> bool {
+          if (!wait_bounded(bar_empty(slot), ring_ph ^ 1u, wd, kSiteLoadRingEmpty)) return false;
+          if (!(p.test_withhold && issued == 0)) {  // test hook: the first tile never arrives
             mbar_arrive_expect_tx(bar_full(slot), L::kTileBytes);
-            const CUtensorMap* map = kv ? &tmV : &tmK;
             for (int pn = 0; pn < L::kPanels; ++pn)
-              tma_load_3d_hint(sRing + slot * L::kTileBytes + pn * kPanelBytes, map, bar_full(slot),
-                               pn * 64, j * kKeys, w.bh, keep);
-            ++it;
+              tma_load_3d_hint(sRing + slot * L::kTileBytes + pn * kPanelBytes, map, bar_full(slot), pn * 64,
+                               j * kKeys, w.bh, keep);
           }
-        }
-      }
-      // Drain: every copy issued must have landed before the CTA may exit.
-      const uint32_t first = it > (uint32_t)L::kStages ? it - L::kStages : 0u;
-      for (uint32_t i = first; i < it; ++i)
-        wait_bounded(bar_full(i % L::kStages), (i / L::kStages) & 1u, wd, kSiteDrain, false);
-      if (q_round > 0) wait_bounded(bar_q_full, (q_round - 1) & 1u, wd, kSiteDrain, false);
-    }
-    __syncwarp();
-  } else if (warp == kMmaWarp) {
-    // ----------------------------------------------------------- MMA issuer
-    if (lane == 0) {
-      constexpr uint32_t idesc_s = make_idesc_f16(kBf16, kKeys, false);
-      constexpr uint32_t idesc_o = make_idesc_f16(kBf16, D, true);
-      // Descriptor low words advance by compile-time offsets (the start
-      // address field never carries: shared memory stays below 256 KB); the
-      // high words are constants.
-      constexpr uint32_t kHi = desc_hi_sw128(1024);  // 8-row (K-major) / 8-key (MN-major) groups 1 KB apart
-      const uint32_t q_lo = desc_lo_sw128(sQ, 16);
-      const uint32_t ring_lo = desc_lo_sw128(sRing, 16);
-      const uint32_t ring_lo_v = desc_lo_sw128(sRing, kPanelBytes);  // V: 64-column panels 16 KB apart
-
-      // S_t = Q_t K^T : D/16 steps of K=16 along the head dimension.
-      auto issue_s = [&](int t, int slot) {
-        const uint32_t qa = q_lo + static_cast<uint32_t>((t * L::kTileBytes) >> 4);
-        const uint32_t ka = ring_lo + static_cast<uint32_t>(slot * (L::kTileBytes >> 4));
-        const uint32_t dt = tmem + static_cast<uint32_t>(t * kKeys);
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = static_cast<uint32_t>(((kk >> 2) * kPanelBytes + (kk & 3) * 32) >> 4);
-          mma_ss_w(dt, qa + off, kHi, ka + off, kHi, idesc_s, kk > 0 ? 1u : 0u);
-        }
-      };
-      // O_t (+)= P_t V over keys [64h, 64h+64): P from TMEM (16-bit pairs), V from
-      // shared memory (MN-major).
-      auto issue_pv_half = [&](int t, int slot, int h, bool acc) {
-        const uint32_t va = ring_lo_v + static_cast<uint32_t>(slot * (L::kTileBytes >> 4));
-        const uint32_t dt = tmem + L::kColO + static_cast<uint32_t>(t * D);
-        const uint32_t pt = tmem + static_cast<uint32_t>(t * kKeys);
-#pragma unroll
-        for (int k4 = 0; k4 < kKeys / 32; ++k4) {
-          const int kk = h * (kKeys / 32) + k4;
-          mma_ts_w(dt, pt + kk * 8, va + static_cast<uint32_t>((kk * 16 * 128) >> 4), kHi, idesc_o,
-                   (acc || kk > 0) ? 1u : 0u);
-        }
-      };
-
-      // ring position: slot and the parity of its current use
-      int slot = 0;
-      uint32_t ring_ph = 0;
-      auto advance = [&]() {
-        if (++slot == L::kStages) {
-          slot = 0;
-          ring_ph ^= 1u;
-        }
-      };
-      uint32_t q_round = 0;
-      uint32_t p_phase[2] = {0u, 0u};  // both halves of a sub-tile flip together
-      bool ok = true;
-      SegCursor cur = first_cursor(p);
-      Segment w;
-      while (ok && next_segment<kCausal>(cur, w, p)) {
-        if (!wait_bounded(bar_q_full, q_round & 1u, wd, kSiteMmaQFull)) { ok = false; break; }
-        ++q_round;
-        int slot_k = slot;
-        if (!wait_bounded(bar_full(slot_k), ring_ph, wd, kSiteMmaRingFull)) {
-          ok = false;
-          break;
-        }
-        advance();
-        tc_fence_after_sync();
-        issue_s(0, slot_k);
-        mma_commit(bar_s_full0);
-        issue_s(1, slot_k);
-        mma_commit(bar_s_full0 + 8);
-        mma_commit(bar_empty(slot_k));
-        if (w.kv_end - w.kv_begin == 1) mma_commit(bar_q_empty);
-
-        for (int j = w.kv_begin; j < w.kv_end; ++j) {
-          const int slot_v = slot;
-          if (!wait_bounded(bar_full(slot_v), ring_ph, wd, kSiteMmaRingFull)) {
+          ++issued;
+          if (++slot == L::kStages) {
+            slot = 0;
+            ring_ph ^= 1u;
+          }
+          return true;
+        };
+        while (ok && next_segment<kCausal>(cur, w, p)) {
+          if (q_round > 0 && !wait_bounded(bar_q_empty, (q_round - 1) & 1u, wd, kSiteLoadQEmpty)) {
             ok = false;
             break;
           }
-          advance();
-          const bool next = j + 1 < w.kv_end;
-          if (next) {
-            slot_k = slot;
-            if (!wait_bounded(bar_full(slot_k), ring_ph, wd, kSiteMmaRingFull)) {
-              ok = false;
-              break;
-            }
-            advance();
-          }
-#pragma unroll
-          for (int t = 0; t < 2; ++t) {
-            if (!wait_bounded(bar_p_full0 + 16 * t, p_phase[t], wd, kSiteMmaPFull)) {
-              ok = false;
-              break;
-            }
-            p_phase[t] ^= 1u;
-            tc_fence_after_sync();
-            issue_pv_half(t, slot_v, 0, j > w.kv_begin);
-            issue_pv_half(t, slot_v, 1, true);
-            if (!next) mma_commit(bar_o_full0 + 8 * t);
-            if (t == 1) mma_commit(bar_empty(slot_v));
-            if (next) {
-              issue_s(t, slot_k);
-              mma_commit(bar_s_full0 + 8 * t);
-            }
-          }
-          if (!ok) break;
-          if (next) {
-            mma_commit(bar_empty(slot_k));
-            if (j + 2 == w.kv_end) mma_commit(bar_q_empty);
+          mbar_arrive_expect_tx(bar_q_full, L::kQBytes);
+          for (int t = 0; t < kSubTiles; ++t)
+            for (int pn = 0; pn < L::kPanels; ++pn)
+              tma_load_3d_hint(sQ + t * L::kTileBytes + pn * kPanelBytes, &tmQ, bar_q_full, pn * 64,
+                               w.q0 + t * kRows, w.bh, stream_once);
+          ++q_round;
+          ok = load_tile(&tmK, w.kv_begin);
+          for (int j = w.kv_begin; j < w.kv_end && ok; ++j) {
+            if (j + 1 < w.kv_end) ok = load_tile(&tmK, j + 1);
+            if (ok) ok = load_tile(&tmV, j);
           }
         }
+        // Drain: every copy issued must have landed before the CTA may exit.
+        const uint32_t first = issued > (uint32_t)L::kStages ? issued - L::kStages : 0u;
+        for (uint32_t i = first; i < issued; ++i)
+          wait_bounded(bar_full(i % L::kStages), (i / L::kStages) & 1u, wd, kSiteDrain, false);
+        if (q_round > 0) wait_bounded(bar_q_full, (q_round - 1) & 1u, wd, kSiteDrain, false);
       }
-      // Drain: all issued tensor-core work completes before TMEM is released.
-      mma_commit(bar_drain);
-      wait_bounded(bar_drain, 0u, wd, kSiteDrain, false);
+      __syncwarp();
+    } else if (warp < kMmaWarp + kIssuers) {
+      // ------------------------------------------------------ MMA issuers
+      if (lane == 0) {
+        const int me = warp - kMmaWarp;  // with two issuers: the sub-tile it drives
+        constexpr uint32_t idesc_s = make_idesc_f16(kBf16, kKeys, false);
+        constexpr uint32_t idesc_o = make_idesc_f16(kBf16, D, true);
+        // Descriptor low words advance by compile-time offsets (the start
+        // address field never carries: shared memory stays below 256 KB);
+        // the high words are constants.
+        constexpr uint32_t kHi = desc_hi_sw128(1024);  // 8-row (K-major) / 8-key (MN-major) groups 1 KB apart
+        const uint32_t q_lo = desc_lo_sw128(sQ, 16);
+        const uint32_t p_lo = desc_lo_sw128(sP, 16);
+        const uint32_t ring_lo = desc_lo_sw128(sRing, 16);
+        const uint32_t ring_lo_v = desc_lo_sw128(sRing, kPanelBytes);  // V: 64-column panels 16 KB apart
+
+        // S_t = Q_t K^T : D/16 steps of K=16 along the head dimension.
+        auto issue_s = [&](int t, int slot) {
+          const uint32_t qa = q_lo + static_cast<uint32_t>((t * L::kTileBytes) >> 4);
+          const uint32_t ka = ring_lo + static_cast<uint32_t>(slot * (L::kTileBytes >> 4));
+          const uint32_t dt = tmem + static_cast<uint32_t>(t * kKeys);
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t off = static_cast<uint32_t>(((kk >> 2) * kPanelBytes + (kk & 3) * 32) >> 4);
+            mma_ss_w(dt, qa + off, kHi, ka + off, kHi, idesc_s, kk > 0 ? 1u : 0u);
+          }
+        };
+        // O_t (+)= P_t V : P (K-major) and V (MN-major) from shared memory,
+        // 8 steps of 16 keys.
+        auto issue_pv = [&](int t, int slot, bool acc) {
+          const uint32_t pa = p_lo + static_cast<uint32_t>((t * kPTileBytes) >> 4);
+          const uint32_t va = ring_lo_v + static_cast<uint32_t>(slot * (L::kTileBytes >> 4));
+          const uint32_t dt = tmem + L::kColO + static_cast<uint32_t>(t * D);
+#pragma unroll
+          for (int kk = 0; kk < kKeys / 16; ++kk) {
+            const uint32_t po = static_cast<uint32_t>(((kk >> 2) * kPanelBytes + (kk & 3) * 32) >> 4);
+            mma_ss_w(dt, pa + po, kHi, va + static_cast<uint32_t>((kk * 16 * 128) >> 4), kHi, idesc_o,
+                     (acc || kk > 0) ? 1u : 0u);
+          }
+        };
+
+        const int t_lo = kIssuers == 2 ? me : 0;
+        const int t_hi = kIssuers == 2 ? me : 1;
+        int slot = 0;
+        uint32_t ring_ph = 0;
+        auto take = [&](int& s) -> bool {
+          s = slot;
+          const bool got = wait_bounded(bar_full(s), ring_ph, wd, kSiteMmaRingFull);
+          if (++slot == L::kStages) {
+            slot = 0;
+            ring_ph ^= 1u;
+          }
+          return got;
+        };
+        uint32_t q_round = 0;
+        uint32_t s_free_ph[2] = {0u, 0u}, p_full_ph[2] = {0u, 0u};
+        bool s_out[2] = {false, false};  // an S issued whose TMEM the softmax has not released yet
+        // Every S after the first waits until the softmax has loaded the
+        // previous S of its sub-tile into registers (also across segments).
+        auto issue_next_s = [&](int t, int slot) -> bool {
+          if (s_out[t]) {
+            if (!wait_bounded(bar_s_free0 + 8 * t, s_free_ph[t], wd, kSiteMmaSFree)) return false;
+            s_free_ph[t] ^= 1u;
+          }
+          tc_fence_after_sync();
+          issue_s(t, slot);
+          mma_commit(bar_s_full0 + 8 * t);
+          s_out[t] = true;
+          return true;
+        };
+        bool ok = true;
+        SegCursor cur = first_cursor(p);
+        Segment w;
+        while (ok && next_segment<kCausal>(cur, w, p)) {
+          const int b = w.kv_begin, e = w.kv_end;
+          if (!wait_bounded(bar_q_full, q_round & 1u, wd, kSiteMmaQFull)) { ok = false; break; }
+          ++q_round;
+          int slot_k;
+          if (!take(slot_k)) { ok = false; break; }
+          for (int t = t_lo; t <= t_hi && ok; ++t) ok = issue_next_s(t, slot_k);
+          if (!ok) break;
+          mma_commit(bar_empty(slot_k));
+          if (e - b == 1) mma_commit(bar_q_empty);
+          for (int j = b; j < e && ok; ++j) {
+            if (j + 1 < e) {
+              if (!take(slot_k)) { ok = false; break; }
+              for (int t = t_lo; t <= t_hi && ok; ++t) ok = issue_next_s(t, slot_k);
+              if (!ok) break;
+              mma_commit(bar_empty(slot_k));
+              if (j + 2 == e) mma_commit(bar_q_empty);
+            }
+            int slot_v;
+            if (!take(slot_v)) { ok = false; break; }
+            for (int t = t_lo; t <= t_hi; ++t) {
+              if (!wait_bounded(bar_p_full0 + 8 * t, p_full_ph[t], wd, kSiteMmaPFull)) { ok = false; break; }
+              p_full_ph[t] ^= 1u;
+              tc_fence_after_sync();
+              issue_pv(t, slot_v, j > b);
+              mma_commit(bar_p_free0 + 8 * t);
+              if (j == e - 1) mma_commit(bar_o_full0 + 8 * t);
+            }
+            if (!ok) break;
+            mma_commit(bar_empty(slot_v));
+          }
+        }
+        // Drain: all issued tensor-core work completes before TMEM is released.
+        mma_commit(bar_drain + 8 * me);
+        wait_bounded(bar_drain + 8 * me, 0u, wd, kSiteDrain, false);
+      }
+      __syncwarp();
     }
-    __syncwarp();
   } else {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kSoftmaxRegs));
     // ------------------------------------------------- softmax warpgroups
     const int t = warp >> 2;                 // sub-tile
     const int wr = warp & 3;                 // warp within the warpgroup: TMEM lanes 32*wr..
-    const uint32_t lane_off = static_cast<uint32_t>(wr * 32) << 16;
-    const uint32_t tS = tmem + lane_off + (uint32_t)(t * kKeys);
-    const uint32_t tO = tmem + lane_off + L::kColO + (uint32_t)(t * D);
-    const uint32_t bar_s = bar_s_full0 + 8 * t;
-    const uint32_t bar_p = bar_p_full0 + 16 * t;  // + 8 for the second half
-    const uint32_t bar_o = bar_o_full0 + 8 * t;
-    const float c = p.scale_log2;
     const int rr = wr * 32 + lane;           // row within the sub-tile
+    const uint32_t lane_off = static_cast<uint32_t>(wr * 32) << 16;
+    const uint32_t tS = tmem + lane_off + static_cast<uint32_t>(t * kKeys);
+    const uint32_t tO = tmem + lane_off + L::kColO + static_cast<uint32_t>(t * D);
+    const uint32_t bar_s = bar_s_full0 + 8 * t;
+    const uint32_t bar_sf = bar_s_free0 + 8 * t;
+    const uint32_t bar_p = bar_p_full0 + 8 * t;
+    const uint32_t bar_pf = bar_p_free0 + 8 * t;
+    const uint32_t bar_o = bar_o_full0 + 8 * t;
+    // this thread's P row in shared memory: 128 bytes per 64 keys, 16-byte
+    // chunks placed by the 128-byte swizzle (chunk c of row r at c ^ (r % 8))
+    const uint32_t p_row = sP + static_cast<uint32_t>(t * kPTileBytes + rr * 128);
+    const uint32_t p_xor = static_cast<uint32_t>(rr & 7);
+    const float c = p.scale_log2;
     uint32_t s_phase = 0, o_phase = 0, part_phase = 0;
+    uint32_t p_count = 0;  // P tiles published so far (= P.V products issued or pending)
     bool ok = true;
     SegCursor cur = first_cursor(p);
     Segment w;
@@ -503,38 +531,30 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!got) { ok = false; break; }
         s_phase ^= 1u;
         tc_fence_after_sync();
-        // Two passes over the S row in TMEM keep only two 32-column chunks in
-        // registers: pass 1 takes the row max, pass 2 re-reads each chunk,
-        // exponentiates it and writes P behind itself (P chunk c lands on
-        // columns [16c, 16c+16), which pass 2 has already read).
+        uint32_t sr[128];
+        tmem_ld32x128_wait(tS, sr);
+        // S is in registers: the issuer may compute the next scores into TMEM.
+        tc_fence_before_sync();
+        mbar_arrive(bar_sf);
+        float s[128];
+#pragma unroll
+        for (int i = 0; i < 128; ++i) s[i] = __uint_as_float(sr[i]);
         const int kv0 = j * kKeys;
-        const bool masked = kv0 + kKeys > limit;  // ragged tail and/or causal diagonal
-        auto mask_chunk = [&](uint32_t (&v)[32], int c0) {
+        if (kv0 + kKeys > limit) {  // ragged tail and/or causal diagonal: mask disallowed keys
 #pragma unroll
-          for (int i = 0; i < 32; ++i)
-            if (kv0 + c0 + i >= limit) v[i] = __float_as_uint(-CUDART_INF_F);
-        };
-        float m_tile = -CUDART_INF_F;
-#pragma unroll
-        for (int c2 = 0; c2 < 4; c2 += 2) {
-          uint32_t va[32], vb[32];
-          tmem_ld32x32(tS + 32 * c2, va);
-          tmem_ld32x32(tS + 32 * (c2 + 1), vb);
-          tmem_wait_ld32(va);
-          tmem_wait_ld32(vb);
-          if (masked) {
-            mask_chunk(va, 32 * c2);
-            mask_chunk(vb, 32 * (c2 + 1));
-          }
-          float m0 = fmax3(__uint_as_float(va[0]), __uint_as_float(va[1]), __uint_as_float(va[2]));
-          float m1 = fmax3(__uint_as_float(vb[0]), __uint_as_float(vb[1]), __uint_as_float(vb[2]));
-#pragma unroll
-          for (int i = 3; i < 31; i += 2) {
-            m0 = fmax3(m0, __uint_as_float(va[i]), __uint_as_float(va[i + 1]));
-            m1 = fmax3(m1, __uint_as_float(vb[i]), __uint_as_float(vb[i + 1]));
-          }
-          m_tile = fmax3(m_tile, fmaxf(m0, __uint_as_float(va[31])), fmaxf(m1, __uint_as_float(vb[31])));
+          for (int i = 0; i < 128; ++i)
+            if (kv0 + i >= limit) s[i] = -CUDART_INF_F;
         }
+        // row max: four independent chains of 3-input maxima
+        float mx[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          mx[q] = fmax3(s[32 * q], s[32 * q + 1], s[32 * q + 2]);
+#pragma unroll
+          for (int i = 3; i < 31; i += 2) mx[q] = fmax3(mx[q], s[32 * q + i], s[32 * q + i + 1]);
+          mx[q] = fmaxf(mx[q], s[32 * q + 31]);
+        }
+        const float m_tile = fmaxf(fmax3(mx[0], mx[1], mx[2]), mx[3]);
         m_raw = fmaxf(m_raw, m_tile);
         // Move the exponent base only when the max has grown by more than
         // kRescaleLog2 (or on the first tile); otherwise keep the old base, so
@@ -547,6 +567,34 @@ __global__ void __launch_bounds__(kThreads, 1)
           alpha = ex2_approx(base - cand);  // 0 on the first tile with an allowed key
           base = cand;
         }
+        // The previous P.V must be complete before O is rescaled and before
+        // its P buffer is overwritten.
+        if (p_count > 0) {
+          bool fr = wait_bounded(bar_pf, (p_count - 1) & 1u, wd, kSiteSoftmaxPFree);
+          fr = __all_sync(0xffffffffu, fr);
+          if (!fr) { ok = false; break; }
+          tc_fence_after_sync();
+        }
+        const float nb = (base == -CUDART_INF_F) ? 0.f : -base;
+        float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+        // P: 16 chunks of 8 keys (4 packed pairs) into the swizzled row
+#pragma unroll
+        for (int ch = 0; ch < 16; ++ch) {
+          uint32_t pk[4];
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            float x0, x1;
+            ffma2_bcast(x0, x1, s[8 * ch + 2 * i], s[8 * ch + 2 * i + 1], c, nb);
+            const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
+            fadd2_acc(acc[2 * i], acc[2 * i + 1], p0, p1);
+            pk[i] = pack2(p0, p1, kBf16);
+          }
+          const uint32_t addr = p_row + static_cast<uint32_t>((ch >> 3) * kPanelBytes) +
+                                ((static_cast<uint32_t>(ch & 7) ^ p_xor) << 4);
+          st_shared_v4(addr, pk[0], pk[1], pk[2], pk[3]);
+        }
+        // O holds P.V up to tile j-1 (complete, see above): rescale it now
+        // that the scores are no longer held in registers.
         if (j > w.kv_begin && __any_sync(0xffffffffu, alpha != 1.f)) {
 #pragma unroll
           for (int cc = 0; cc < D; cc += 32) {
@@ -556,46 +604,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
             tmem_st32x32(tO + cc, o);
           }
+          tmem_wait_st();
         }
-        const float nb = (base == -CUDART_INF_F) ? 0.f : -base;
-        float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-        // P (16-bit pairs) over the first 64 columns of this sub-tile's S
-        // region, published in two halves so that P.V can start on the
-        // first 64 keys while the second half is exponentiated.
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          uint32_t va[32], vb[32];
-          tmem_ld32x32(tS + 64 * h, va);
-          tmem_ld32x32(tS + 64 * h + 32, vb);
-          tmem_wait_ld32(va);
-          tmem_wait_ld32(vb);
-          if (masked) {
-            mask_chunk(va, 64 * h);
-            mask_chunk(vb, 64 * h + 32);
-          }
-          uint32_t pk[16];
-#pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            float x0, x1;
-            ffma2_bcast(x0, x1, __uint_as_float(va[2 * i]), __uint_as_float(va[2 * i + 1]), c, nb);
-            const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
-            fadd2_acc(acc[2 * (i & 3)], acc[2 * (i & 3) + 1], p0, p1);
-            pk[i] = pack2(p0, p1, kBf16);
-          }
-          tmem_st32x16(tS + 32 * h, pk);
-#pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            float x0, x1;
-            ffma2_bcast(x0, x1, __uint_as_float(vb[2 * i]), __uint_as_float(vb[2 * i + 1]), c, nb);
-            const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
-            fadd2_acc(acc[2 * (i & 3)], acc[2 * (i & 3) + 1], p0, p1);
-            pk[i] = pack2(p0, p1, kBf16);
-          }
-          tmem_st32x16(tS + 32 * h + 16, pk);
-        }
-        tmem_wait_st();
+        // the tensor core reads P through the async proxy
+        fence_proxy_async_shared();
         tc_fence_before_sync();
         mbar_arrive(bar_p);
+        ++p_count;
         const float lt = ((acc[0] + acc[1]) + (acc[2] + acc[3])) + ((acc[4] + acc[5]) + (acc[6] + acc[7]));
         // P.V uses p rounded to 16 bits. With the base lagging the max, the
         // tile's largest p is not a power of two, so its rounding would leave
@@ -721,7 +736,13 @@ cudaError_t launch_fwd(const CUtensorMap& q, const CUtensorMap& k, const CUtenso
                        int grid, cudaStream_t stream) {
   auto kern = fa2_fwd_kernel<D, kBf16, kCausal>;
   const int smem = Layout<D>::kSmemBytes;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  cudaFuncAttributes fa;
+  cudaError_t e = cudaFuncGetAttributes(&fa, kern);
+  if (e != cudaSuccess) return e;
+  // The in-kernel register split assumes exactly kLaunchRegs per thread at
+  // launch; any other count could leave a warpgroup waiting for registers.
+  if (fa.numRegs != kLaunchRegs) return cudaErrorInvalidConfiguration;
+  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);

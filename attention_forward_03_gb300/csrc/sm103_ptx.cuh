@@ -212,6 +212,17 @@ __host__ __device__ constexpr uint32_t make_idesc_f16(bool bf16, int n, bool b_m
          (static_cast<uint32_t>(128 >> 4) << 24);
 }
 
+// ---------------------------------------------------------- shared memory
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+  asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
+}
+
+// Make this thread's generic-proxy shared-memory writes visible to the async
+// proxy (tensor-core and TMA reads) before signalling the consumer.
+__device__ __forceinline__ void fence_proxy_async_shared() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
 // ------------------------------------------------------------------- math
 __device__ __forceinline__ float ex2_approx(float x) {
   float y;
