@@ -567,31 +567,33 @@ __global__ void __launch_bounds__(kThreads, 1)
           alpha = ex2_approx(base - cand);  // 0 on the first tile with an allowed key
           base = cand;
         }
-        // The previous P.V must be complete before O is rescaled and before
-        // its P buffer is overwritten.
+        const float nb = (base == -CUDART_INF_F) ? 0.f : -base;
+        float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+        // p = 2^(s*c - base), packed to 16-bit pairs in registers while the
+        // previous P.V may still be reading the P buffer.
+        uint32_t pk[64];
+#pragma unroll
+        for (int i = 0; i < 64; ++i) {
+          float x0, x1;
+          ffma2_bcast(x0, x1, s[2 * i], s[2 * i + 1], c, nb);
+          const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
+          fadd2_acc(acc[2 * (i & 3)], acc[2 * (i & 3) + 1], p0, p1);
+          pk[i] = pack2(p0, p1, kBf16);
+        }
+        // The previous P.V must be complete before its P buffer is
+        // overwritten and before O is rescaled.
         if (p_count > 0) {
           bool fr = wait_bounded(bar_pf, (p_count - 1) & 1u, wd, kSiteSoftmaxPFree);
           fr = __all_sync(0xffffffffu, fr);
           if (!fr) { ok = false; break; }
           tc_fence_after_sync();
         }
-        const float nb = (base == -CUDART_INF_F) ? 0.f : -base;
-        float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
         // P: 16 chunks of 8 keys (4 packed pairs) into the swizzled row
 #pragma unroll
         for (int ch = 0; ch < 16; ++ch) {
-          uint32_t pk[4];
-#pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            float x0, x1;
-            ffma2_bcast(x0, x1, s[8 * ch + 2 * i], s[8 * ch + 2 * i + 1], c, nb);
-            const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
-            fadd2_acc(acc[2 * i], acc[2 * i + 1], p0, p1);
-            pk[i] = pack2(p0, p1, kBf16);
-          }
           const uint32_t addr = p_row + static_cast<uint32_t>((ch >> 3) * kPanelBytes) +
                                 ((static_cast<uint32_t>(ch & 7) ^ p_xor) << 4);
-          st_shared_v4(addr, pk[0], pk[1], pk[2], pk[3]);
+          st_shared_v4(addr, pk[4 * ch], pk[4 * ch + 1], pk[4 * ch + 2], pk[4 * ch + 3]);
         }
         // O holds P.V up to tile j-1 (complete, see above): rescale it now
         // that the scores are no longer held in registers.
