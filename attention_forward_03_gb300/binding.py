@@ -34,6 +34,11 @@ SIGNATURES = {
                                   _VP]),
     "fa2_fwd_noalloc": (ctypes.c_int, [_VP, _VP, _VP, _VP, _VP, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                        ctypes.c_int, ctypes.c_float, ctypes.c_int, ctypes.c_int, _VP]),
+    "fa2_fwd_host_buffer_bytes": (ctypes.c_int, [ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                                 ctypes.POINTER(ctypes.c_size_t)]),
+    "fa2_fwd_host": (ctypes.c_int, [_VP, _VP, _VP, _VP, _VP, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                    ctypes.c_int, ctypes.c_float, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                    ctypes.c_int, _VP, ctypes.c_size_t, _VP]),
     "fa2_device_status": (ctypes.c_int, [_VP, ctypes.POINTER(ctypes.c_int), ctypes.c_int]),
     "fa2_set_watchdog_ns": (ctypes.c_int, [ctypes.c_ulonglong]),
     "fa2_test_withhold_next_load": (ctypes.c_int, [ctypes.c_int]),
@@ -99,6 +104,13 @@ def fa2_fwd_workspace_bytes(D: int) -> int:
     return n.value
 
 
+def fa2_fwd_host_buffer_bytes(B: int, H: int, N: int, D: int) -> int:
+    n = ctypes.c_size_t(0)
+    _check(library().fa2_fwd_host_buffer_bytes(int(B), int(H), int(N), int(D), ctypes.byref(n)),
+           "fa2_fwd_host_buffer_bytes")
+    return n.value
+
+
 def fa2_device_status(stream: int | None = None, clear: bool = False) -> int:
     v = ctypes.c_int(0)
     _check(library().fa2_device_status(stream, ctypes.byref(v), int(bool(clear))), "fa2_device_status")
@@ -141,23 +153,35 @@ def workspace_for(device, D: int):
 
 
 UNIT_ROWS = 256  # query rows per work unit of the kernel
+KV_TILE = 128    # keys per K/V tile
+SPLIT_COST_STEPS = 4  # measured cost of a split unit (partial write, merge), in K/V-tile steps
+
+
+def steps_per_head(N: int, is_causal: bool) -> int:
+    """K/V-tile steps (one 256-row unit against one 128-key tile) of one head."""
+    n_qt, nkv = -(-N // UNIT_ROWS), -(-N // KV_TILE)
+    if not is_causal:
+        return n_qt * nkv
+    return sum(min(2 * qt + 2, nkv) for qt in range(n_qt))
 
 
 def choose_schedule(B: int, H: int, N: int, is_causal: bool, sms: int) -> str:
     """Pick the kernel schedule for a problem (a choice between two C entry points).
 
-    The balanced schedule (fa2_fwd_ws) splits work exactly across the SMs at the
-    cost of a partial-result merge per CTA; it pays off only for non-causal work
-    of at least one unit per SM whose last round of whole units would leave more
-    than 8% of the SMs idle. Causal work is already balanced by the round
-    schedule's heaviest-first zig-zag, and small problems are dominated by the
-    fixed per-segment cost, so both use the round schedule (fa2_fwd).
+    Cost in K/V-tile steps of the busiest SM: the round schedule (fa2_fwd)
+    takes ceil(units / SMs) rounds of whole units; the balanced schedule
+    (fa2_fwd_ws) takes total steps / SMs plus the cost of the partial-result
+    merge of the units it splits. Balanced is chosen when it is at least 5%
+    cheaper. Causal work stays on the round schedule, whose heaviest-first
+    zig-zag measured faster than the split on every causal workload.
     """
     units = B * H * -(-N // UNIT_ROWS)
-    if is_causal or units < sms:
+    if is_causal or units == 0:
         return "units"
-    rounds = -(-units // sms)
-    return "balanced" if units / (rounds * sms) < 0.92 else "units"
+    nkv = -(-N // KV_TILE)
+    rounds_cost = -(-units // sms) * nkv
+    balanced_cost = units * nkv / sms + SPLIT_COST_STEPS
+    return "balanced" if balanced_cost < 0.95 * rounds_cost else "units"
 
 
 def attention_forward(q, k, v, scale: float | None = None, is_causal: bool = False, out=None, lse=None,
@@ -210,4 +234,90 @@ def attention_forward(q, k, v, scale: float | None = None, is_causal: bool = Fal
                               B, H, N, D, scale, int(bool(is_causal)), _dtype_code(q), ws.data_ptr(),
                               ws.numel() * ws.element_size(), s.cuda_stream)
             _check(code, "fa2_fwd_ws")
+    return out, lse
+
+
+HOST_CHUNKS = 16           # target number of head chunks of attention_forward_host
+HOST_CHUNK_MIN_STEPS = 4096  # K/V-tile steps a chunk needs to keep the GPU busy (~27 per SM)
+
+
+def host_chunk_heads(B: int, H: int, N: int, is_causal: bool, sms: int) -> int:
+    """Heads per chunk of the host-memory pipeline.
+
+    The copies are the bottleneck end to end, so the pipeline wants many
+    chunks (its fill and drain are one chunk's copy-in and one chunk's kernel
+    and copy-out), but each chunk's kernel must still fill the GPU: at least
+    HOST_CHUNK_MIN_STEPS steps, and for causal work (round schedule) at least
+    one unit per SM. Measured on target-like shapes this picks the fastest of
+    1-64 heads per chunk.
+    """
+    bh = B * H
+    if bh <= 0:
+        return 1
+    hpc = max(-(-bh // HOST_CHUNKS), -(-HOST_CHUNK_MIN_STEPS // max(1, steps_per_head(N, is_causal))))
+    if is_causal:
+        hpc = max(hpc, -(-sms // -(-N // UNIT_ROWS)))
+    return max(1, min(hpc, bh))
+
+
+def attention_forward_host(q, k, v, scale: float | None = None, is_causal: bool = False, out=None, lse=None,
+                           stream=None, device=None, heads_per_chunk: int | None = None, schedule: str = "auto",
+                           device_buffer=None, synchronize: bool = True):
+    """FlashAttention-2 forward over host (CPU) tensors [B, H, N, D] through fa2_fwd_host.
+
+    The inputs are copied to `device` (default: the current CUDA device), the
+    forward pass runs there and O, LSE are copied back into `out` / `lse`
+    (allocated in page-locked memory when not given), chunk by chunk so that
+    the copies overlap the kernels. Page-locked inputs are needed for the
+    copies to overlap. With synchronize=False the call returns once the work
+    is enqueued on `stream`; the results are valid after that stream is
+    synchronised.
+    schedule: "auto" (choose_schedule applied to one chunk), "balanced" or "units".
+    device_buffer: optional uint8 CUDA tensor of at least
+    fa2_fwd_host_buffer_bytes(B, H, N, D) bytes; by default one is allocated.
+    """
+    import torch
+    if q.is_cuda or k.is_cuda or v.is_cuda:
+        raise ValueError("q, k, v must be host (CPU) tensors; use attention_forward for CUDA tensors")
+    if q.shape != k.shape or q.shape != v.shape or q.dim() != 4:
+        raise ValueError("q, k, v must share one [B, H, N, D] shape")
+    if q.dtype != k.dtype or q.dtype != v.dtype:
+        raise ValueError("q, k, v must share one dtype")
+    if not (q.is_contiguous() and k.is_contiguous() and v.is_contiguous()):
+        raise ValueError("q, k, v must be contiguous")
+    if schedule not in ("auto", "balanced", "units"):
+        raise ValueError("schedule must be 'auto', 'balanced' or 'units'")
+    B, H, N, D = q.shape
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    hpc = host_chunk_heads(B, H, N, is_causal, sms) if heads_per_chunk is None else int(heads_per_chunk)
+    if hpc < 1:
+        raise ValueError("heads_per_chunk must be >= 1")
+    if schedule == "auto":
+        schedule = choose_schedule(1, min(hpc, B * H), N, is_causal, sms)
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    if out is None:
+        out = torch.empty(q.shape, dtype=q.dtype).pin_memory()
+    if lse is None:
+        lse = torch.empty((B, H, N), dtype=torch.float32).pin_memory()
+    if out.is_cuda or out.shape != q.shape or out.dtype != q.dtype or not out.is_contiguous():
+        raise ValueError("out must be a contiguous host tensor like q")
+    if lse.is_cuda or lse.shape != (B, H, N) or lse.dtype != torch.float32 or not lse.is_contiguous():
+        raise ValueError("lse must be a contiguous float32 [B, H, N] host tensor")
+    with torch.cuda.device(dev):
+        need = fa2_fwd_host_buffer_bytes(B, H, N, D)
+        buf = device_buffer if device_buffer is not None else torch.empty(need, dtype=torch.uint8, device=dev)
+        if not buf.is_cuda or buf.device != dev or buf.numel() * buf.element_size() < need:
+            raise ValueError(f"device_buffer must be a CUDA tensor on {dev} of at least {need} bytes")
+        s = stream if stream is not None else torch.cuda.current_stream(dev)
+        code = library().fa2_fwd_host(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(),
+                                      B, H, N, D, float(scale), int(bool(is_causal)), _dtype_code(q), hpc,
+                                      int(schedule == "balanced"), buf.data_ptr(),
+                                      buf.numel() * buf.element_size(), s.cuda_stream)
+        _check(code, "fa2_fwd_host")
+        if device_buffer is None:
+            buf.record_stream(s)
+        if synchronize:
+            s.synchronize()
     return out, lse

@@ -221,6 +221,8 @@ int launch(const void* Q, const void* K, const void* V, void* O, float* LSE, int
 }  // namespace
 
 namespace fa2 {
+int record_cuda_error(cudaError_t e) { return record_cuda(e); }
+
 int launch_forward(const void* Q, const void* K, const void* V, void* O, float* LSE, int B, int H, int N, int D,
                    float scale, int is_causal, int dtype, void* workspace, size_t workspace_bytes,
                    cudaStream_t stream) {

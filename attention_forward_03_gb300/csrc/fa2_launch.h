@@ -50,6 +50,10 @@ int launch_forward(const void* Q, const void* K, const void* V, void* O, float* 
                    float scale, int is_causal, int dtype, void* workspace, size_t workspace_bytes,
                    cudaStream_t stream);
 
+// Records `e` as the calling thread's last CUDA error (fa2_last_cuda_error)
+// and returns FA2_ERR_CUDA.
+int record_cuda_error(cudaError_t e);
+
 template <int D, bool kBf16, bool kCausal>
 cudaError_t launch_fwd(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v, const Params& p,
                        int grid, cudaStream_t stream);

@@ -319,20 +319,25 @@ def run_gb300(args, w, rank, world, local):
     value = whole_job_tflops(flops, args.steps, world, t_max)
     per_launch = elapsed / args.steps
 
-    # end to end through the public API, host buffers in pinned memory
+    # End to end through the C ABI's host-memory entry point (fa2_fwd_host):
+    # page-locked host buffers in, host buffers out, every copy inside the
+    # timed region, chunks of heads pipelined over the copy engines.
     qh, kh, vh = (t.pin_memory() for t in (q, k, v))
     oh = torch.empty_like(q).pin_memory()
     lh = torch.empty((w.B, w.H, w.N), dtype=torch.float32).pin_memory()
-    qd, kd, vd, od, ld = sets[0]
+    del sets
+    torch.cuda.empty_cache()
+    host_buf = torch.empty(fa2.fa2_fwd_host_buffer_bytes(w.B, w.H, w.N, w.D), dtype=torch.uint8, device=dev)
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    hpc = args.e2e_heads_per_chunk or fa2.binding.host_chunk_heads(w.B, w.H, w.N, w.causal, sms)
+    chunk_schedule = args.schedule
+    if chunk_schedule == "auto":
+        chunk_schedule = fa2.binding.choose_schedule(1, min(hpc, w.B * w.H), w.N, w.causal, sms)
 
     def e2e_step():
-        qd.copy_(qh, non_blocking=True)
-        kd.copy_(kh, non_blocking=True)
-        vd.copy_(vh, non_blocking=True)
-        fa2.attention_forward(qd, kd, vd, scale=w.scale, is_causal=w.causal, out=od, lse=ld, stream=stream,
-                              schedule=args.schedule)
-        oh.copy_(od, non_blocking=True)
-        lh.copy_(ld, non_blocking=True)
+        fa2.attention_forward_host(qh, kh, vh, scale=w.scale, is_causal=w.causal, out=oh, lse=lh, stream=stream,
+                                   device=dev, heads_per_chunk=hpc, schedule=chunk_schedule,
+                                   device_buffer=host_buf, synchronize=False)
 
     for _ in range(2):
         e2e_step()
@@ -369,7 +374,9 @@ def run_gb300(args, w, rank, world, local):
                      "traffic": traffic_per_launch(w.name),
                      "algorithmic_bytes": workloads.algorithmic_bytes(w),
                      "achieved_hbm_gbs": workloads.algorithmic_bytes(w) / per_launch / 1e9},
-        "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "path": "fa2_fwd_host (C ABI, page-locked host buffers)", "heads_per_chunk": hpc,
+                "chunk_schedule": chunk_schedule, "steps": e2e_steps},
         "gpu_launches": args.steps,
         "clocks": clock_info,
     }
@@ -391,6 +398,8 @@ def main(argv=None):
                     help="auto: the binding's choice; balanced: fa2_fwd_ws (equal K/V-tile steps per SM); "
                          "units: fa2_fwd")
     ap.add_argument("--settle-seconds", type=float, default=1.0)
+    ap.add_argument("--e2e-heads-per-chunk", type=int, default=0,
+                    help="heads per chunk of the end-to-end host-memory pipeline (0 = the binding's default)")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--reference-seconds", type=float, default=120.0,
                     help="total CPU time budget of the reference arm")

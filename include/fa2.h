@@ -134,6 +134,59 @@ int fa2_fwd_noalloc(const void* Q, const void* K, const void* V, void* O, float*
                     struct CUstream_st* stream);
 
 /*
+ * fa2_fwd_host_buffer_bytes — bytes of device staging memory fa2_fwd_host
+ * needs for a [B, H, N, D] problem on the current device: room for Q, K, V,
+ * O (B*H*N*D 16-bit values each), LSE (B*H*N floats plus 12 bytes of
+ * alignment padding per head) and the balanced schedule's workspace, each
+ * rounded up to 256 bytes. Returns FA2_OK,
+ * FA2_ERR_INVALID_ARG (bytes NULL, negative size, B*H above INT32_MAX),
+ * FA2_ERR_UNSUPPORTED (D) or FA2_ERR_CUDA (no usable device).
+ */
+int fa2_fwd_host_buffer_bytes(int B, int H, int N, int D, size_t* bytes);
+
+/*
+ * fa2_fwd_host — the same operation and results as fa2_fwd, from and to HOST
+ * memory: Q, K, V are copied to the device, the forward pass runs there and
+ * O, LSE are copied back, in chunks of whole heads so that copies in both
+ * directions overlap the computation of other chunks. The pages have no
+ * counterpart to this entry point (their kernels take device tensors).
+ *
+ * Q, K, V : host pointers, contiguous [B, H, N, D] of `dtype`. Read only.
+ * O, LSE  : host pointers, contiguous [B, H, N, D] of `dtype` and [B, H, N]
+ *           fp32; fully overwritten. Must not overlap the inputs or each
+ *           other. Page-locked memory (cudaHostAlloc / cudaHostRegister) is
+ *           needed for the copies to overlap anything; pageable memory works
+ *           but the copies then run one after another.
+ * B, H, N, D, scale, is_causal, dtype: as fa2_fwd.
+ * heads_per_chunk: heads (of the flattened B*H) per chunk; 0 = ceil(B*H / 4).
+ * balanced: nonzero runs each chunk on the balanced schedule of fa2_fwd_ws
+ *           (workspace inside dev_buffer), zero on the schedule of fa2_fwd.
+ * dev_buffer, dev_bytes: caller-owned device staging memory of the current
+ *           device, 256-byte aligned, at least fa2_fwd_host_buffer_bytes
+ *           bytes. Its contents are scratch: they need no initialisation
+ *           and are not part of the result.
+ * stream  : the ordering stream (NULL = legacy default stream). The copies
+ *           run on two non-blocking streams the library creates once per
+ *           device and keeps until the process exits; they start after the
+ *           work already queued on `stream`, and work queued on `stream`
+ *           after the call starts only once every copy is complete. The host
+ *           buffers must stay valid, and unmodified for Q, K, V, until then.
+ *
+ * Ownership: the caller owns every buffer; the library allocates no memory.
+ * Asynchronous as fa2_fwd: synchronise `stream` before reading O or LSE.
+ * Argument errors are detected before anything is enqueued. If a CUDA call
+ * fails part way, the chunks enqueued before it still complete, `stream` is
+ * still ordered behind them, and the call returns FA2_ERR_CUDA (O and LSE
+ * are then partly written). Calls for one device are enqueued one at a time
+ * (an internal lock); calls that share a dev_buffer must be ordered by the
+ * caller.
+ */
+int fa2_fwd_host(const void* Q, const void* K, const void* V, void* O, float* LSE,
+                 int B, int H, int N, int D, float scale, int is_causal, int dtype,
+                 int heads_per_chunk, int balanced, void* dev_buffer, size_t dev_bytes,
+                 struct CUstream_st* stream);
+
+/*
  * fa2_device_status — read the device-side watchdog word of the current
  * device, synchronising `stream` first. *status receives 0 when no kernel of
  * this library has timed out waiting on one of its internal barriers since

@@ -111,6 +111,50 @@ def test_no_alloc_entry_point_checks_arguments_first(lib):
     assert so.fa2_fwd_noalloc(*args(N=0)) == lib.FA2_OK
 
 
+def test_host_entry_point_checks_arguments_first(lib):
+    so = lib.library()
+    H1, H2, H3, H4, H5 = (A * i for i in (100, 116, 132, 148, 164))  # fake host addresses, never touched
+    base = dict(Q=H1, K=H2, V=H3, O=H4, LSE=H5, B=1, H=2, N=64, D=64, scale=0.125, is_causal=0, dtype=0, hpc=0,
+                balanced=0, buf=A * 256, nbuf=1 << 30, stream=None)
+
+    def host(**o):
+        a = dict(base, **o)
+        return so.fa2_fwd_host(*[a[x] for x in ("Q", "K", "V", "O", "LSE", "B", "H", "N", "D", "scale", "is_causal",
+                                                "dtype", "hpc", "balanced", "buf", "nbuf", "stream")])
+    assert host(B=-1) == lib.FA2_ERR_INVALID_ARG
+    assert host(hpc=-2) == lib.FA2_ERR_INVALID_ARG
+    assert host(D=96) == lib.FA2_ERR_UNSUPPORTED
+    assert host(dtype=3) == lib.FA2_ERR_UNSUPPORTED
+    assert host(scale=0.0) == lib.FA2_ERR_INVALID_ARG
+    assert host(Q=None) == lib.FA2_ERR_INVALID_ARG
+    assert host(buf=None) == lib.FA2_ERR_INVALID_ARG
+    assert host(buf=A * 256 + 128) == lib.FA2_ERR_ALIGN
+    assert host(O=H1 + 64) == lib.FA2_ERR_INVALID_ARG      # O overlaps Q
+    assert host(LSE=H4 + 16) == lib.FA2_ERR_INVALID_ARG    # LSE overlaps O
+    assert host(B=0) == lib.FA2_OK and host(N=0, Q=None, buf=None) == lib.FA2_OK
+    n = ctypes.c_size_t(0)
+    assert so.fa2_fwd_host_buffer_bytes(1, 2, 64, 64, None) == lib.FA2_ERR_INVALID_ARG
+    assert so.fa2_fwd_host_buffer_bytes(1, 2, 64, 96, ctypes.byref(n)) == lib.FA2_ERR_UNSUPPORTED
+    assert so.fa2_fwd_host_buffer_bytes(-1, 2, 64, 64, ctypes.byref(n)) == lib.FA2_ERR_INVALID_ARG
+
+
+def test_host_chunking_rule():
+    from attention_forward_03_gb300.binding import HOST_CHUNKS, host_chunk_heads, steps_per_head
+    # one K/V tile per 128 keys, one unit per 256 queries; causal unit qt sees 2qt+2 tiles
+    assert steps_per_head(8192, False) == 32 * 64
+    assert steps_per_head(512, True) == 2 + 4 and steps_per_head(300, True) == 2 + 3
+    assert host_chunk_heads(1, 1, 128, False, 152) == 1
+    # the shapes the host pipeline was measured on, and the fastest chunking found
+    assert host_chunk_heads(1, 8, 8192, False, 152) == 2
+    assert host_chunk_heads(4, 16, 8192, False, 152) == 4
+    assert host_chunk_heads(1, 4, 32768, True, 152) == 2
+    assert host_chunk_heads(4, 16, 4096, True, 152) == 16
+    for B, H, N, c in ((1, 8, 8192, False), (4, 16, 8192, False), (2, 12, 1000, False), (1, 4, 300, True),
+                       (3, 7, 64, False)):
+        hpc = host_chunk_heads(B, H, N, c, 152)
+        assert 1 <= hpc <= B * H and -(-(B * H) // hpc) <= HOST_CHUNKS
+
+
 @pytest.mark.parametrize("over", [dict(B=0), dict(H=0), dict(N=0),
                                   dict(B=0, Q=None, K=None, V=None, O=None, LSE=None)])
 def test_empty_problem_is_a_no_op(lib, over):
@@ -151,8 +195,11 @@ def test_product_never_imports_the_oracle():
 
 def test_schedule_choice():
     from attention_forward_03_gb300.binding import choose_schedule
-    assert choose_schedule(1, 8, 8192, False, 152) == "balanced"   # 256 units: last round 68% busy
-    assert choose_schedule(4, 16, 8192, False, 152) == "units"     # 2048 units: 96% of rounds busy
+    assert choose_schedule(1, 8, 8192, False, 152) == "balanced"   # 256 units: 2 rounds of 64 vs 112 steps
+    assert choose_schedule(4, 16, 8192, False, 152) == "units"     # 2048 units: 14 rounds of 64 vs 866 steps
     assert choose_schedule(1, 8, 8192, True, 152) == "units"       # causal: zig-zag rounds
-    assert choose_schedule(2, 12, 1000, False, 152) == "units"     # fewer units than SMs
+    assert choose_schedule(2, 12, 1000, False, 152) == "units"     # 8-tile units: 8 vs 9 steps
     assert choose_schedule(1, 152, 256, False, 152) == "units"     # exactly one full round
+    assert choose_schedule(1, 1, 8192, False, 152) == "balanced"   # 32 long units on 152 SMs
+    assert choose_schedule(1, 1, 128, False, 152) == "units"       # one tiny unit
+    assert choose_schedule(0, 8, 8192, False, 152) == "units"      # empty
