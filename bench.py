@@ -93,7 +93,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.dev), f"--query-gpu={self.QUERY}", "--format=csv,noheader,nounits",
-                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+                 "-lms", "50"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except OSError:
             self.proc = None
             return
@@ -182,44 +182,63 @@ def whole_job_tflops(flops_per_step: float, steps: int, world: int, max_seconds:
 
 
 # ------------------------------------------------------------- CPU oracle leg
-def oracle_sample(w: workloads.Workload, target_seconds: float, inputs=None):
-    """Time the fp64 oracle on a bounded sample of the workload's rows.
+def _row_flops(w: workloads.Workload, rows):
+    import numpy as np
+    rows = np.asarray(rows)
+    if not w.causal:
+        return 4.0 * w.D * w.N * len(rows)
+    return float(np.sum(4.0 * w.D * np.minimum(w.N, rows % w.N + 1)))
 
-    The sample is a uniform random subset of all B*H*N query rows (each row
-    over its full allowed key range), sized from a short calibration run so
-    that it takes about `target_seconds`; if the whole workload fits in that
-    time, the sample is the whole workload.
-    Returns (tflops, seconds, rows, threads, description)."""
+
+def oracle_rows(w: workloads.Workload, target_seconds: float, inputs):
+    """Rows of a bounded oracle sample of the workload: a uniform random subset
+    of all B*H*N query rows sized so that one oracle call on it takes about
+    `target_seconds` (None = the whole workload, when that fits). The rate is
+    calibrated on growing probes until one runs for about a second, so that
+    per-call fixed costs do not dominate it."""
     import numpy as np
 
     import oracle
-    q, k, v = inputs if inputs is not None else workloads.make_inputs(w)
+    q, k, v = inputs
     threads = oracle.default_threads()
-    N = w.N
-    total = w.B * w.H * N
-
-    def row_flops(rows):
-        rows = np.asarray(rows)
-        if not w.causal:
-            return 4.0 * w.D * N * len(rows)
-        return float(np.sum(4.0 * w.D * np.minimum(N, rows % N + 1)))
-
-    rng = np.random.default_rng(0)
-    probe = np.sort(rng.choice(total, size=min(total, 2 * threads), replace=False))
-    t0 = time.perf_counter()
-    oracle.attention_fwd(q, k, v, w.scale, w.causal, rows=probe, nthreads=threads)
-    rate = row_flops(probe) / max(time.perf_counter() - t0, 1e-4)
+    total = w.B * w.H * w.N
     per_row = workloads.flops(w) / total
+    rng = np.random.default_rng(0)
+    size = min(total, 2 * threads)
+    while True:
+        probe = np.sort(rng.choice(total, size=size, replace=False))
+        t0 = time.perf_counter()
+        oracle.attention_fwd(q, k, v, w.scale, w.causal, rows=probe, nthreads=threads)
+        took = max(time.perf_counter() - t0, 1e-4)
+        rate = _row_flops(w, probe) / took
+        if took >= min(1.0, target_seconds / 4) or size >= total:
+            break
+        size = int(min(total, max(2 * size, size * min(1.0, target_seconds / 4) / took)))
     want = int(min(total, max(threads, target_seconds * rate / per_row)))
-    rows = np.sort(rng.choice(total, size=want, replace=False)) if want < total else None
+    return np.sort(rng.choice(total, size=want, replace=False)) if want < total else None
+
+
+def time_oracle(w: workloads.Workload, rows, inputs):
+    """One timed oracle call on `rows` (None = every row).
+    Returns (tflops, seconds, rows, threads, description)."""
+    import oracle
+    q, k, v = inputs
+    threads = oracle.default_threads()
+    total = w.B * w.H * w.N
     t0 = time.perf_counter()
     oracle.attention_fwd(q, k, v, w.scale, w.causal, rows=rows, nthreads=threads)
     secs = time.perf_counter() - t0
     n = total if rows is None else len(rows)
-    fl = workloads.flops(w) if rows is None else row_flops(rows)
+    fl = workloads.flops(w) if rows is None else _row_flops(w, rows)
     what = "the whole workload" if rows is None else f"{n} of its {total} query rows, drawn uniformly"
     desc = f"{what} ({w.describe()}, each row over its full allowed key range), fp64, {threads} threads"
     return fl / secs / 1e12, secs, n, threads, desc
+
+
+def oracle_sample(w: workloads.Workload, target_seconds: float, inputs=None):
+    """Time the fp64 oracle on a bounded sample of about `target_seconds`."""
+    inputs = inputs if inputs is not None else workloads.make_inputs(w)
+    return time_oracle(w, oracle_rows(w, target_seconds, inputs), inputs)
 
 
 # -------------------------------------------------------------------- arms
@@ -227,14 +246,17 @@ def run_reference(args, w, rank, world):
     if rank != 0:
         return None
     import numpy as np  # noqa: F401
-    per_step = max(1.0, args.reference_seconds / max(1, args.steps + args.warmup))
+    # one sample of rows, sized once, timed every step: the whole run takes
+    # about reference_seconds plus the calibration
+    per_step = max(0.05, args.reference_seconds / max(1, args.steps + args.warmup))
     inputs = workloads.make_inputs(w)
+    rows = oracle_rows(w, per_step, inputs)
     for _ in range(args.warmup):
-        oracle_sample(w, per_step, inputs)
+        time_oracle(w, rows, inputs)
     vals, secs = [], []
     desc, threads = "", 1
     for _ in range(args.steps):
-        tf, s, rows, threads, desc = oracle_sample(w, per_step, inputs)
+        tf, s, n, threads, desc = time_oracle(w, rows, inputs)
         vals.append(tf)
         secs.append(s)
     value = statistics.median(vals)
@@ -390,7 +412,7 @@ def run_gb300(args, w, rank, world, local):
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--steps", type=int, default=1000)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--workload", default="target", choices=sorted(workloads.WORKLOADS))
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
