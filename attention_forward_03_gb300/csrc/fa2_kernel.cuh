@@ -23,10 +23,14 @@
 // Tensor memory (512 columns x 128 lanes of 32 bits):
 //   [128t, 128t+128)      S of sub-tile t (fp32 scores)
 //   [256+tD, 256+tD+D)    O accumulator of sub-tile t (fp32)
-// Shared memory: Q (2 sub-tiles, resident for the segment), P (2 sub-tiles,
-// 16-bit), and a ring of K/V tiles; all 128-byte swizzled in 64-element-wide
-// panels, the operand layout the MMAs read (TMA writes Q/K/V that way; the
-// softmax threads write P that way).
+//   [384+64t, 448+64t)    D = 64 only: P of sub-tile t (16-bit pairs)
+// Shared memory: Q (2 sub-tiles, resident for the segment), at D = 128 P
+// (2 sub-tiles, 16-bit), and a ring of K/V tiles; all 128-byte swizzled in
+// 64-element-wide panels, the operand layout the MMAs read (TMA writes Q/K/V
+// that way; the softmax threads write P that way). At D = 64 the O
+// accumulators leave room for P in tensor memory, where the P.V MMA reads it
+// as its A operand (the faster form of the instruction) and its shared
+// memory goes to a deeper K/V ring.
 //
 // Per K/V tile j the MMA issuer of sub-tile t issues:
 //   S_t(j+1) = Q_t K_{j+1}^T   once softmax t has loaded S_t(j) into registers
@@ -100,10 +104,11 @@ template <int D>
 struct Layout {
   static constexpr int kPanels = D / 64;
   static constexpr int kTileBytes = kPanels * kPanelBytes;  // 128 rows x D (Q sub-tile, K or V tile)
-  static constexpr int kStages = (D == 128) ? 3 : 8;
+  static constexpr bool kPInTmem = (D == 64);
+  static constexpr int kStages = (D == 128) ? 3 : 12;
   static constexpr int kQBytes = kSubTiles * kTileBytes;
   static constexpr int kPOffset = kQBytes;
-  static constexpr int kRingOffset = kPOffset + kSubTiles * kPTileBytes;
+  static constexpr int kRingOffset = kPOffset + (kPInTmem ? 0 : kSubTiles * kPTileBytes);
   static constexpr int kBarOffset = kRingOffset + kStages * kTileBytes;
   // barriers: q_full, q_empty, ring full[S], ring empty[S], s_full[2], s_free[2], p_full[2], p_free[2],
   // o_full[2], drain[2], part_done[2]
@@ -111,7 +116,8 @@ struct Layout {
   static constexpr int kMiscOffset = kBarOffset + kNumBars * 8;
   static constexpr int kSmemBytes = kMiscOffset + 16 + 1024;  // + slack for 1 KB alignment
   static constexpr uint32_t kColO = 2 * kKeys;                 // O0 at 256, O1 at 256 + D
-  static_assert(kColO + 2 * D <= kTmemCols, "TMEM budget");
+  static constexpr uint32_t kColP = kColO + 2 * D;              // D = 64: P0 at 384, P1 at 448
+  static_assert(kColO + 2 * D + (kPInTmem ? 2 * kKeys / 2 : 0) <= kTmemCols, "TMEM budget");
   static_assert(kSmemBytes <= 232448, "shared memory budget");
 };
 
@@ -410,17 +416,23 @@ __global__ void __launch_bounds__(kThreads, 1)
             mma_ss_w(dt, qa + off, kHi, ka + off, kHi, idesc_s, kk > 0 ? 1u : 0u);
           }
         };
-        // O_t (+)= P_t V : P (K-major) and V (MN-major) from shared memory,
-        // 8 steps of 16 keys.
+        // O_t (+)= P_t V : P (K-major, shared memory; D = 64: tensor memory)
+        // and V (MN-major, shared memory), 8 steps of 16 keys.
         auto issue_pv = [&](int t, int slot, bool acc) {
           const uint32_t pa = p_lo + static_cast<uint32_t>((t * kPTileBytes) >> 4);
           const uint32_t va = ring_lo_v + static_cast<uint32_t>(slot * (L::kTileBytes >> 4));
           const uint32_t dt = tmem + L::kColO + static_cast<uint32_t>(t * D);
+          const uint32_t pt = tmem + L::kColP + static_cast<uint32_t>(t * (kKeys / 2));
 #pragma unroll
           for (int kk = 0; kk < kKeys / 16; ++kk) {
-            const uint32_t po = static_cast<uint32_t>(((kk >> 2) * kPanelBytes + (kk & 3) * 32) >> 4);
-            mma_ss_w(dt, pa + po, kHi, va + static_cast<uint32_t>((kk * 16 * 128) >> 4), kHi, idesc_o,
-                     (acc || kk > 0) ? 1u : 0u);
+            const uint32_t vb = va + static_cast<uint32_t>((kk * 16 * 128) >> 4);
+            const uint32_t acc_kk = (acc || kk > 0) ? 1u : 0u;
+            if constexpr (L::kPInTmem) {
+              mma_ts_w(dt, pt + 8u * kk, vb, kHi, idesc_o, acc_kk);
+            } else {
+              const uint32_t po = static_cast<uint32_t>(((kk >> 2) * kPanelBytes + (kk & 3) * 32) >> 4);
+              mma_ss_w(dt, pa + po, kHi, vb, kHi, idesc_o, acc_kk);
+            }
           }
         };
 
@@ -511,6 +523,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // this thread's P row in shared memory: 128 bytes per 64 keys, 16-byte
     // chunks placed by the 128-byte swizzle (chunk c of row r at c ^ (r % 8))
     const uint32_t p_row = sP + static_cast<uint32_t>(t * kPTileBytes + rr * 128);
+    const uint32_t tP = tmem + lane_off + L::kColP + static_cast<uint32_t>(t * (kKeys / 2));
     const uint32_t p_xor = static_cast<uint32_t>(rr & 7);
     const float c = p.scale_log2;
     uint32_t s_phase = 0, o_phase = 0, part_phase = 0;
@@ -588,12 +601,18 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (!fr) { ok = false; break; }
           tc_fence_after_sync();
         }
-        // P: 16 chunks of 8 keys (4 packed pairs) into the swizzled row
+        if constexpr (L::kPInTmem) {
+          // P: this row's 64 packed pairs into its lane of the P columns
+          tmem_st32x32(tP, *reinterpret_cast<const uint32_t(*)[32]>(pk));
+          tmem_st32x32(tP + 32, *reinterpret_cast<const uint32_t(*)[32]>(pk + 32));
+        } else {
+          // P: 16 chunks of 8 keys (4 packed pairs) into the swizzled row
 #pragma unroll
-        for (int ch = 0; ch < 16; ++ch) {
-          const uint32_t addr = p_row + static_cast<uint32_t>((ch >> 3) * kPanelBytes) +
-                                ((static_cast<uint32_t>(ch & 7) ^ p_xor) << 4);
-          st_shared_v4(addr, pk[4 * ch], pk[4 * ch + 1], pk[4 * ch + 2], pk[4 * ch + 3]);
+          for (int ch = 0; ch < 16; ++ch) {
+            const uint32_t addr = p_row + static_cast<uint32_t>((ch >> 3) * kPanelBytes) +
+                                  ((static_cast<uint32_t>(ch & 7) ^ p_xor) << 4);
+            st_shared_v4(addr, pk[4 * ch], pk[4 * ch + 1], pk[4 * ch + 2], pk[4 * ch + 3]);
+          }
         }
         // O holds P.V up to tile j-1 (complete, see above): rescale it now
         // that the scores are no longer held in registers.
@@ -606,10 +625,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
             tmem_st32x32(tO + cc, o);
           }
-          tmem_wait_st();
         }
-        // the tensor core reads P through the async proxy
-        fence_proxy_async_shared();
+        tmem_wait_st();
+        // the tensor core reads a shared-memory P through the async proxy
+        if constexpr (!L::kPInTmem) fence_proxy_async_shared();
         tc_fence_before_sync();
         mbar_arrive(bar_p);
         ++p_count;
