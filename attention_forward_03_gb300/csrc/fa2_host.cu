@@ -42,7 +42,7 @@ size_t round256(size_t x) { return (x + 255) / 256 * 256; }
 // starting on a 256-byte boundary. The LSE part holds each chunk's rows from
 // a 16-byte boundary (the kernel's alignment rule), so it is sized for the
 // worst case of one head per chunk: B*H*N floats plus 3 floats of padding
-// per head.
+// per head (there are never more chunks than heads).
 struct BufferLayout {
   size_t k, v, o, lse, ws, ws_bytes, total;
 };
@@ -135,7 +135,11 @@ extern "C" int fa2_fwd_host(const void* Q, const void* K, const void* V, void* O
   char* dv = base + L.v;
   char* dout = base + L.o;
   float* dlse = reinterpret_cast<float*>(base + L.lse);
-  const size_t lse_stride = (static_cast<size_t>(hpc) * N + 3) / 4 * 4;  // floats per chunk slot
+  // The first chunk is half the size (so the first kernel starts sooner);
+  // the others hold hpc heads, the last what remains (half a chunk when B*H
+  // is a multiple of hpc, so the work after the last copy-in is short too).
+  const int first = hpc >= 2 ? hpc / 2 : hpc;
+  size_t lse_at = 0;  // device LSE rows of the next chunk start here (a multiple of 4 floats)
   void* ws = balanced ? static_cast<void*>(base + L.ws) : nullptr;
   const char* hq = static_cast<const char*>(Q);
   const char* hk = static_cast<const char*>(K);
@@ -148,12 +152,14 @@ extern "C" int fa2_fwd_host(const void* Q, const void* K, const void* V, void* O
   if (e == cudaSuccess) e = cudaStreamWaitEvent(pp.out, pp.entry, 0);
   if (e != cudaSuccess) return fa2::record_cuda_error(e);
   rc = FA2_OK;
-  for (int h0 = 0, c = 0; h0 < bh && rc == FA2_OK; h0 += hpc, ++c) {
-    const int nh = hpc < bh - h0 ? hpc : bh - h0;
+  for (int h0 = 0, nh = 0; h0 < bh && rc == FA2_OK; h0 += nh) {
+    nh = h0 == 0 ? first : hpc;
+    if (nh > bh - h0) nh = bh - h0;
     const size_t off = static_cast<size_t>(h0) * head_elems * 2;
     const size_t n = static_cast<size_t>(nh) * head_elems * 2;
     const size_t loff = static_cast<size_t>(h0) * N;  // host LSE rows of the chunk
-    float* dl = dlse + static_cast<size_t>(c) * lse_stride;
+    float* dl = dlse + lse_at;
+    lse_at = (lse_at + static_cast<size_t>(nh) * N + 3) / 4 * 4;
     e = cudaMemcpyAsync(dq + off, hq + off, n, cudaMemcpyHostToDevice, pp.in);
     if (e == cudaSuccess) e = cudaMemcpyAsync(dk + off, hk + off, n, cudaMemcpyHostToDevice, pp.in);
     if (e == cudaSuccess) e = cudaMemcpyAsync(dv + off, hv + off, n, cudaMemcpyHostToDevice, pp.in);

@@ -159,6 +159,9 @@ int fa2_fwd_host_buffer_bytes(int B, int H, int N, int D, size_t* bytes);
  *           but the copies then run one after another.
  * B, H, N, D, scale, is_causal, dtype: as fa2_fwd.
  * heads_per_chunk: heads (of the flattened B*H) per chunk; 0 = ceil(B*H / 4).
+ *           The first chunk holds half as many (rounded down, at least one)
+ *           so that the first kernel starts sooner; the last holds what
+ *           remains.
  * balanced: nonzero runs each chunk on the balanced schedule of fa2_fwd_ws
  *           (workspace inside dev_buffer), zero on the schedule of fa2_fwd.
  * dev_buffer, dev_bytes: caller-owned device staging memory of the current
