@@ -43,12 +43,17 @@ KERNEL_SOURCES = os.path.join(ROOT, "attention_forward_03_gb300", "csrc")
 
 
 # ------------------------------------------------------------------ helpers
+# the files that define the kernel and its device-resident launch (the
+# host-memory pipeline and the no-allocation entry point do not change either)
+KERNEL_FILES = ("fa2_kernel.cuh", "fa2_launch.h", "sm103_ptx.cuh", "tmem_io.cuh", "fa2_fwd_d64.cu", "fa2_fwd_d128.cu",
+                "fa2_api.cu")
+
+
 def kernel_source_hash() -> str:
     h = hashlib.sha256()
-    for f in sorted(os.listdir(KERNEL_SOURCES)):
-        if f.endswith((".cu", ".cuh", ".h")):
-            with open(os.path.join(KERNEL_SOURCES, f), "rb") as fh:
-                h.update(f.encode() + b"\0" + fh.read())
+    for f in sorted(KERNEL_FILES):
+        with open(os.path.join(KERNEL_SOURCES, f), "rb") as fh:
+            h.update(f.encode() + b"\0" + fh.read())
     return h.hexdigest()[:16]
 
 
