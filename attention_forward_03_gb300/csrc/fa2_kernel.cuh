@@ -83,6 +83,8 @@ constexpr uint32_t kTmemCols = 512;
 // than this many powers of two (so p <= 2^8 = 256, exact in the 16-bit P and
 // far from overflow in the fp32 sums).
 constexpr float kRescaleLog2 = 8.0f;
+// Sleep between polls of the producer's and MMA issuers' waits (see wait_bounded).
+constexpr unsigned kNapNs = 20;
 
 // Watchdog codes written to the status word (site of the wait that gave up).
 enum : int {
@@ -214,11 +216,15 @@ struct Watchdog {
 // Bounded wait. Returns false when the limit passes (recording `site` in the
 // status word and raising the CTA's abort flag) or when another role of the
 // CTA has already aborted. `honour_abort` = false is used while draining.
+// `nap_ns` > 0 sleeps between polls: the single-thread roles (producer, MMA
+// issuers) share each SM sub-partition with softmax warps, whose issue slots
+// a tight polling loop would take (measured: 12 % on long causal work).
 __device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, const Watchdog& wd, int site,
-                                          bool honour_abort = true) {
+                                          bool honour_abort = true, unsigned nap_ns = 0) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = global_timer_ns();
   for (uint32_t it = 1;; ++it) {
+    if (nap_ns) __nanosleep(nap_ns);
     if (mbar_try_wait(bar, parity)) return true;
     if ((it & 31u) == 0) {
       if (honour_abort && *wd.abort_flag) return false;
@@ -368,7 +374,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         SegCursor cur = first_cursor(p);
         Segment w;
         auto load_tile = [&](const CUtensorMap* map, int j, uint32_t is_v) -> bool {
-          if (!wait_bounded(bar_empty(slot), ring_ph ^ 1u, wd, kSiteLoadRingEmpty)) return false;
+          if (!wait_bounded(bar_empty(slot), ring_ph ^ 1u, wd, kSiteLoadRingEmpty, true, kNapNs)) return false;
           const uint32_t full = bar_full(slot, is_v);
           if (!(p.test_withhold && issued == 0)) {  // test hook: the first tile never arrives
             mbar_arrive_expect_tx(full, L::kTileBytes);
@@ -386,7 +392,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           return true;
         };
         while (ok && next_segment<kCausal>(cur, w, p)) {
-          if (q_round > 0 && !wait_bounded(bar_q_empty, (q_round - 1) & 1u, wd, kSiteLoadQEmpty)) {
+          if (q_round > 0 && !wait_bounded(bar_q_empty, (q_round - 1) & 1u, wd, kSiteLoadQEmpty, true, kNapNs)) {
             ok = false;
             break;
           }
@@ -408,9 +414,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int s = static_cast<int>(i % L::kStages);
           const uint32_t is_v = (types >> s) & 1u;
           const uint32_t par = (((is_v ? vbits : kbits) >> s) & 1u) ^ 1u;
-          wait_bounded(bar_full(s, is_v), par, wd, kSiteDrain, false);
+          wait_bounded(bar_full(s, is_v), par, wd, kSiteDrain, false, kNapNs);
         }
-        if (q_round > 0) wait_bounded(bar_q_full, (q_round - 1) & 1u, wd, kSiteDrain, false);
+        if (q_round > 0) wait_bounded(bar_q_full, (q_round - 1) & 1u, wd, kSiteDrain, false, kNapNs);
       }
       __syncwarp();
     } else if (warp < kMmaWarp + kIssuers) {
@@ -471,7 +477,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int s = static_cast<int>(idx % L::kStages);
           const uint32_t par = (bits[is_v] >> s) & 1u;
           bits[is_v] ^= 1u << s;
-          return wait_bounded(bar_full(s, is_v), par, wd, kSiteMmaRingFull) ? s : -1;
+          return wait_bounded(bar_full(s, is_v), par, wd, kSiteMmaRingFull, true, kNapNs) ? s : -1;
         };
         uint32_t base_idx = 0;  // global load index of the current segment's first tile
         bool ok = true;
@@ -486,14 +492,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             bool s_out[2] = {false, false};  // an S issued whose TMEM the softmax has not released yet
             while (ok && next_segment<kCausal>(cur, w, p)) {
               const int b = w.kv_begin, e = w.kv_end;
-              if (!wait_bounded(bar_q_full, q_round & 1u, wd, kSiteMmaQFull)) { ok = false; break; }
+              if (!wait_bounded(bar_q_full, q_round & 1u, wd, kSiteMmaQFull, true, kNapNs)) { ok = false; break; }
               ++q_round;
               for (int j = b; j < e && ok; ++j) {
                 const int slot_k = take(base_idx + k_index(j, b), 0u);
                 if (slot_k < 0) { ok = false; break; }
                 for (int t = 0; t < 2; ++t) {
                   if (s_out[t]) {
-                    if (!wait_bounded(bar_s_free0 + 8 * t, s_free_ph[t], wd, kSiteMmaSFree)) { ok = false; break; }
+                    if (!wait_bounded(bar_s_free0 + 8 * t, s_free_ph[t], wd, kSiteMmaSFree, true, kNapNs)) { ok = false; break; }
                     s_free_ph[t] ^= 1u;
                   }
                   tc_fence_after_sync();
@@ -517,7 +523,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int slot_v = take(base_idx + v_index(j, b, e), 1u);
                 if (slot_v < 0) { ok = false; break; }
                 for (int t = 0; t < 2; ++t) {
-                  if (!wait_bounded(bar_p_full0 + 8 * t, p_full_ph[t], wd, kSiteMmaPFull)) { ok = false; break; }
+                  if (!wait_bounded(bar_p_full0 + 8 * t, p_full_ph[t], wd, kSiteMmaPFull, true, kNapNs)) { ok = false; break; }
                   p_full_ph[t] ^= 1u;
                   tc_fence_after_sync();
                   issue_pv(t, slot_v, j > b);
@@ -540,7 +546,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           bool s_out = false;
           auto next_s = [&](int slot_k) -> bool {
             if (s_out) {
-              if (!wait_bounded(bar_s_free0 + 8 * t, s_free_ph, wd, kSiteMmaSFree)) return false;
+              if (!wait_bounded(bar_s_free0 + 8 * t, s_free_ph, wd, kSiteMmaSFree, true, kNapNs)) return false;
               s_free_ph ^= 1u;
             }
             tc_fence_after_sync();
@@ -552,7 +558,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           };
           while (ok && next_segment<kCausal>(cur, w, p)) {
             const int b = w.kv_begin, e = w.kv_end;
-            if (!wait_bounded(bar_q_full, q_round & 1u, wd, kSiteMmaQFull)) { ok = false; break; }
+            if (!wait_bounded(bar_q_full, q_round & 1u, wd, kSiteMmaQFull, true, kNapNs)) { ok = false; break; }
             ++q_round;
             int slot_k = take(base_idx + k_index(b, b), 0u);
             if (slot_k < 0 || !next_s(slot_k)) { ok = false; break; }
@@ -565,7 +571,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               }
               const int slot_v = take(base_idx + v_index(j, b, e), 1u);
               if (slot_v < 0) { ok = false; break; }
-              if (!wait_bounded(bar_p_full0 + 8 * t, p_full_ph, wd, kSiteMmaPFull)) { ok = false; break; }
+              if (!wait_bounded(bar_p_full0 + 8 * t, p_full_ph, wd, kSiteMmaPFull, true, kNapNs)) { ok = false; break; }
               p_full_ph ^= 1u;
               tc_fence_after_sync();
               issue_pv(t, slot_v, j > b);
@@ -578,7 +584,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         // Drain: all issued tensor-core work completes before TMEM is released.
         mma_commit(bar_drain + 8 * me);
-        wait_bounded(bar_drain + 8 * me, 0u, wd, kSiteDrain, false);
+        wait_bounded(bar_drain + 8 * me, 0u, wd, kSiteDrain, false, kNapNs);
       }
       __syncwarp();
     }
