@@ -283,9 +283,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   using L = Layout<D>;
   // MMA issuers split by instruction type (one thread for every S, one for
   // every P.V) or by sub-tile (each thread S and P.V of one sub-tile). Both
-  // measured: by type is 3-7 % faster on causal head-dim-128 work, by sub-tile
-  // 3-5 % faster on the non-causal and head-dim-64 workloads.
-  constexpr bool kTypeSplit = kCausal && D == 128;
+  // measured (with the issuers sleeping between polls): by type is 10-15 %
+  // faster at head dim 128, by sub-tile 2-6 % faster at head dim 64.
+  constexpr bool kTypeSplit = D == 128;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   const uint32_t raw = smem_addr(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
