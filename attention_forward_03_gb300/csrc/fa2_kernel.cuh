@@ -15,9 +15,12 @@
 //   work unit  = 256 query rows of one (batch, head): two 128-row sub-tiles.
 //   warps 0-3  softmax warpgroup for sub-tile 0 (thread = query row = TMEM lane)
 //   warps 4-7  softmax warpgroup for sub-tile 1
-//   warps 8-9  tcgen05 MMA issuers: with two issuers warp 8 + t drives
-//              sub-tile t, with one issuer warp 8 drives both; warp 8 also
-//              owns the TMEM allocation
+//   warps 8-9  tcgen05 MMA issuers (one thread each): at head dim 128 warp 8
+//              issues every S and warp 9 every P.V; at head dim 64 warp 8 + t
+//              issues both of sub-tile t. Warp 8 also owns the TMEM
+//              allocation. The issuers and the producer sleep briefly between
+//              barrier polls, leaving issue slots to the softmax warps that
+//              share their SM sub-partitions.
 //   warp  10   TMA producer (one thread); warp 11 idle. Warps 8-11 form the
 //              third warpgroup, which gives registers to the softmax ones.
 // Tensor memory (512 columns x 128 lanes of 32 bits):
@@ -32,9 +35,9 @@
 // as its A operand (the faster form of the instruction) and its shared
 // memory goes to a deeper K/V ring.
 //
-// Per K/V tile j the MMA issuer of sub-tile t issues:
+// Per K/V tile j and sub-tile t the issuers issue:
 //   S_t(j+1) = Q_t K_{j+1}^T   once softmax t has loaded S_t(j) into registers
-//   O_t (+)= P_t(j) V_j        once softmax t has written P_t(j) to shared memory
+//   O_t (+)= P_t(j) V_j        once softmax t has written P_t(j)
 // P lives in shared memory, so the next scores are computed while the softmax
 // of the current tile runs: each softmax warpgroup works tile after tile
 // without waiting for a P.V product. Rescaling O (rare: the exponent base
