@@ -54,17 +54,8 @@ __device__ __forceinline__ void tma_prefetch_map(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
 
-// 3-D tiled bulk tensor load global -> shared, completion counted on `bar` in bytes.
-__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, uint32_t bar,
-                                            int c0, int c1, int c2) {
-  asm volatile(
-      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-      " [%0], [%1, {%3, %4, %5}], [%2];"
-      ::"r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1), "r"(c2)
-      : "memory");
-}
-
-// Same, with an L2 eviction-priority policy (from createpolicy).
+// 3-D tiled bulk tensor load global -> shared, completion counted on `bar` in
+// bytes, with an L2 eviction-priority policy (from createpolicy).
 __device__ __forceinline__ void tma_load_3d_hint(uint32_t dst, const CUtensorMap* map, uint32_t bar,
                                                  int c0, int c1, int c2, uint64_t policy) {
   asm volatile(
@@ -115,36 +106,11 @@ __device__ __forceinline__ void tmem_wait_st() {
   asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
 
-// D[tmem] (+)= A[smem] * B[smem]^T   (kind::f16, fp32 accumulate, one CTA)
-__device__ __forceinline__ void mma_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
-                                       uint32_t idesc, uint32_t accumulate) {
-  asm volatile(
-      "{\n"
-      ".reg .pred p;\n"
-      "setp.ne.b32 p, %4, 0;\n"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n"
-      "}\n" ::"r"(d_tmem),
-      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
-
-// D[tmem] (+)= A[tmem] * B[smem]   (A read from tensor memory)
-__device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
-                                       uint32_t idesc, uint32_t accumulate) {
-  asm volatile(
-      "{\n"
-      ".reg .pred p;\n"
-      "setp.ne.b32 p, %4, 0;\n"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n"
-      "}\n" ::"r"(d_tmem),
-      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
-
-// The same two MMAs with each 64-bit shared-memory descriptor passed as
-// (low word, high word): the low word holds the start address and the
-// leading byte offset, the high word the stride byte offset, version and
-// swizzle mode, so stepping through a tile only adds to the low word.
+// D[tmem] (+)= A * B (kind::f16, fp32 accumulate, one CTA), A and B from
+// shared memory. Each 64-bit shared-memory descriptor is passed as (low
+// word, high word): the low word holds the start address and the leading
+// byte offset, the high word the stride byte offset, version and swizzle
+// mode, so stepping through a tile only adds to the low word.
 __device__ __forceinline__ void mma_ss_w(uint32_t d_tmem, uint32_t a_lo, uint32_t a_hi, uint32_t b_lo, uint32_t b_hi,
                                          uint32_t idesc, uint32_t accumulate) {
   asm volatile(
@@ -160,6 +126,7 @@ __device__ __forceinline__ void mma_ss_w(uint32_t d_tmem, uint32_t a_lo, uint32_
       : "memory");
 }
 
+// The same with A read from tensor memory.
 __device__ __forceinline__ void mma_ts_w(uint32_t d_tmem, uint32_t a_tmem, uint32_t b_lo, uint32_t b_hi,
                                          uint32_t idesc, uint32_t accumulate) {
   asm volatile(
@@ -174,7 +141,10 @@ __device__ __forceinline__ void mma_ts_w(uint32_t d_tmem, uint32_t a_tmem, uint3
       : "memory");
 }
 
-// Low / high words of the 128B-swizzle descriptor built by smem_desc_sw128.
+// Low / high words of a shared-memory matrix descriptor for a 128-byte-
+// swizzled operand: start address, leading and stride byte offsets (16-byte
+// units), descriptor version 1 (bits 46-47), swizzle mode 2 = 128B (bits
+// 61-63).
 __host__ __device__ constexpr uint32_t desc_lo_sw128(uint32_t saddr, uint32_t lbo_bytes) {
   return ((saddr >> 4) & 0x3FFFu) | (((lbo_bytes >> 4) & 0x3FFFu) << 16);
 }
@@ -186,20 +156,6 @@ __host__ __device__ constexpr uint32_t desc_hi_sw128(uint32_t sbo_bytes) {
 __device__ __forceinline__ void mma_commit(uint32_t bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
                : "memory");
-}
-
-// Shared-memory matrix descriptor for a 128-byte-swizzled operand tile.
-//   start address, leading/stride byte offsets (16-byte units), descriptor
-//   version 1 (bits 46-47), swizzle mode 2 = 128B (bits 61-63).
-__device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr, uint32_t lbo_bytes,
-                                                    uint32_t sbo_bytes) {
-  uint64_t d = 0;
-  d |= static_cast<uint64_t>((saddr >> 4) & 0x3FFFu);
-  d |= static_cast<uint64_t>((lbo_bytes >> 4) & 0x3FFFu) << 16;
-  d |= static_cast<uint64_t>((sbo_bytes >> 4) & 0x3FFFu) << 32;
-  d |= static_cast<uint64_t>(1) << 46;
-  d |= static_cast<uint64_t>(2) << 61;
-  return d;
 }
 
 // Instruction descriptor for kind::f16 with fp32 accumulation, M = 128.
