@@ -12,8 +12,12 @@ Contents
   online_merge    the tile-by-tile (m, l) recurrence of the pages, in numpy
                   fp64, used only to pin the definition against the method's
                   own recurrence.
+  attention_bwd   the gradient of the forward definition w.r.t. Q, K, V for
+                  an upstream gradient dO (C, fp64). See ``fa2_bwd_oracle.c``.
 
-Every function here is pinned by ``tests/test_oracle_pins.py``.
+Every function here is pinned by ``tests/test_oracle_pins.py`` (forward) and
+``tests/test_oracle_bwd_pins.py`` (gradient).
 """
 from .reference import attention_fwd, sample_rows, default_threads  # noqa: F401
 from .online import online_merge  # noqa: F401
+from .gradient import attention_bwd  # noqa: F401
