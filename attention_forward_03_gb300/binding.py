@@ -39,6 +39,11 @@ SIGNATURES = {
     "fa2_fwd_host": (ctypes.c_int, [_VP, _VP, _VP, _VP, _VP, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                     ctypes.c_int, ctypes.c_float, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                     ctypes.c_int, _VP, ctypes.c_size_t, _VP]),
+    "fa2_bwd_workspace_bytes": (ctypes.c_int, [ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                               ctypes.POINTER(ctypes.c_size_t)]),
+    "fa2_bwd": (ctypes.c_int, [_VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, ctypes.c_int, ctypes.c_int,
+                               ctypes.c_int, ctypes.c_int, ctypes.c_float, ctypes.c_int, ctypes.c_int, _VP,
+                               ctypes.c_size_t, _VP]),
     "fa2_device_status": (ctypes.c_int, [_VP, ctypes.POINTER(ctypes.c_int), ctypes.c_int]),
     "fa2_set_watchdog_ns": (ctypes.c_int, [ctypes.c_ulonglong]),
     "fa2_test_withhold_next_load": (ctypes.c_int, [ctypes.c_int]),
@@ -109,6 +114,21 @@ def fa2_fwd_host_buffer_bytes(B: int, H: int, N: int, D: int) -> int:
     _check(library().fa2_fwd_host_buffer_bytes(int(B), int(H), int(N), int(D), ctypes.byref(n)),
            "fa2_fwd_host_buffer_bytes")
     return n.value
+
+
+def fa2_bwd_workspace_bytes(B: int, H: int, N: int, D: int) -> int:
+    n = ctypes.c_size_t(0)
+    _check(library().fa2_bwd_workspace_bytes(int(B), int(H), int(N), int(D), ctypes.byref(n)),
+           "fa2_bwd_workspace_bytes")
+    return n.value
+
+
+def fa2_bwd(Q: int, K: int, V: int, O: int, dO: int, LSE: int, dQ: int, dK: int, dV: int, B: int, H: int, N: int,
+            D: int, scale: float, is_causal: int, dtype: int, workspace: int | None, workspace_bytes: int,
+            stream: int | None) -> int:
+    """Pointer-level call of the backward pass; returns the raw status code."""
+    return library().fa2_bwd(Q, K, V, O, dO, LSE, dQ, dK, dV, B, H, N, D, float(scale), int(is_causal),
+                             int(dtype), workspace, int(workspace_bytes), stream)
 
 
 def fa2_device_status(stream: int | None = None, clear: bool = False) -> int:
@@ -321,3 +341,51 @@ def attention_forward_host(q, k, v, scale: float | None = None, is_causal: bool 
         if synchronize:
             s.synchronize()
     return out, lse
+
+
+def attention_backward(q, k, v, o, lse, do, scale: float | None = None, is_causal: bool = False, dq=None, dk=None,
+                       dv=None, workspace=None, stream=None):
+    """Gradient of attention_forward w.r.t. q, k, v for an upstream gradient `do` (fa2_bwd).
+
+    q, k, v, o, do: contiguous CUDA tensors [B, H, N, D] of one dtype (fp16/bf16);
+    o and lse are the forward's outputs for q, k, v (same scale and mask).
+    Returns (dQ, dK, dV) like q. `dq` / `dk` / `dv` may be caller-owned
+    outputs; `workspace` an optional uint8 CUDA tensor of at least
+    fa2_bwd_workspace_bytes(B, H, N, D) bytes (allocated per call otherwise).
+    Runs on `stream` (a torch.cuda.Stream) or the current stream.
+    """
+    import torch
+    ts = (q, k, v, o, do)
+    if not all(t.is_cuda for t in ts) or not lse.is_cuda:
+        raise ValueError("q, k, v, o, do and lse must be CUDA tensors")
+    if any(t.shape != q.shape for t in ts) or q.dim() != 4:
+        raise ValueError("q, k, v, o, do must share one [B, H, N, D] shape")
+    if any(t.dtype != q.dtype for t in ts):
+        raise ValueError("q, k, v, o, do must share one dtype")
+    if not all(t.is_contiguous() for t in ts):
+        raise ValueError("q, k, v, o, do must be contiguous")
+    B, H, N, D = q.shape
+    if lse.shape != (B, H, N) or lse.dtype != torch.float32 or not lse.is_contiguous():
+        raise ValueError("lse must be a contiguous float32 [B, H, N] tensor")
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    outs = []
+    for name, t in (("dq", dq), ("dk", dk), ("dv", dv)):
+        if t is None:
+            t = torch.empty_like(q)
+        elif t.shape != q.shape or t.dtype != q.dtype or not t.is_contiguous() or not t.is_cuda:
+            raise ValueError(f"{name} must be a contiguous CUDA tensor like q")
+        outs.append(t)
+    need = fa2_bwd_workspace_bytes(B, H, N, D)
+    if workspace is None:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=q.device)
+    elif not workspace.is_cuda or workspace.numel() * workspace.element_size() < need:
+        raise ValueError(f"workspace must be a CUDA tensor of at least {need} bytes")
+    s = stream if stream is not None else torch.cuda.current_stream(q.device)
+    with torch.cuda.device(q.device):
+        code = fa2_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), do.data_ptr(), lse.data_ptr(),
+                       outs[0].data_ptr(), outs[1].data_ptr(), outs[2].data_ptr(), B, H, N, D, scale,
+                       int(bool(is_causal)), _dtype_code(q), workspace.data_ptr(),
+                       workspace.numel() * workspace.element_size(), s.cuda_stream)
+        _check(code, "fa2_bwd")
+    return tuple(outs)

@@ -78,20 +78,24 @@ EncodeTiledFn encode_fn() {
   return fn;
 }
 
-// [B*H, N, D] view of a [B,H,N,D] tensor; 128 rows x 64 elements per box,
+// [B*H, N, D] view of a [B,H,N,D] tensor; `rows` rows x 64 elements per box,
 // 128-byte swizzle; rows past N read as zeros.
-bool make_map(CUtensorMap* map, const void* ptr, int bh, int n, int d, int dtype) {
+bool make_rows_map(CUtensorMap* map, const void* ptr, int bh, int n, int d, int dtype, unsigned rows) {
   EncodeTiledFn enc = encode_fn();
   if (!enc) return false;
   cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)n, (cuuint64_t)bh};
   cuuint64_t strides[2] = {(cuuint64_t)d * 2, (cuuint64_t)n * d * 2};
-  cuuint32_t box[3] = {64, 128, 1};
+  cuuint32_t box[3] = {64, rows, 1};
   cuuint32_t estride[3] = {1, 1, 1};
   CUresult r = enc(map, dtype == FA2_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3,
                    const_cast<void*>(ptr), dims, strides, box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE,
                    CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
+}
+
+bool make_map(CUtensorMap* map, const void* ptr, int bh, int n, int d, int dtype) {
+  return make_rows_map(map, ptr, bh, n, d, dtype, 128);
 }
 
 bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
@@ -222,6 +226,27 @@ int launch(const void* Q, const void* K, const void* V, void* O, float* LSE, int
 
 namespace fa2 {
 int record_cuda_error(cudaError_t e) { return record_cuda(e); }
+
+int current_device_facts(int* sms, int** status) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return record_cuda(e);
+  DeviceInfo* info = device_info(dev);
+  if (!info) return FA2_ERR_UNSUPPORTED;
+  if (info->err != cudaSuccess) return record_cuda(info->err);
+  if (info->cc_major != 10 || info->cc_minor != 3) return FA2_ERR_UNSUPPORTED;
+  *sms = info->sms;
+  *status = info->status;
+  return FA2_OK;
+}
+
+bool encode_tile_map(CUtensorMap* map, const void* ptr, int bh, int n, int d, int dtype, unsigned rows) {
+  return make_rows_map(map, ptr, bh, n, d, dtype, rows);
+}
+
+unsigned long long watchdog_limit_ns() { return g_watchdog_ns.load(std::memory_order_relaxed); }
+
+bool ranges_overlap(const void* a, size_t na, const void* b, size_t nb) { return overlaps(a, na, b, nb); }
 
 int launch_forward(const void* Q, const void* K, const void* V, void* O, float* LSE, int B, int H, int N, int D,
                    float scale, int is_causal, int dtype, void* workspace, size_t workspace_bytes,

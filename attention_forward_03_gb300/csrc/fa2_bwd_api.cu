@@ -1,0 +1,255 @@
+// C ABI of the backward pass: argument validation, the workspace layout,
+// the two elementwise kernels around the main one (prologue: Delta = rowsum
+// of dO * O, LSE in log2 units, zeroed dQ accumulator; epilogue: dQ =
+// scale * accumulator in the dtype), tensor maps and the persistent launch.
+// Declarations and the contract of every entry point: include/fa2.h.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <math_constants.h>
+
+#include <cmath>
+#include <cstdint>
+
+#include "fa2.h"
+#include "fa2_launch.h"
+
+namespace fa2 {
+namespace {
+
+constexpr int kElemThreads = 256;
+constexpr int kElemBlocksPerSm = 8;
+
+size_t round256(size_t x) { return (x + 255) / 256 * 256; }
+
+struct BwdWorkspace {
+  size_t dq_bytes, stat_bytes, total;
+};
+
+BwdWorkspace workspace_layout(int64_t bh, int N, int D) {
+  const int64_t npad = (static_cast<int64_t>(N) + kBwdRows - 1) / kBwdRows * kBwdRows;
+  BwdWorkspace w;
+  w.dq_bytes = round256(static_cast<size_t>(bh) * N * D * sizeof(float));
+  w.stat_bytes = round256(static_cast<size_t>(bh) * npad * sizeof(float));
+  w.total = w.dq_bytes + 2 * w.stat_bytes;
+  return w;
+}
+
+__device__ __forceinline__ void unpack8(const uint4& u, float (&f)[8], bool bf16) {
+  const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    if (bf16) {
+      const __nv_bfloat162 h = *reinterpret_cast<const __nv_bfloat162*>(&w[i]);
+      f[2 * i] = __low2float(h);
+      f[2 * i + 1] = __high2float(h);
+    } else {
+      const __half2 h = *reinterpret_cast<const __half2*>(&w[i]);
+      f[2 * i] = __low2float(h);
+      f[2 * i + 1] = __high2float(h);
+    }
+  }
+}
+
+__device__ __forceinline__ uint32_t pack_pair(float lo, float hi, bool bf16) {
+  if (bf16) {
+    __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&h);
+  }
+  __half2 h = __floats2half2_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&h);
+}
+
+// Per row (b, h, i) of the padded [B*H, Npad] grid: Delta_i = <dO_i, O_i>
+// and LSE_i * log2(e) (rows >= N: 0 and +inf, so the main kernel's P is 0
+// there), and zeroes the row of the fp32 dQ accumulator. D/8 threads per
+// row, 8 elements (16 bytes) each; the loop bound is a multiple of 32 so that
+// whole warps take part in the row reduction.
+template <int D, bool kBf16>
+__global__ void __launch_bounds__(kElemThreads) fa2_bwd_prologue(const uint4* __restrict__ O,
+                                                                 const uint4* __restrict__ dO,
+                                                                 const float* __restrict__ LSE,
+                                                                 float* __restrict__ dq_acc, float* __restrict__ lse2,
+                                                                 float* __restrict__ delta, int N, int Npad,
+                                                                 long long rows) {
+  constexpr int kPer = D / 8;  // threads per row
+  const long long items = rows * kPer;
+  const long long bound = (items + 31) / 32 * 32;
+  const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
+  for (long long idx = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; idx < bound; idx += stride) {
+    const long long row = idx / kPer;
+    const int part = static_cast<int>(idx % kPer);
+    const bool live = idx < items;
+    const long long bh = live ? row / Npad : 0;
+    const int i = live ? static_cast<int>(row % Npad) : 0;
+    const bool real = live && i < N;
+    float acc = 0.f;
+    if (real) {
+      const long long e = (bh * N + i) * kPer + part;  // in 16-byte units
+      float o[8], g[8];
+      unpack8(O[e], o, kBf16);
+      unpack8(dO[e], g, kBf16);
+#pragma unroll
+      for (int k = 0; k < 8; ++k) acc = fmaf(o[k], g[k], acc);
+      float4* z = reinterpret_cast<float4*>(dq_acc + e * 8);
+      z[0] = make_float4(0.f, 0.f, 0.f, 0.f);
+      z[1] = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+#pragma unroll
+    for (int off = kPer / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off, kPer);
+    if (live && part == 0) {
+      delta[row] = real ? acc : 0.f;
+      lse2[row] = real ? LSE[bh * N + i] * 1.4426950408889634f : CUDART_INF_F;
+    }
+  }
+}
+
+// dQ = dtype(scale * accumulator), 8 elements per thread.
+template <bool kBf16>
+__global__ void __launch_bounds__(kElemThreads) fa2_bwd_dq_convert(const float4* __restrict__ acc,
+                                                                   uint4* __restrict__ dq, float scale,
+                                                                   long long n8) {
+  const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
+  for (long long idx = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; idx < n8; idx += stride) {
+    const float4 a = acc[2 * idx], b = acc[2 * idx + 1];
+    dq[idx] = make_uint4(pack_pair(a.x * scale, a.y * scale, kBf16), pack_pair(a.z * scale, a.w * scale, kBf16),
+                         pack_pair(b.x * scale, b.y * scale, kBf16), pack_pair(b.z * scale, b.w * scale, kBf16));
+  }
+}
+
+using BwdLaunchFn = cudaError_t (*)(const CUtensorMap&, const CUtensorMap&, const CUtensorMap&, const CUtensorMap&,
+                                    const BwdParams&, int, cudaStream_t);
+
+BwdLaunchFn pick_bwd(int d, int dtype, int causal) {
+  const bool bf = dtype == FA2_BF16, c = causal != 0;
+  if (d == 64) {
+    if (bf) return c ? launch_bwd<64, true, true> : launch_bwd<64, true, false>;
+    return c ? launch_bwd<64, false, true> : launch_bwd<64, false, false>;
+  }
+  if (bf) return c ? launch_bwd<128, true, true> : launch_bwd<128, true, false>;
+  return c ? launch_bwd<128, false, true> : launch_bwd<128, false, false>;
+}
+
+template <int D>
+cudaError_t launch_prologue(bool bf16, const void* O, const void* dO, const float* LSE, float* dq_acc, float* lse2,
+                            float* delta, int N, int Npad, long long rows, int grid, cudaStream_t s) {
+  const uint4* o = static_cast<const uint4*>(O);
+  const uint4* g = static_cast<const uint4*>(dO);
+  if (bf16)
+    fa2_bwd_prologue<D, true><<<grid, kElemThreads, 0, s>>>(o, g, LSE, dq_acc, lse2, delta, N, Npad, rows);
+  else
+    fa2_bwd_prologue<D, false><<<grid, kElemThreads, 0, s>>>(o, g, LSE, dq_acc, lse2, delta, N, Npad, rows);
+  return cudaGetLastError();
+}
+
+int grid_for(long long items, int sms) {
+  const long long need = (items + kElemThreads - 1) / kElemThreads;
+  const long long cap = static_cast<long long>(sms) * kElemBlocksPerSm;
+  return static_cast<int>(need < cap ? (need > 0 ? need : 1) : cap);
+}
+
+}  // namespace
+}  // namespace fa2
+
+using namespace fa2;
+
+extern "C" int fa2_bwd_workspace_bytes(int B, int H, int N, int D, size_t* bytes) {
+  if (!bytes || B < 0 || H < 0 || N < 0) return FA2_ERR_INVALID_ARG;
+  if (D != 64 && D != 128) return FA2_ERR_UNSUPPORTED;
+  *bytes = workspace_layout(static_cast<int64_t>(B) * H, N, D).total;
+  return FA2_OK;
+}
+
+extern "C" int fa2_bwd(const void* Q, const void* K, const void* V, const void* O, const void* dO, const float* LSE,
+                       void* dQ, void* dK, void* dV, int B, int H, int N, int D, float scale, int is_causal,
+                       int dtype, void* workspace, size_t workspace_bytes, struct CUstream_st* stream) {
+  if (B < 0 || H < 0 || N < 0) return FA2_ERR_INVALID_ARG;
+  if (D != 64 && D != 128) return FA2_ERR_UNSUPPORTED;
+  if (dtype != FA2_F16 && dtype != FA2_BF16) return FA2_ERR_UNSUPPORTED;
+  if (!std::isfinite(scale) || !(scale > 0.f)) return FA2_ERR_INVALID_ARG;
+  if (B == 0 || H == 0 || N == 0) return FA2_OK;
+  if (!Q || !K || !V || !O || !dO || !LSE || !dQ || !dK || !dV || !workspace) return FA2_ERR_INVALID_ARG;
+  const int64_t bh = static_cast<int64_t>(B) * H;
+  const int64_t nkv = (static_cast<int64_t>(N) + kBwdKeys - 1) / kBwdKeys;
+  if (bh > INT32_MAX || bh * nkv > INT32_MAX) return FA2_ERR_INVALID_ARG;
+  const uintptr_t mis = reinterpret_cast<uintptr_t>(Q) | reinterpret_cast<uintptr_t>(K) |
+                        reinterpret_cast<uintptr_t>(V) | reinterpret_cast<uintptr_t>(O) |
+                        reinterpret_cast<uintptr_t>(dO) | reinterpret_cast<uintptr_t>(LSE) |
+                        reinterpret_cast<uintptr_t>(dQ) | reinterpret_cast<uintptr_t>(dK) |
+                        reinterpret_cast<uintptr_t>(dV);
+  if (mis & 15u) return FA2_ERR_ALIGN;
+  if (reinterpret_cast<uintptr_t>(workspace) & 255u) return FA2_ERR_ALIGN;
+  const BwdWorkspace wl = workspace_layout(bh, N, D);
+  if (workspace_bytes < wl.total) return FA2_ERR_INVALID_ARG;
+  const size_t tb = static_cast<size_t>(bh) * N * D * 2;
+  const size_t lb = static_cast<size_t>(bh) * N * 4;
+  const void* ins[6] = {Q, K, V, O, dO, LSE};
+  const size_t in_bytes[6] = {tb, tb, tb, tb, tb, lb};
+  const void* outs[4] = {dQ, dK, dV, workspace};
+  const size_t out_bytes[4] = {tb, tb, tb, workspace_bytes};
+  for (int a = 0; a < 4; ++a) {
+    for (int b = 0; b < 6; ++b)
+      if (ranges_overlap(outs[a], out_bytes[a], ins[b], in_bytes[b])) return FA2_ERR_INVALID_ARG;
+    for (int b = a + 1; b < 4; ++b)
+      if (ranges_overlap(outs[a], out_bytes[a], outs[b], out_bytes[b])) return FA2_ERR_INVALID_ARG;
+  }
+
+  int sms = 0;
+  int* status = nullptr;
+  const int rc = current_device_facts(&sms, &status);
+  if (rc != FA2_OK) return rc;
+
+  CUtensorMap mk, mv, mq, mdo;
+  if (!encode_tile_map(&mk, K, (int)bh, N, D, dtype, kBwdKeys) ||
+      !encode_tile_map(&mv, V, (int)bh, N, D, dtype, kBwdKeys) ||
+      !encode_tile_map(&mq, Q, (int)bh, N, D, dtype, kBwdRows) ||
+      !encode_tile_map(&mdo, dO, (int)bh, N, D, dtype, kBwdRows))
+    return record_cuda_error(cudaErrorInvalidValue);
+
+  const int npad = (N + kBwdRows - 1) / kBwdRows * kBwdRows;
+  char* ws = static_cast<char*>(workspace);
+  float* dq_acc = reinterpret_cast<float*>(ws);
+  float* lse2 = reinterpret_cast<float*>(ws + wl.dq_bytes);
+  float* delta = reinterpret_cast<float*>(ws + wl.dq_bytes + wl.stat_bytes);
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const bool bf = dtype == FA2_BF16;
+
+  const long long rows = bh * npad;
+  const int pgrid = grid_for(rows * (D / 8), sms);
+  cudaError_t e = D == 64 ? launch_prologue<64>(bf, O, dO, LSE, dq_acc, lse2, delta, N, npad, rows, pgrid, s)
+                          : launch_prologue<128>(bf, O, dO, LSE, dq_acc, lse2, delta, N, npad, rows, pgrid, s);
+  if (e != cudaSuccess) return record_cuda_error(e);
+
+  BwdParams p = {};
+  p.dk = dK;
+  p.dv = dV;
+  p.dq_acc = dq_acc;
+  p.lse2 = lse2;
+  p.delta = delta;
+  p.status = status;
+  p.watchdog_ns = watchdog_limit_ns();
+  p.N = N;
+  p.Npad = npad;
+  p.BH = (int)bh;
+  p.nkv = (int)nkv;
+  p.nq = npad / kBwdRows;
+  p.num_units = (int)(bh * nkv);
+  p.scale_log2 = scale * 1.4426950408889634f;
+  p.scale = scale;
+  const int grid = p.num_units < sms ? p.num_units : sms;
+  e = pick_bwd(D, dtype, is_causal)(mk, mv, mq, mdo, p, grid, s);
+  if (e != cudaSuccess) return record_cuda_error(e);
+
+  const long long n8 = bh * N * (D / 8);
+  const int cgrid = grid_for(n8, sms);
+  if (bf)
+    fa2_bwd_dq_convert<true><<<cgrid, kElemThreads, 0, s>>>(reinterpret_cast<const float4*>(dq_acc),
+                                                             static_cast<uint4*>(dQ), scale, n8);
+  else
+    fa2_bwd_dq_convert<false><<<cgrid, kElemThreads, 0, s>>>(reinterpret_cast<const float4*>(dq_acc),
+                                                              static_cast<uint4*>(dQ), scale, n8);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return record_cuda_error(e);
+  return FA2_OK;
+}

@@ -1,0 +1,567 @@
+// FlashAttention-2 backward for GB300 (sm_103a): persistent, warp-specialised,
+// TMA-fed, tcgen05 tensor cores accumulating in tensor memory (TMEM).
+//
+// What it computes is the gradient of the forward pass for an upstream
+// gradient dO, the way the yangyitao.com CUDA book, ch. 15, describes the
+// FlashAttention-2 backward: only LSE = m + log l is kept from the forward
+// (section 15.1, change 4) and S and P are recomputed from it; the outer loop
+// runs over K/V tiles and the inner loop over query tiles, and dQ is
+// accumulated across K/V tiles with atomic adds (the chapter's closing
+// paragraph). Per K/V tile (128 keys) and query step i (64 rows):
+//
+//   S^T  = K Q_i^T            P^T  = 2^(S^T * scale*log2(e) - LSE_i*log2(e))
+//   dP^T = V dO_i^T           dS^T = P^T * (dP^T - Delta_i),  Delta_i = <dO_i, O_i>
+//   dV  += P^T dO_i           dK  += dS^T Q_i        (in TMEM for the whole tile)
+//   dQ_i^T = K^T dS^T         added into an fp32 dQ accumulator in global memory
+//
+// and at the end of the tile dK *= scale; dQ = scale * accumulator is
+// converted to the dtype by a separate elementwise kernel.
+//
+// Layout of one CTA (one per SM, persistent over work units = K/V tiles):
+//   warps 0-7  two compute warpgroups; thread = key row = TMEM lane, warpgroup
+//              g takes query columns [32g, 32g+32) of every step (and the
+//              halves [gD/2, (g+1)D/2) of the dK / dV rows in the epilogue)
+//   warp  8    tcgen05 MMA issuer (one thread), owns the TMEM allocation
+//   warp  9    TMA producer (one thread)
+// Tensor memory (fp32 columns x 128 lanes):
+//   [0, D)          dV accumulator        [D, 2D)        dK accumulator
+//   [2D, 2D+64)     S^T of the step       [2D+64, 2D+128) dP^T of the step
+//   [2D+128, 2D+192) dQ^T of the step (lane = head-dim index; at D = 64 the
+//                   MMA runs with M = 128 and lanes 64-127 are discarded)
+// Shared memory (128-byte swizzled, 64-element panels): K and V of the tile
+// (resident for the unit), a ring of query steps (Q_i, dO_i, and the 64
+// LSE*log2(e) and Delta values), and the 16-bit P^T and dS^T of the step
+// (written by the compute threads, read by the tensor core).
+//
+// Pipelining: the issuer computes S^T, dP^T of step i+1 as soon as the
+// compute threads have loaded those of step i into registers, so the tensor
+// core works on step i+1 while P^T and dS^T of step i are formed; the
+// compute threads read dQ^T of step i-1 after publishing step i.
+#pragma once
+#include "fa2_kernel.cuh"
+
+namespace fa2 {
+
+constexpr int kBwdThreads = 320;    // 10 warps
+constexpr int kBwdMmaWarp = 8;
+constexpr int kBwdLoadWarp = 9;
+constexpr int kBwdComputeThreads = 256;
+constexpr int kBwdQPanelBytes = kBwdRows * 128;   // 64 rows x 64 16-bit elements
+constexpr int kBwdPTileBytes = kBwdKeys * 128;    // 128 keys x 64 query columns (16-bit)
+constexpr int kBwdStatBytes = 2 * kBwdRows * 4;   // LSE*log2(e) and Delta of one step
+
+enum : int {
+  kSiteBwdKvEmpty = 21,
+  kSiteBwdStageEmpty = 22,
+  kSiteBwdKvFull = 23,
+  kSiteBwdStageFull = 24,
+  kSiteBwdSFree = 25,
+  kSiteBwdPFull = 26,
+  kSiteBwdAccFree = 27,
+  kSiteBwdDqFree = 28,
+  kSiteBwdSFull = 29,
+  kSiteBwdPFree = 30,
+  kSiteBwdDqFull = 31,
+  kSiteBwdAccFull = 32,
+  kSiteBwdDrain = 33,
+};
+
+template <int D>
+struct BwdLayout {
+  static constexpr int kPanels = D / 64;
+  static constexpr int kKVBytes = kPanels * kPanelBytes;      // K or V tile: 128 rows x D
+  static constexpr int kQBytes = kPanels * kBwdQPanelBytes;   // Q or dO step: 64 rows x D
+  static constexpr int kStages = (D == 128) ? 3 : 6;
+  static constexpr int kStageBytes = 2 * kQBytes;             // Q then dO
+  static constexpr int kK = 0;
+  static constexpr int kV = kKVBytes;
+  static constexpr int kRing = 2 * kKVBytes;
+  static constexpr int kP = kRing + kStages * kStageBytes;
+  static constexpr int kDS = kP + kBwdPTileBytes;
+  static constexpr int kStats = kDS + kBwdPTileBytes;
+  static constexpr int kBars = kStats + kStages * kBwdStatBytes;
+  // kv_full, kv_empty, stage_full[S], stage_empty[S], s_full, s_free, p_full,
+  // p_free, dq_full, dq_free, acc_full, acc_free, drain
+  static constexpr int kNumBars = 2 + 2 * kStages + 9;
+  static constexpr int kMisc = kBars + kNumBars * 8;
+  static constexpr int kSmemBytes = kMisc + 16 + 1024;  // + slack for 1 KB alignment
+  static constexpr uint32_t kColDV = 0;
+  static constexpr uint32_t kColDK = D;
+  static constexpr uint32_t kColS = 2 * D;
+  static constexpr uint32_t kColDP = 2 * D + kBwdRows;
+  static constexpr uint32_t kColDQ = 2 * D + 2 * kBwdRows;
+  static_assert(kColDQ + kBwdRows <= kTmemCols, "TMEM budget");
+  static_assert(kSmemBytes <= 232448, "shared memory budget");
+  static_assert(kRing % 1024 == 0 && kP % 1024 == 0 && kDS % 1024 == 0, "swizzled tiles need 1 KB alignment");
+};
+
+// Work unit u -> (head, K/V tile). Non-causal: the tiles of a head are
+// consecutive (its Q and dO stay hot in L2). Causal: the tiles with the most
+// query steps (lowest index) first, over all heads.
+template <bool kCausal>
+__device__ __forceinline__ void bwd_unit(int u, const BwdParams& p, int& bh, int& kv) {
+  if (kCausal) {
+    kv = u / p.BH;
+    bh = u % p.BH;
+  } else {
+    bh = u / p.nkv;
+    kv = u % p.nkv;
+  }
+}
+
+// Query steps [first, nq) that see keys of tile kv.
+template <bool kCausal>
+__device__ __forceinline__ int bwd_first_step(int kv) {
+  return kCausal ? kv * (kBwdKeys / kBwdRows) : 0;
+}
+
+// Unit of this CTA in round r (zig-zag when causal, as in the forward).
+template <bool kCausal>
+__device__ __forceinline__ int bwd_round_unit(int r) {
+  const int g = gridDim.x, b = blockIdx.x;
+  return r * g + ((kCausal && (r & 1)) ? (g - 1 - b) : b);
+}
+
+template <int D, bool kBf16, bool kCausal>
+__global__ void __launch_bounds__(kBwdThreads, 1)
+    fa2_bwd_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
+                   const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmDO,
+                   const BwdParams p) {
+  using L = BwdLayout<D>;
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  const uint32_t raw = smem_addr(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t* smem = smem_raw + (base - raw);
+
+  const uint32_t sK = base + L::kK;
+  const uint32_t sV = base + L::kV;
+  const uint32_t sRing = base + L::kRing;
+  const uint32_t sP = base + L::kP;
+  const uint32_t sDS = base + L::kDS;
+  const uint32_t sStats = base + L::kStats;
+  const float* stats = reinterpret_cast<const float*>(smem + L::kStats);
+  const uint32_t bars = base + L::kBars;
+  const uint32_t bar_kv_full = bars;
+  const uint32_t bar_kv_empty = bars + 8;
+  auto bar_stage_full = [&](int s) { return bars + 16 + 8u * s; };
+  auto bar_stage_empty = [&](int s) { return bars + 16 + 8u * (L::kStages + s); };
+  const uint32_t bar_s_full = bars + 16 + 16u * L::kStages;  // S^T, dP^T of a step in TMEM
+  const uint32_t bar_s_free = bar_s_full + 8;                 // ... loaded by the compute threads
+  const uint32_t bar_p_full = bar_s_full + 16;                // P^T, dS^T of a step in shared memory
+  const uint32_t bar_p_free = bar_s_full + 24;                // ... read by the tensor core
+  const uint32_t bar_dq_full = bar_s_full + 32;               // dQ^T of a step in TMEM
+  const uint32_t bar_dq_free = bar_s_full + 40;               // ... loaded by the compute threads
+  const uint32_t bar_acc_full = bar_s_full + 48;              // dV, dK of a unit complete
+  const uint32_t bar_acc_free = bar_s_full + 56;              // ... loaded by the compute threads
+  const uint32_t bar_drain = bar_s_full + 64;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kMisc);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kMisc + 4);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    mbar_init(bar_kv_full, 1);
+    mbar_init(bar_kv_empty, 1);
+    for (int s = 0; s < L::kStages; ++s) {
+      mbar_init(bar_stage_full(s), 1);
+      mbar_init(bar_stage_empty(s), 1);
+    }
+    mbar_init(bar_s_full, 1);
+    mbar_init(bar_s_free, kBwdComputeThreads);
+    mbar_init(bar_p_full, kBwdComputeThreads);
+    mbar_init(bar_p_free, 1);
+    mbar_init(bar_dq_full, 1);
+    mbar_init(bar_dq_free, kBwdComputeThreads);
+    mbar_init(bar_acc_full, 1);
+    mbar_init(bar_acc_free, kBwdComputeThreads);
+    mbar_init(bar_drain, 1);
+    *abort_flag = 0;
+    mbar_init_fence();
+  }
+  if (warp == kBwdMmaWarp) {
+    tmem_alloc(smem_addr(tmem_slot), kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+  const uint32_t tmem = *tmem_slot;
+
+  Watchdog wd;
+  wd.status = p.status;
+  wd.abort_flag = abort_flag;
+  wd.limit_ns = p.watchdog_ns;
+
+  if (warp == kBwdLoadWarp) {
+    // ------------------------------------------------------------ producer
+    // Per unit: K and V of the tile once, then every query step (Q_i, dO_i
+    // and their 64 LSE*log2(e) / Delta values) through the ring.
+    if (lane == 0) {
+      tma_prefetch_map(&tmK);
+      tma_prefetch_map(&tmV);
+      tma_prefetch_map(&tmQ);
+      tma_prefetch_map(&tmDO);
+      const uint64_t once = l2_policy_evict_first();  // K, V: read by one unit
+      const uint64_t keep = l2_policy_evict_last();   // Q, dO: read by every K/V tile of the head
+      int slot = 0;
+      uint32_t ph = 0, units = 0, loads = 0;
+      bool ok = true;
+      for (int r = 0; ok; ++r) {
+        const int u = bwd_round_unit<kCausal>(r);
+        if (u >= p.num_units) break;
+        int bh, kv;
+        bwd_unit<kCausal>(u, p, bh, kv);
+        if (units > 0 && !wait_bounded(bar_kv_empty, (units - 1) & 1u, wd, kSiteBwdKvEmpty, true, kNapNs)) {
+          ok = false;
+          break;
+        }
+        mbar_arrive_expect_tx(bar_kv_full, 2 * L::kKVBytes);
+        for (int pn = 0; pn < L::kPanels; ++pn) {
+          tma_load_3d_hint(sK + pn * kPanelBytes, &tmK, bar_kv_full, pn * 64, kv * kBwdKeys, bh, once);
+          tma_load_3d_hint(sV + pn * kPanelBytes, &tmV, bar_kv_full, pn * 64, kv * kBwdKeys, bh, once);
+        }
+        ++units;
+        for (int i = bwd_first_step<kCausal>(kv); i < p.nq; ++i) {
+          if (!wait_bounded(bar_stage_empty(slot), ph ^ 1u, wd, kSiteBwdStageEmpty, true, kNapNs)) {
+            ok = false;
+            break;
+          }
+          const uint32_t full = bar_stage_full(slot);
+          const uint32_t st = sRing + static_cast<uint32_t>(slot * L::kStageBytes);
+          mbar_arrive_expect_tx(full, L::kStageBytes + kBwdStatBytes);
+          for (int pn = 0; pn < L::kPanels; ++pn) {
+            tma_load_3d_hint(st + pn * kBwdQPanelBytes, &tmQ, full, pn * 64, i * kBwdRows, bh, keep);
+            tma_load_3d_hint(st + L::kQBytes + pn * kBwdQPanelBytes, &tmDO, full, pn * 64, i * kBwdRows, bh, keep);
+          }
+          const size_t off = static_cast<size_t>(bh) * p.Npad + static_cast<size_t>(i) * kBwdRows;
+          const uint32_t sst = sStats + static_cast<uint32_t>(slot * kBwdStatBytes);
+          bulk_load(sst, p.lse2 + off, kBwdRows * 4, full);
+          bulk_load(sst + kBwdRows * 4, p.delta + off, kBwdRows * 4, full);
+          ++loads;
+          if (++slot == L::kStages) {
+            slot = 0;
+            ph ^= 1u;
+          }
+        }
+      }
+      // Drain: every copy issued must have landed before the CTA may exit.
+      const uint32_t first = loads > static_cast<uint32_t>(L::kStages) ? loads - L::kStages : 0u;
+      for (uint32_t x = first; x < loads; ++x)
+        wait_bounded(bar_stage_full(static_cast<int>(x % L::kStages)), (x / L::kStages) & 1u, wd, kSiteBwdDrain,
+                     false, kNapNs);
+      if (units > 0) wait_bounded(bar_kv_full, (units - 1) & 1u, wd, kSiteBwdDrain, false, kNapNs);
+    }
+    __syncwarp();
+  } else if (warp == kBwdMmaWarp) {
+    // ---------------------------------------------------------- MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idesc_s = make_idesc_f16(kBf16, kBwdRows, false);            // S^T, dP^T: N = 64
+      constexpr uint32_t idesc_acc = make_idesc_f16(kBf16, D, true);                  // dV, dK: N = D
+      constexpr uint32_t idesc_dq = make_idesc_f16_ab(kBf16, kBwdRows, true, true);   // dQ^T: N = 64
+      constexpr uint32_t kHi = desc_hi_sw128(1024);  // 8-row (K-major) / 8-row-of-K (MN-major) groups 1 KB apart
+      // S^T = K Q_i^T and dP^T = V dO_i^T: A = K / V (K-major, 128-row
+      // panels), B = Q_i / dO_i (K-major, 64-row panels), D/16 steps.
+      auto issue_sdp = [&](int slot) {
+        const uint32_t st = sRing + static_cast<uint32_t>(slot * L::kStageBytes);
+        const uint32_t k_lo = desc_lo_sw128(sK, 16), v_lo = desc_lo_sw128(sV, 16);
+        const uint32_t q_lo = desc_lo_sw128(st, 16), do_lo = desc_lo_sw128(st + L::kQBytes, 16);
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t a = static_cast<uint32_t>(((kk >> 2) * kPanelBytes + (kk & 3) * 32) >> 4);
+          const uint32_t b = static_cast<uint32_t>(((kk >> 2) * kBwdQPanelBytes + (kk & 3) * 32) >> 4);
+          mma_ss_w(tmem + L::kColS, k_lo + a, kHi, q_lo + b, kHi, idesc_s, kk > 0 ? 1u : 0u);
+        }
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t a = static_cast<uint32_t>(((kk >> 2) * kPanelBytes + (kk & 3) * 32) >> 4);
+          const uint32_t b = static_cast<uint32_t>(((kk >> 2) * kBwdQPanelBytes + (kk & 3) * 32) >> 4);
+          mma_ss_w(tmem + L::kColDP, v_lo + a, kHi, do_lo + b, kHi, idesc_s, kk > 0 ? 1u : 0u);
+        }
+      };
+      // dV += P^T dO_i and dK += dS^T Q_i: A = P^T / dS^T (K-major, one
+      // panel of 64 query columns), B = dO_i / Q_i (MN-major: rows are the
+      // contraction index, 64-column panels 8 KB apart), 4 steps of 16 rows.
+      auto issue_grads = [&](int slot, bool acc) {
+        const uint32_t st = sRing + static_cast<uint32_t>(slot * L::kStageBytes);
+        const uint32_t p_lo = desc_lo_sw128(sP, 16), ds_lo = desc_lo_sw128(sDS, 16);
+        const uint32_t q_mn = desc_lo_sw128(st, kBwdQPanelBytes);
+        const uint32_t do_mn = desc_lo_sw128(st + L::kQBytes, kBwdQPanelBytes);
+#pragma unroll
+        for (int kk = 0; kk < kBwdRows / 16; ++kk) {
+          const uint32_t a = static_cast<uint32_t>((kk * 32) >> 4);
+          const uint32_t b = static_cast<uint32_t>((kk * 16 * 128) >> 4);
+          mma_ss_w(tmem + L::kColDV, p_lo + a, kHi, do_mn + b, kHi, idesc_acc, (acc || kk > 0) ? 1u : 0u);
+        }
+#pragma unroll
+        for (int kk = 0; kk < kBwdRows / 16; ++kk) {
+          const uint32_t a = static_cast<uint32_t>((kk * 32) >> 4);
+          const uint32_t b = static_cast<uint32_t>((kk * 16 * 128) >> 4);
+          mma_ss_w(tmem + L::kColDK, ds_lo + a, kHi, q_mn + b, kHi, idesc_acc, (acc || kk > 0) ? 1u : 0u);
+        }
+      };
+      // dQ_i^T = K^T dS^T: A = K read MN-major (M = head-dim index, two
+      // 64-row M panels 16 KB apart; at D = 64 the second panel is the V
+      // tile and its rows are discarded), B = dS^T MN-major (N = 64 query
+      // columns, one panel), 8 steps of 16 keys.
+      auto issue_dq = [&]() {
+        const uint32_t kt_lo = desc_lo_sw128(sK, kPanelBytes);
+        const uint32_t ds_mn = desc_lo_sw128(sDS, kBwdPTileBytes);
+#pragma unroll
+        for (int kk = 0; kk < kBwdKeys / 16; ++kk) {
+          const uint32_t off = static_cast<uint32_t>((kk * 16 * 128) >> 4);
+          mma_ss_w(tmem + L::kColDQ, kt_lo + off, kHi, ds_mn + off, kHi, idesc_dq, kk > 0 ? 1u : 0u);
+        }
+      };
+
+      int slot = 0;
+      uint32_t ph = 0;
+      uint32_t g = 0;      // global query-step counter of this CTA
+      uint32_t units = 0;
+      bool ok = true;
+      // Takes the next ring slot (Q_i, dO_i loaded) and, once the compute
+      // threads hold the previous step's S^T / dP^T, issues this step's.
+      auto start_step = [&](uint32_t step) -> int {
+        const int s = slot;
+        if (!wait_bounded(bar_stage_full(s), ph, wd, kSiteBwdStageFull, true, kNapNs)) return -1;
+        if (step > 0 && !wait_bounded(bar_s_free, (step - 1) & 1u, wd, kSiteBwdSFree, true, kNapNs)) return -1;
+        tc_fence_after_sync();
+        issue_sdp(s);
+        mma_commit(bar_s_full);
+        if (++slot == L::kStages) {
+          slot = 0;
+          ph ^= 1u;
+        }
+        return s;
+      };
+      for (int r = 0; ok; ++r) {
+        const int u = bwd_round_unit<kCausal>(r);
+        if (u >= p.num_units) break;
+        int bh, kv;
+        bwd_unit<kCausal>(u, p, bh, kv);
+        const int n_steps = p.nq - bwd_first_step<kCausal>(kv);
+        if (!wait_bounded(bar_kv_full, units & 1u, wd, kSiteBwdKvFull, true, kNapNs)) {
+          ok = false;
+          break;
+        }
+        int cur = start_step(g);
+        if (cur < 0) {
+          ok = false;
+          break;
+        }
+        for (int t = 0; t < n_steps; ++t, ++g) {
+          // the next step's scores first: the tensor core computes them
+          // while the compute threads form P^T and dS^T of this one
+          int nxt = -1;
+          if (t + 1 < n_steps) {
+            nxt = start_step(g + 1);
+            if (nxt < 0) {
+              ok = false;
+              break;
+            }
+          }
+          if (!wait_bounded(bar_p_full, g & 1u, wd, kSiteBwdPFull, true, kNapNs)) {
+            ok = false;
+            break;
+          }
+          // the unit's first accumulation overwrites dV / dK: the previous
+          // unit's epilogue must have loaded them
+          if (t == 0 && units > 0 && !wait_bounded(bar_acc_free, (units - 1) & 1u, wd, kSiteBwdAccFree, true, kNapNs)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after_sync();
+          issue_grads(cur, t > 0);
+          mma_commit(bar_stage_empty(cur));
+          if (g > 0 && !wait_bounded(bar_dq_free, (g - 1) & 1u, wd, kSiteBwdDqFree, true, kNapNs)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after_sync();
+          issue_dq();
+          mma_commit(bar_p_free);
+          mma_commit(bar_dq_full);
+          cur = nxt;
+        }
+        if (!ok) break;
+        mma_commit(bar_acc_full);
+        mma_commit(bar_kv_empty);
+        ++units;
+      }
+      // Drain: the CTA must not exit (or free TMEM) with MMAs in flight.
+      mma_commit(bar_drain);
+      wait_bounded(bar_drain, 0u, wd, kSiteBwdDrain, false, kNapNs);
+    }
+    __syncwarp();
+  } else if (warp < 8) {
+    // ------------------------------------------------------- compute warps
+    const int wg = warp >> 2;                 // query-column half of every step
+    const int quarter = warp & 3;             // TMEM lane quarter this warp may access
+    const int rr = quarter * 32 + lane;       // key row within the tile = TMEM lane
+    const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
+    const uint32_t tS = tmem + lane_off + L::kColS + 32u * wg;
+    const uint32_t tDP = tmem + lane_off + L::kColDP + 32u * wg;
+    const uint32_t tDQ = tmem + lane_off + L::kColDQ + 32u * wg;
+    const uint32_t p_row = sP + static_cast<uint32_t>(rr * 128);
+    const uint32_t ds_row = sDS + static_cast<uint32_t>(rr * 128);
+    const uint32_t xr = static_cast<uint32_t>(rr & 7);
+    const bool dq_rows = quarter * 32 < D;    // warp-uniform: lanes >= D of dQ^T are discarded
+    const float c = p.scale_log2;
+    uint32_t g = 0, units = 0, ph = 0;
+    int slot = 0;
+    bool ok = true;
+    int pend_bh = 0, pend_q0 = 0;  // head and first row of the step whose dQ^T is pending
+
+    // dQ^T of global step `step` (head pend_bh, rows pend_q0 + [32wg, 32wg+32))
+    // from TMEM into the fp32 accumulator: this thread holds head-dim index
+    // rr of 32 query rows; the 32 lanes of a warp add 32 consecutive floats.
+    auto drain_dq = [&](uint32_t step) -> bool {
+      bool got = wait_bounded(bar_dq_full, step & 1u, wd, kSiteBwdDqFull);
+      got = __all_sync(0xffffffffu, got);
+      if (!got) return false;
+      tc_fence_after_sync();
+      uint32_t v[32];
+      if (dq_rows) tmem_ld32x32_wait(tDQ, v);
+      tc_fence_before_sync();
+      mbar_arrive(bar_dq_free);
+      if (dq_rows) {
+        const int q0 = pend_q0 + 32 * wg;
+        const int rows = min(32, p.N - q0);
+        float* dst = p.dq_acc + (static_cast<size_t>(pend_bh) * p.N + q0) * D + rr;
+#pragma unroll
+        for (int i = 0; i < 32; ++i)
+          if (i < rows) atomicAdd(dst + static_cast<size_t>(i) * D, __uint_as_float(v[i]));
+      }
+      return true;
+    };
+
+    for (int r = 0; ok; ++r) {
+      const int u = bwd_round_unit<kCausal>(r);
+      if (u >= p.num_units) break;
+      int bh, kv;
+      bwd_unit<kCausal>(u, p, bh, kv);
+      const int key = kv * kBwdKeys + rr;
+      const bool key_ok = key < p.N;
+      for (int i = bwd_first_step<kCausal>(kv); i < p.nq; ++i, ++g) {
+        bool got = wait_bounded(bar_s_full, g & 1u, wd, kSiteBwdSFull);
+        got = got && wait_bounded(bar_stage_full(slot), ph, wd, kSiteBwdStageFull);
+        got = __all_sync(0xffffffffu, got);
+        if (!got) {
+          ok = false;
+          break;
+        }
+        tc_fence_after_sync();
+        uint32_t sr[32], dpr[32];
+        tmem_ld32x32_wait(tS, sr);
+        tmem_ld32x32_wait(tDP, dpr);
+        // S^T and dP^T are in registers: the issuer may compute the next ones.
+        tc_fence_before_sync();
+        mbar_arrive(bar_s_free);
+        const float* lse2 = stats + slot * (kBwdStatBytes / 4) + 32 * wg;
+        const float* delta = lse2 + kBwdRows;
+        const int q0 = i * kBwdRows + 32 * wg;  // query row of this thread's first column
+        // masked: keys past N (ragged last tile) and, causal, keys after the query
+        const bool masked = !key_ok || (kCausal && key > q0);
+        uint32_t pk[16], dk[16];
+#pragma unroll
+        for (int j = 0; j < 32; j += 2) {
+          float p0 = ex2_approx(__uint_as_float(sr[j]) * c - lse2[j]);
+          float p1 = ex2_approx(__uint_as_float(sr[j + 1]) * c - lse2[j + 1]);
+          if (masked) {
+            if (!key_ok || key > q0 + j) p0 = 0.f;
+            if (!key_ok || key > q0 + j + 1) p1 = 0.f;
+          }
+          const float d0 = p0 * (__uint_as_float(dpr[j]) - delta[j]);
+          const float d1 = p1 * (__uint_as_float(dpr[j + 1]) - delta[j + 1]);
+          pk[j / 2] = pack2(p0, p1, kBf16);
+          dk[j / 2] = pack2(d0, d1, kBf16);
+        }
+        // the previous step's P^T / dS^T must have been read by the tensor core
+        if (g > 0) {
+          bool fr = wait_bounded(bar_p_free, (g - 1) & 1u, wd, kSiteBwdPFree);
+          fr = __all_sync(0xffffffffu, fr);
+          if (!fr) {
+            ok = false;
+            break;
+          }
+        }
+        // 4 chunks of 8 query columns into the 128-byte-swizzled key row
+#pragma unroll
+        for (int ch = 0; ch < 4; ++ch) {
+          const uint32_t col = ((static_cast<uint32_t>(4 * wg + ch) ^ xr) << 4);
+          st_shared_v4(p_row + col, pk[4 * ch], pk[4 * ch + 1], pk[4 * ch + 2], pk[4 * ch + 3]);
+          st_shared_v4(ds_row + col, dk[4 * ch], dk[4 * ch + 1], dk[4 * ch + 2], dk[4 * ch + 3]);
+        }
+        fence_proxy_async_shared();
+        tc_fence_before_sync();
+        mbar_arrive(bar_p_full);
+        if (g > 0 && !drain_dq(g - 1)) {
+          ok = false;
+          break;
+        }
+        pend_bh = bh;
+        pend_q0 = i * kBwdRows;
+        if (++slot == L::kStages) {
+          slot = 0;
+          ph ^= 1u;
+        }
+      }
+      if (!ok) break;
+      // Epilogue: this thread's key row of dV and dK (half of the columns).
+      bool got = wait_bounded(bar_acc_full, units & 1u, wd, kSiteBwdAccFull);
+      got = __all_sync(0xffffffffu, got);
+      if (!got) {
+        ok = false;
+        break;
+      }
+      tc_fence_after_sync();
+      constexpr int kHalf = D / 2;
+      uint32_t dv[kHalf], dkr[kHalf];
+#pragma unroll
+      for (int cc = 0; cc < kHalf; cc += 32) {
+        tmem_ld32x32_wait(tmem + lane_off + L::kColDV + wg * kHalf + cc, *reinterpret_cast<uint32_t(*)[32]>(dv + cc));
+        tmem_ld32x32_wait(tmem + lane_off + L::kColDK + wg * kHalf + cc, *reinterpret_cast<uint32_t(*)[32]>(dkr + cc));
+      }
+      tc_fence_before_sync();
+      mbar_arrive(bar_acc_free);
+      if (key_ok) {
+        const size_t off = (static_cast<size_t>(bh) * p.N + key) * (D * 2) + wg * kHalf * 2;
+        uint4* dvp = reinterpret_cast<uint4*>(reinterpret_cast<uint8_t*>(p.dv) + off);
+        uint4* dkp = reinterpret_cast<uint4*>(reinterpret_cast<uint8_t*>(p.dk) + off);
+#pragma unroll
+        for (int q = 0; q < kHalf / 8; ++q) {
+          const float* a = reinterpret_cast<const float*>(dv + 8 * q);
+          const float* b = reinterpret_cast<const float*>(dkr + 8 * q);
+          dvp[q] = make_uint4(pack2(a[0], a[1], kBf16), pack2(a[2], a[3], kBf16), pack2(a[4], a[5], kBf16),
+                              pack2(a[6], a[7], kBf16));
+          const float s = p.scale;
+          dkp[q] = make_uint4(pack2(b[0] * s, b[1] * s, kBf16), pack2(b[2] * s, b[3] * s, kBf16),
+                              pack2(b[4] * s, b[5] * s, kBf16), pack2(b[6] * s, b[7] * s, kBf16));
+        }
+      }
+      ++units;
+    }
+    // the last step's dQ^T
+    if (ok && g > 0) drain_dq(g - 1);
+  }
+
+  tc_fence_before_sync();
+  __syncthreads();
+  if (warp == kBwdMmaWarp) {
+    tc_fence_after_sync();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+template <int D, bool kBf16, bool kCausal>
+cudaError_t launch_bwd(const CUtensorMap& k, const CUtensorMap& v, const CUtensorMap& q, const CUtensorMap& dout,
+                       const BwdParams& p, int grid, cudaStream_t stream) {
+  auto kern = fa2_bwd_kernel<D, kBf16, kCausal>;
+  const int smem = BwdLayout<D>::kSmemBytes;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e != cudaSuccess) return e;
+  kern<<<grid, kBwdThreads, smem, stream>>>(k, v, q, dout, p);
+  return cudaGetLastError();
+}
+
+}  // namespace fa2

@@ -1,6 +1,6 @@
-// Host-visible pieces of the forward kernel: tile constants, the parameter
-// block, and the launcher template (instantiated in fa2_fwd_d64.cu and
-// fa2_fwd_d128.cu).
+// Host-visible pieces of the forward and backward kernels: tile constants,
+// the parameter blocks, and the launcher templates (instantiated in
+// fa2_fwd_d64.cu, fa2_fwd_d128.cu, fa2_bwd_d64.cu and fa2_bwd_d128.cu).
 #pragma once
 #include <cuda.h>
 #include <cuda_runtime.h>
@@ -37,6 +37,27 @@ struct Params {
   int test_withhold;        // test hook: the producer withholds its first K/V tile
 };
 
+constexpr int kBwdKeys = 128;       // keys per backward work unit (= TMEM lanes)
+constexpr int kBwdRows = 64;        // query rows per backward step
+
+struct BwdParams {
+  void* dk;                 // [B,H,N,D] 16-bit outputs
+  void* dv;
+  float* dq_acc;            // [B,H,N,D] fp32 dQ accumulator (zeroed by the prologue kernel)
+  const float* lse2;        // [B*H, Npad] LSE * log2(e); +inf for rows >= N
+  const float* delta;       // [B*H, Npad] <dO_i, O_i>; 0 for rows >= N
+  int* status;              // device watchdog word
+  unsigned long long watchdog_ns;
+  int N;
+  int Npad;                 // N rounded up to a multiple of kBwdRows
+  int BH;
+  int nkv;                  // K/V tiles (work units) per head = ceil(N / 128)
+  int nq;                   // query steps per head = ceil(N / 64)
+  int num_units;            // BH * nkv
+  float scale_log2;         // scale * log2(e)
+  float scale;
+};
+
 // Bytes of stream-K workspace for `grid` CTAs at head dimension d.
 constexpr size_t stream_k_workspace_bytes(int grid, int d) {
   return (static_cast<size_t>(grid) * (2ull * (static_cast<size_t>(d) * 128 + 3 * 128) * sizeof(float)) + 255) /
@@ -53,6 +74,19 @@ int launch_forward(const void* Q, const void* K, const void* V, void* O, float* 
 // Records `e` as the calling thread's last CUDA error (fa2_last_cuda_error)
 // and returns FA2_ERR_CUDA.
 int record_cuda_error(cudaError_t e);
+
+// Shared with the backward pass: the current device's SM count and watchdog
+// word (FA2_ERR_UNSUPPORTED unless it is a compute-capability 10.3 GPU), a
+// 128-byte-swizzled [B*H, N, D] tensor map with boxes of `rows` rows x 64
+// elements, the watchdog limit, and an address-range overlap test.
+int current_device_facts(int* sms, int** status);
+bool encode_tile_map(CUtensorMap* map, const void* ptr, int bh, int n, int d, int dtype, unsigned rows);
+unsigned long long watchdog_limit_ns();
+bool ranges_overlap(const void* a, size_t na, const void* b, size_t nb);
+
+template <int D, bool kBf16, bool kCausal>
+cudaError_t launch_bwd(const CUtensorMap& k, const CUtensorMap& v, const CUtensorMap& q, const CUtensorMap& dout,
+                       const BwdParams& p, int grid, cudaStream_t stream);
 
 template <int D, bool kBf16, bool kCausal>
 cudaError_t launch_fwd(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v, const Params& p,

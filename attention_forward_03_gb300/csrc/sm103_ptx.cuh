@@ -1,5 +1,6 @@
-// Thin inline-PTX wrappers for the sm_103a features the forward kernel uses:
-// mbarriers, TMA tensor loads, tcgen05 MMA / TMEM management, and timers.
+// Thin inline-PTX wrappers for the sm_103a features the forward and backward
+// kernels use: mbarriers, TMA tensor and bulk loads, tcgen05 MMA / TMEM
+// management, and timers.
 #pragma once
 #include <cuda.h>
 #include <stdint.h>
@@ -64,6 +65,14 @@ __device__ __forceinline__ void tma_load_3d_hint(uint32_t dst, const CUtensorMap
       ::"r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1), "r"(c2),
       "l"(policy)
       : "memory");
+}
+
+// 1-D bulk copy global -> shared of `bytes` (a multiple of 16; both
+// addresses 16-byte aligned), completion counted on `bar` in bytes.
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+               ::"r"(dst), "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar)
+               : "memory");
 }
 
 __device__ __forceinline__ uint64_t l2_policy_evict_last() {
@@ -166,6 +175,11 @@ __host__ __device__ constexpr uint32_t make_idesc_f16(bool bf16, int n, bool b_m
   return (1u << 4) | ((bf16 ? 1u : 0u) << 7) | ((bf16 ? 1u : 0u) << 10) |
          ((b_mn_major ? 1u : 0u) << 16) | (static_cast<uint32_t>(n >> 3) << 17) |
          (static_cast<uint32_t>(128 >> 4) << 24);
+}
+
+// The same with the major-ness of both operands chosen (A: bit 15).
+__host__ __device__ constexpr uint32_t make_idesc_f16_ab(bool bf16, int n, bool a_mn_major, bool b_mn_major) {
+  return make_idesc_f16(bf16, n, b_mn_major) | ((a_mn_major ? 1u : 0u) << 15);
 }
 
 // ---------------------------------------------------------- shared memory

@@ -1,5 +1,6 @@
 /*
- * fa2.h — C ABI of the GB300 (sm_103a) FlashAttention-2 forward library.
+ * fa2.h — C ABI of the GB300 (sm_103a) FlashAttention-2 library: the forward
+ * pass and its gradient (fa2_bwd).
  *
  * The operation (FlashAttention-2 forward):
  *   for every batch b, head h and query row i of an N-long sequence,
@@ -188,6 +189,54 @@ int fa2_fwd_host(const void* Q, const void* K, const void* V, void* O, float* LS
                  int B, int H, int N, int D, float scale, int is_causal, int dtype,
                  int heads_per_chunk, int balanced, void* dev_buffer, size_t dev_bytes,
                  struct CUstream_st* stream);
+
+/*
+ * fa2_bwd_workspace_bytes — bytes of device workspace fa2_bwd needs for these
+ * sizes: an fp32 dQ accumulator [B, H, N, D] and two fp32 row statistics of
+ * B*H*ceil(N/64)*64 entries each, every part rounded up to 256 bytes.
+ * Returns FA2_OK, FA2_ERR_INVALID_ARG (bytes NULL or a negative size) or
+ * FA2_ERR_UNSUPPORTED (D not 64 or 128). Needs no device.
+ */
+int fa2_bwd_workspace_bytes(int B, int H, int N, int D, size_t* bytes);
+
+/*
+ * fa2_bwd — enqueue the backward pass (the gradient of fa2_fwd's O with
+ * respect to Q, K and V for an upstream gradient dO) on `stream`.
+ *
+ * The operation, for every (b, h), with P the softmax weights of the forward:
+ *   dV = P^T dO,  dP = dO V^T,  Delta_i = <dO_i, O_i>,  dS = P * (dP - Delta)
+ *   dQ = scale * dS K,  dK = scale * dS^T Q
+ * P is recomputed from Q, K and LSE (P_ij = exp(S_ij - LSE_i)); S and P never
+ * reach device memory; the outer loop runs over K/V tiles and dQ is summed
+ * across them with fp32 atomic adds. Source: the yangyitao.com CUDA book,
+ * ch. 15, section 15.1 (change 4: only LSE is kept for the backward pass)
+ * and the chapter's closing paragraph (S and P recomputed, dQ accumulated
+ * atomically, outer loop over K/V).
+ *
+ * Q, K, V : device pointers, the forward's inputs ([B, H, N, D], `dtype`).
+ * O, LSE  : the forward's outputs for those inputs (fa2_fwd's O and LSE).
+ * dO      : device pointer, [B, H, N, D] of `dtype`: the upstream gradient.
+ * dQ, dK, dV: device pointers, [B, H, N, D] of `dtype`. Fully overwritten,
+ *           rounded to nearest-even. Must not overlap each other, an input
+ *           or the workspace.
+ * B, H, N, D, scale, is_causal, dtype: as for fa2_fwd (the same values the
+ *           forward was called with).
+ * workspace: device memory of at least fa2_bwd_workspace_bytes(B, H, N, D)
+ *           bytes, 256-byte aligned, owned by the caller. Its contents on
+ *           entry do not matter; it is scratch for the duration of the call
+ *           on `stream` and must not be used by other work until the call's
+ *           kernels have finished.
+ * stream  : CUDA stream of the current device (NULL = legacy default).
+ *
+ * All tensor pointers must be 16-byte aligned. Three kernels are enqueued in
+ * order (row statistics, the backward, dQ conversion). Errors as fa2_fwd,
+ * plus FA2_ERR_INVALID_ARG for a missing or too small workspace and
+ * FA2_ERR_ALIGN for a misaligned one. The library allocates nothing.
+ */
+int fa2_bwd(const void* Q, const void* K, const void* V, const void* O, const void* dO,
+            const float* LSE, void* dQ, void* dK, void* dV,
+            int B, int H, int N, int D, float scale, int is_causal, int dtype,
+            void* workspace, size_t workspace_bytes, struct CUstream_st* stream);
 
 /*
  * fa2_device_status — read the device-side watchdog word of the current

@@ -33,10 +33,14 @@
  * m_i, l_i). Each output row is computed by one thread with a fixed loop
  * order, so results do not depend on the thread count.
  *
- * Optional outputs *_mag hold, per element, the sum of the absolute values
- * of the terms of that element's sum (for dQ: scale * sum_j |dS_ij K_jd|).
- * Tests use them to bound the rounding error a 16-bit operand in each term
- * can cause.
+ * Optional outputs *_mag are per-element condition sums for error bounds:
+ *   dV_mag = sum_i |P_ij dO_id|
+ *   dQ_mag = scale * sum_j P_ij (|dP_ij - Delta_i| + A_i) |K_jd|
+ *   dK_mag = scale * sum_i P_ij (|dP_ij - Delta_i| + A_i) |Q_id|
+ * with A_i = sum_d |dO_id O_id|. A relative perturbation of size u of each
+ * P_ij, of each dS_ij and of each O_id (16-bit rounding of those operands)
+ * moves an element by at most about u times its condition sum. Each is at
+ * least the sum of the absolute values of the element's terms.
  */
 #include <math.h>
 #include <pthread.h>
@@ -49,6 +53,7 @@ typedef struct {
     double scale;
     int causal;
     double *m, *l, *delta;             /* [N] row statistics (pass 1 output)  */
+    double *amag;                      /* [N] sum_d |dO_id O_id| (pass 1)     */
     double *dq, *dk, *dv;              /* [N, D]                              */
     double *dq_mag, *dk_mag, *dv_mag;  /* [N, D] or NULL                      */
 } bwd_ctx;
@@ -99,15 +104,17 @@ static void bwd_query_row(const bwd_ctx *c, long i, double *s)
         l += s[j];
     }
     /* O_i, then Delta_i = <dO_i, O_i> */
-    double delta = 0.0;
+    double delta = 0.0, amag = 0.0;
     for (long col = 0; col < d; ++col) {
         double o = 0.0;
         for (long j = 0; j < nvis; ++j) o += s[j] * c->v[j * d + col];
         delta += doi[col] * (o / l);
+        amag += fabs(doi[col] * (o / l));
     }
     c->m[i] = m;
     c->l[i] = l;
     c->delta[i] = delta;
+    c->amag[i] = amag;
     for (long col = 0; col < d; ++col) {
         dqi[col] = 0.0;
         if (dqm) dqm[col] = 0.0;
@@ -117,10 +124,11 @@ static void bwd_query_row(const bwd_ctx *c, long i, double *s)
         const double p = s[j] / l;
         const double dp = dot(doi, c->v + j * d, d);
         const double ds = p * (dp - delta);
+        const double cond = c->scale * p * (fabs(dp - delta) + amag);
         for (long col = 0; col < d; ++col) {
             const double t = c->scale * ds * kj[col];
             dqi[col] += t;
-            if (dqm) dqm[col] += fabs(t);
+            if (dqm) dqm[col] += cond * fabs(kj[col]);
         }
     }
 }
@@ -145,13 +153,14 @@ static void bwd_key_row(const bwd_ctx *c, long j)
         const double p = exp(sij - c->m[i]) / c->l[i];
         const double dp = dot(doi, vj, d);
         const double ds = p * (dp - c->delta[i]);
+        const double cond = c->scale * p * (fabs(dp - c->delta[i]) + c->amag[i]);
         for (long col = 0; col < d; ++col) {
             const double tv = p * doi[col];
             const double tk = c->scale * ds * qi[col];
             dvj[col] += tv;
             dkj[col] += tk;
             if (dvm) dvm[col] += fabs(tv);
-            if (dkm) dkm[col] += fabs(tk);
+            if (dkm) dkm[col] += cond * fabs(qi[col]);
         }
     }
 }
@@ -205,7 +214,7 @@ static int run_pass(const bwd_ctx *c, int pass, int nthreads)
 /*
  * One head. q, k, v, dout: [n, d] row-major doubles. dq, dk, dv: [n, d]
  * outputs. delta (optional, [n]): receives Delta_i. *_mag (optional, [n, d]):
- * per-element sums of the absolute values of the terms. Returns 0, or -1 on
+ * per-element condition sums (see above). Returns 0, or -1 on
  * a bad argument or an allocation failure.
  */
 int fa2_oracle_bwd_head(const double *q, const double *k, const double *v, const double *dout,
@@ -214,13 +223,13 @@ int fa2_oracle_bwd_head(const double *q, const double *k, const double *v, const
                         double *dq_mag, double *dk_mag, double *dv_mag, int nthreads)
 {
     if (!q || !k || !v || !dout || !dq || !dk || !dv || n < 1 || d < 1) return -1;
-    double *stats = (double *)malloc((size_t)3 * (size_t)n * sizeof(double));
+    double *stats = (double *)malloc((size_t)4 * (size_t)n * sizeof(double));
     if (!stats) return -1;
     bwd_ctx c;
     memset(&c, 0, sizeof(c));
     c.q = q; c.k = k; c.v = v; c.dout = dout;
     c.n = n; c.d = d; c.scale = scale; c.causal = causal;
-    c.m = stats; c.l = stats + n; c.delta = stats + 2 * n;
+    c.m = stats; c.l = stats + n; c.delta = stats + 2 * n; c.amag = stats + 3 * n;
     c.dq = dq; c.dk = dk; c.dv = dv;
     c.dq_mag = dq_mag; c.dk_mag = dk_mag; c.dv_mag = dv_mag;
     int rc = run_pass(&c, 1, nthreads);

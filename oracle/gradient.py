@@ -44,8 +44,10 @@ def attention_bwd(q, k, v, do, scale: float, causal: bool, heads=None, magnitude
 
     q, k, v, do: [B, H, N, D] tensors or arrays (any float dtype; widened exactly).
     heads: None for every head, else a list of flat head ids bh = b*H + h.
-    magnitudes: also return, per element, the sum of the absolute values of
-      the terms of its sum (dQ_mag, dK_mag, dV_mag), for error bounds.
+    magnitudes: also return per-element condition sums (dq_mag, dk_mag, dv_mag):
+      a relative perturbation u of every P, dS and O value moves an element by
+      at most about u times its sum (see fa2_bwd_oracle.c); each is at least
+      the sum of the absolute values of the element's terms.
     libpath: load the C code from another build of it (mutation tests only).
     Returns a dict of float64 arrays: dq, dk, dv ([B,H,N,D], or [len(heads),N,D]),
     delta ([B,H,N] or [len(heads),N]) and, with magnitudes, dq_mag, dk_mag, dv_mag.

@@ -203,3 +203,46 @@ def test_schedule_choice():
     assert choose_schedule(1, 1, 8192, False, 152) == "balanced"   # 32 long units on 152 SMs
     assert choose_schedule(1, 1, 128, False, 152) == "units"       # one tiny unit
     assert choose_schedule(0, 8, 8192, False, 152) == "units"      # empty
+
+
+BWD = dict(Q=A, K=A * 16, V=A * 32, O=A * 48, dO=A * 64, LSE=A * 80, dQ=A * 96, dK=A * 112, dV=A * 128, B=1, H=2,
+           N=64, D=64, scale=0.125, is_causal=0, dtype=0, ws=A * 144, nws=1 << 24, stream=None)
+
+
+def call_bwd(lib, **over):
+    a = dict(BWD, **over)
+    return lib.library().fa2_bwd(*[a[x] for x in ("Q", "K", "V", "O", "dO", "LSE", "dQ", "dK", "dV", "B", "H", "N",
+                                                  "D", "scale", "is_causal", "dtype", "ws", "nws", "stream")])
+
+
+@pytest.mark.parametrize("over,code", [
+    (dict(B=-1), -1), (dict(N=-2), -1), (dict(D=96), -2), (dict(dtype=7), -2),
+    (dict(scale=0.0), -1), (dict(scale=float("nan")), -1),
+    (dict(Q=None), -1), (dict(dO=None), -1), (dict(LSE=None), -1), (dict(dK=None), -1), (dict(ws=None), -1),
+    (dict(dO=A * 64 + 8), -3), (dict(dV=A * 128 + 4), -3), (dict(ws=A * 144 + 16), -3),
+    (dict(nws=1024), -1),                 # workspace too small
+    (dict(dQ=A + 512), -1),               # dQ overlaps Q
+    (dict(dK=A * 96 + 256), -1),          # dK overlaps dQ
+    (dict(ws=A * 128 + 256), -1),         # workspace overlaps dV
+    (dict(B=1 << 16, H=1 << 16), -1),     # B*H overflows int32
+])
+def test_backward_rejects_bad_arguments_before_any_gpu_work(lib, over, code):
+    assert call_bwd(lib, **over) == code
+
+
+def test_backward_empty_problem_and_workspace_size(lib):
+    assert call_bwd(lib, B=0) == lib.FA2_OK
+    assert call_bwd(lib, N=0, Q=None, ws=None) == lib.FA2_OK
+    # fp32 dQ accumulator [B,H,N,D] + LSE*log2(e) and Delta rows padded to 64, each rounded to 256 bytes
+    r256 = lambda x: -(-x // 256) * 256  # noqa: E731
+    for (B, H, N, D) in ((1, 2, 64, 64), (2, 12, 1000, 64), (1, 8, 8192, 128), (1, 1, 1, 128)):
+        npad = -(-N // 64) * 64
+        assert lib.fa2_bwd_workspace_bytes(B, H, N, D) == r256(B * H * N * D * 4) + 2 * r256(B * H * npad * 4)
+    n = ctypes.c_size_t(0)
+    assert lib.library().fa2_bwd_workspace_bytes(1, 1, 64, 96, ctypes.byref(n)) == lib.FA2_ERR_UNSUPPORTED
+    assert lib.library().fa2_bwd_workspace_bytes(1, 1, 64, 64, None) == lib.FA2_ERR_INVALID_ARG
+
+
+@pytest.mark.skipif(torch.cuda.is_available(), reason="only meaningful on a host without a GPU")
+def test_backward_without_a_gpu_fails_loudly(lib):
+    assert call_bwd(lib) == lib.FA2_ERR_CUDA

@@ -1,0 +1,166 @@
+"""Parity of the sm_103a backward pass with the CPU fp64 gradient oracle, through the C ABI.
+
+Inputs: the seeded Q, K, V of a workload and an upstream gradient dO
+(workloads.make_grad_output). The GPU runs its own forward (fa2_fwd: O and
+LSE) and then fa2_bwd; the oracle differentiates the exact definition.
+
+Tolerance, per element x of dQ, dK and dV (derived from the arithmetic):
+  |x_gpu - x_ref| <= 3u * cond(x) + u * |x_ref| + 2^-20 * max(cond)
+with u the unit roundoff of the dtype (2^-11 fp16, 2^-8 bf16) and cond(x)
+the oracle's condition sum: a relative change u of every P, dS and O value,
+which the kernel rounds to the dtype before the tensor core reads them, moves
+x by at most about u * cond(x). The factor 3 covers those three roundings;
+u * |x_ref| is the rounding of the output; the last term covers fp32
+accumulation (ex2.approx, MMA and atomic summation order), far below u.
+"""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+import torch
+
+import workloads
+
+pytestmark = pytest.mark.gpu
+
+U = {"f16": 2.0 ** -11, "bf16": 2.0 ** -8}
+
+
+@pytest.fixture(scope="module")
+def fa2():
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    from attention_forward_03_gb300 import build
+    build.build()
+    import attention_forward_03_gb300 as m
+    m.fa2_device_status(clear=True)
+    return m
+
+
+def run_gpu(fa2, w, q, k, v, do, stream=None, outs=None, workspace=None):
+    qd, kd, vd, dod = (t.cuda() for t in (q, k, v, do))
+    O, L = fa2.attention_forward(qd, kd, vd, scale=w.scale, is_causal=w.causal)
+    kw = {}
+    if outs is not None:
+        kw = dict(dq=outs[0], dk=outs[1], dv=outs[2])
+    grads = fa2.attention_backward(qd, kd, vd, O, L, dod, scale=w.scale, is_causal=w.causal, stream=stream,
+                                   workspace=workspace, **kw)
+    torch.cuda.synchronize()
+    assert fa2.fa2_device_status(clear=True) == 0, "device watchdog fired"
+    return dict(zip(("dq", "dk", "dv"), grads))
+
+
+def check(w, gpu, ref, heads=None):
+    """Compare GPU gradients (all heads, or the listed flat head ids) with the oracle's."""
+    u = U[w.dtype]
+    worst = {}
+    for name in ("dq", "dk", "dv"):
+        g = gpu[name].float().cpu().numpy().astype(np.float64).reshape(w.B * w.H, w.N, w.D)
+        if heads is not None:
+            g = g[np.asarray(heads)]
+        r = ref[name].reshape(g.shape)
+        m = ref[name + "_mag"].reshape(g.shape)
+        assert np.isfinite(g).all(), f"{w.describe()} {name}: non-finite values"
+        bound = 3 * u * m + u * np.abs(r) + 2.0 ** -20 * m.max()
+        ratio = float((np.abs(g - r) / bound).max())
+        worst[name] = (ratio, float(np.abs(g - r).max()))
+        assert ratio <= 1.0, f"{w.describe()} {name}: error/bound = {ratio:.3f}, max|err| = {worst[name][1]:.3e}"
+    return worst
+
+
+def compare(fa2, oracle_mod, w, heads=None):
+    q, k, v = workloads.make_inputs(w)
+    do = workloads.make_grad_output(w)
+    gpu = run_gpu(fa2, w, q, k, v, do)
+    ref = oracle_mod.attention_bwd(q, k, v, do, w.scale, w.causal, heads=heads, magnitudes=True)
+    return check(w, gpu, ref, heads)
+
+
+def test_tiny_every_element(fa2, oracle_mod):
+    compare(fa2, oracle_mod, workloads.WORKLOADS["tiny"])
+
+
+EDGE_N = [1, 7, 63, 64, 65, 127, 128, 129, 255, 257, 1000]
+
+
+@pytest.mark.parametrize("N", EDGE_N)
+@pytest.mark.parametrize("D", [64, 128])
+@pytest.mark.parametrize("dtype", ["f16", "bf16"])
+@pytest.mark.parametrize("causal", [False, True])
+def test_edge_shapes_every_element(fa2, oracle_mod, N, D, dtype, causal):
+    compare(fa2, oracle_mod, workloads.custom(1, 2, N, D, dtype, causal, seed=N * 11 + D))
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_many_units_per_cta(fa2, oracle_mod, causal):
+    """160 K/V tiles on at most 152 CTAs: units after the first reuse TMEM, the ring and barriers."""
+    compare(fa2, oracle_mod, workloads.custom(1, 40, 512, 64, "bf16", causal, seed=77))
+
+
+@pytest.mark.parametrize("D", [64, 128])
+def test_long_rows_every_element(fa2, oracle_mod, D):
+    """Many query steps per unit (N = 2048: 32 steps of 64 rows) and ragged N."""
+    compare(fa2, oracle_mod, workloads.custom(1, 2, 2000, D, "f16", True, seed=78))
+
+
+def test_peaked_logits_every_element(fa2, oracle_mod):
+    """Q, K ~ N(0, 3^2): sharply peaked rows, P close to one-hot."""
+    compare(fa2, oracle_mod, workloads.custom(2, 3, 700, 64, "f16", False, seed=79, sigma_qk=3.0))
+
+
+@pytest.mark.parametrize("name", workloads.CONTRACT + ("target",))
+def test_contract_workloads_full_size(fa2, oracle_mod, name):
+    """Full-size workloads, launched as the benchmark launches them; the oracle checks the
+    first and last head whole (every row of dQ, dK and dV there)."""
+    w = workloads.WORKLOADS[name]
+    heads = [w.B * w.H - 1] if w.N > 16384 else [0, w.B * w.H - 1]
+    compare(fa2, oracle_mod, w, heads=heads)
+
+
+def test_workspace_and_outputs_may_hold_garbage(fa2, oracle_mod):
+    """The workspace (fp32 accumulator, row statistics) and the outputs start as NaN bytes:
+    every output element is written and the accumulator is cleared by the call itself."""
+    w = workloads.custom(1, 3, 333, 128, "bf16", True, seed=80)
+    q, k, v = workloads.make_inputs(w)
+    do = workloads.make_grad_output(w)
+    need = fa2.fa2_bwd_workspace_bytes(w.B, w.H, w.N, w.D)
+    ws = torch.full((need,), 0xFF, dtype=torch.uint8, device="cuda")
+    outs = [torch.full(q.shape, float("nan"), dtype=q.dtype, device="cuda") for _ in range(3)]
+    ref = oracle_mod.attention_bwd(q, k, v, do, w.scale, w.causal, magnitudes=True)
+    first = run_gpu(fa2, w, q, k, v, do, outs=outs, workspace=ws)
+    check(w, first, ref)
+    keep = {n: t.clone() for n, t in first.items()}
+    second = run_gpu(fa2, w, q, k, v, do, outs=outs, workspace=ws)
+    check(w, second, ref)
+    # dK and dV are summed in one fixed order; dQ by atomics (order may vary)
+    assert torch.equal(keep["dk"], second["dk"]) and torch.equal(keep["dv"], second["dv"])
+
+
+def test_runs_on_a_side_stream(fa2, oracle_mod):
+    w = workloads.custom(2, 2, 300, 64, "f16", False, seed=81)
+    q, k, v = workloads.make_inputs(w)
+    do = workloads.make_grad_output(w)
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        gpu = run_gpu(fa2, w, q, k, v, do, stream=s)
+    ref = oracle_mod.attention_bwd(q, k, v, do, w.scale, w.causal, magnitudes=True)
+    check(w, gpu, ref)
+
+
+def test_non_default_scale(fa2, oracle_mod):
+    w = workloads.custom(1, 2, 200, 128, "bf16", True, seed=82)
+    q, k, v = workloads.make_inputs(w)
+    do = workloads.make_grad_output(w)
+    scale = 0.3
+    qd, kd, vd, dod = (t.cuda() for t in (q, k, v, do))
+    O, L = fa2.attention_forward(qd, kd, vd, scale=scale, is_causal=True)
+    dq, dk, dv = fa2.attention_backward(qd, kd, vd, O, L, dod, scale=scale, is_causal=True)
+    torch.cuda.synchronize()
+    ref = oracle_mod.attention_bwd(q, k, v, do, scale, True, magnitudes=True)
+    check(w, dict(dq=dq, dk=dk, dv=dv), ref)
+
+
+def test_empty_problem(fa2):
+    q = torch.empty(0, 2, 64, 64, dtype=torch.float16, device="cuda")
+    lse = torch.empty(0, 2, 64, dtype=torch.float32, device="cuda")
+    dq, dk, dv = fa2.attention_backward(q, q, q, q, lse, q)
+    assert dq.numel() == 0 and dk.numel() == 0 and dv.numel() == 0

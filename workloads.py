@@ -92,6 +92,16 @@ def make_inputs(w: Workload):
     return q.to(dt).contiguous(), k.to(dt).contiguous(), v.to(dt).contiguous()
 
 
+def make_grad_output(w: Workload) -> torch.Tensor:
+    """The upstream gradient dO for the backward pass: i.i.d. N(0, 1) of the
+    workload's shape, drawn from a CPU generator seeded with seed + 1000 (so
+    Q, K, V are the forward's inputs unchanged), cast to the 16-bit dtype."""
+    g = torch.Generator(device="cpu")
+    g.manual_seed(w.seed + 1000)
+    shape = (w.B, w.H, w.N, w.D)
+    return (torch.randn(shape, dtype=torch.float32, generator=g)).to(w.torch_dtype).contiguous()
+
+
 def flops(w: Workload) -> float:
     """Metric FLOPs of one forward: 4*B*H*N^2*D, halved under the causal mask."""
     f = 4.0 * w.B * w.H * float(w.N) * w.N * w.D
@@ -106,3 +116,17 @@ def algorithmic_bytes(w: Workload) -> int:
 
 def with_seed(w: Workload, seed: int) -> Workload:
     return replace(w, seed=seed)
+
+
+def bwd_flops(w: Workload) -> float:
+    """Metric FLOPs of one backward: five N x N x D matrix products per head
+    (S, dP, dV, dK, dQ), 10*B*H*N^2*D, halved under the causal mask
+    (2.5 times the forward's)."""
+    return 2.5 * flops(w)
+
+
+def bwd_algorithmic_bytes(w: Workload) -> int:
+    """Compulsory HBM bytes of one backward: read Q, K, V, O, dO (16-bit) and
+    LSE (fp32) once, write dQ, dK, dV (16-bit)."""
+    elems = w.B * w.H * w.N * w.D
+    return 8 * elems * 2 + w.B * w.H * w.N * 4
