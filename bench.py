@@ -2,6 +2,7 @@
 """Benchmark of the GB300 FlashAttention-2 forward (one JSON line on stdout).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl gb300|reference]
+                  [--pass fwd|bwd]
 
 A step is one forward pass (one kernel launch) over the workload's [B,H,N,D]
 inputs, already resident in HBM. Timing uses CUDA events on the launching
@@ -13,6 +14,8 @@ own GPU (weak scaling, no collective on the data path) and the slowest rank's
 time is reported.
 
 Metric: attention forward TFLOP/s = 4*B*H*N^2*D (halved when causal) / time.
+`--pass bwd` times the backward pass (fa2_bwd) instead: 10*B*H*N^2*D
+(halved when causal) / time of the whole call.
 `--impl reference` times the CPU fp64 oracle (this path's reference
 implementation) on a bounded sample of the same workload instead.
 """
@@ -414,6 +417,119 @@ def run_gb300(args, w, rank, world, local):
     return line
 
 
+BWD_METRIC = "attention backward TFLOPS (10·B·H·N²·D: S, dP, dV, dK, dQ products) and % of GB300 dense fp16/bf16 peak"
+
+
+def time_grad_oracle(w: workloads.Workload, heads, inputs):
+    """One timed gradient-oracle call on whole heads. Returns (tflops, seconds, threads, description)."""
+    import oracle
+    q, k, v, do = inputs
+    threads = oracle.default_threads()
+    t0 = time.perf_counter()
+    oracle.attention_bwd(q, k, v, do, w.scale, w.causal, heads=heads, nthreads=threads)
+    secs = time.perf_counter() - t0
+    fl = workloads.bwd_flops(w) * len(heads) / (w.B * w.H)
+    desc = (f"{len(heads)} of its {w.B * w.H} heads, whole ({w.describe()}), gradient of the fp64 definition, "
+            f"{threads} threads")
+    return fl / secs / 1e12, secs, threads, desc
+
+
+def run_gb300_bwd(args, w, rank, world, local):
+    """The backward pass (fa2_bwd: row-statistics prologue, backward kernel, dQ conversion) as the step."""
+    import torch
+
+    import attention_forward_03_gb300 as fa2
+    if not torch.cuda.is_available():
+        raise RuntimeError("the gb300 arm needs a CUDA device")
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    fa2.library()
+    stream = torch.cuda.current_stream(dev)
+    q, k, v = workloads.make_inputs(w)
+    do = workloads.make_grad_output(w)
+    set_bytes = workloads.bwd_algorithmic_bytes(w)
+    l2 = getattr(torch.cuda.get_device_properties(dev), "L2_cache_size", 128 * 2 ** 20)
+    nsets = max(2, math.ceil(2 * l2 / set_bytes))
+    need = fa2.fa2_bwd_workspace_bytes(w.B, w.H, w.N, w.D)
+    sets = []
+    for _ in range(nsets):
+        qd, kd, vd, dod = (t.to(dev) for t in (q, k, v, do))
+        od, ld = fa2.attention_forward(qd, kd, vd, scale=w.scale, is_causal=w.causal, stream=stream)
+        outs = tuple(torch.empty_like(qd) for _ in range(3))
+        ws = torch.empty(need, dtype=torch.uint8, device=dev)
+        sets.append((qd, kd, vd, od, ld, dod, outs, ws))
+    torch.cuda.synchronize(dev)
+
+    def step(i):
+        qd, kd, vd, od, ld, dod, outs, ws = sets[i % nsets]
+        fa2.attention_backward(qd, kd, vd, od, ld, dod, scale=w.scale, is_causal=w.causal, dq=outs[0], dk=outs[1],
+                               dv=outs[2], workspace=ws, stream=stream)
+
+    clocks = ClockSampler(local)
+    clocks.start()
+    for i in range(args.warmup):
+        step(i)
+    torch.cuda.synchronize(dev)
+    t0 = time.perf_counter()
+    i = 0
+    while time.perf_counter() - t0 < args.settle_seconds:
+        step(i)
+        i += 1
+        if i % 8 == 0:
+            torch.cuda.synchronize(dev)
+    torch.cuda.synchronize(dev)
+    fa2.fa2_device_status(clear=True)
+    ev0 = torch.cuda.Event(enable_timing=True)
+    ev1 = torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    clocks.mark_start()
+    ev0.record(stream)
+    for i in range(args.steps):
+        step(i)
+    ev1.record(stream)
+    torch.cuda.synchronize(dev)
+    clocks.mark_stop()
+    barrier(world)
+    elapsed = ev0.elapsed_time(ev1) / 1e3
+    clock_info = clocks.stop()
+    status = fa2.fa2_device_status(clear=True)
+    if status != 0:
+        raise RuntimeError(f"device watchdog fired during the timed region (code {status})")
+    t_max = max_over_ranks(elapsed, world, dev)
+    flops = workloads.bwd_flops(w)
+    value = whole_job_tflops(flops, args.steps, world, t_max)
+    per_call = elapsed / args.steps
+    if rank != 0:
+        return None
+    peaks, peak_src = load_peaks()
+    peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    achieved = flops / per_call / 1e12
+    line = {
+        "pass": "backward", "metric": BWD_METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * t_max / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": w.dtype,
+        "data": "synthetic (seeded N(0, sigma^2) Q, K, V and dO, cast to the workload's 16-bit dtype; "
+                "O and LSE from fa2_fwd)",
+        "config": {"workload": w.describe(), "B": w.B, "H": w.H, "N": w.N, "D": w.D, "causal": w.causal,
+                   "scale": "1/sqrt(D)", "parallelism": f"weak x{world} (one independent replica per GPU)",
+                   "l2": f"inputs rotate over {nsets} copies ({nsets * set_bytes / 2**20:.0f} MiB > 2x L2)"},
+        "pct_of_peak": 100.0 * achieved / peak,
+        "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                     "frac": achieved / peak, "peak_source": f"{peak_src} bf16 dense (burst)",
+                     "timed": "the whole fa2_bwd call (prologue, backward kernel and dQ conversion)",
+                     "traffic": None, "algorithmic_bytes": set_bytes,
+                     "achieved_hbm_gbs": set_bytes / per_call / 1e9},
+        "gpu_launches": 3 * args.steps,
+        "clocks": clock_info,
+    }
+    if not args.no_cpu_baseline:
+        tf, secs, threads, desc = time_grad_oracle(w, [0], (q, k, v, do))
+        line["cpu_baseline"] = {"value": tf, "unit": UNIT, "cores": threads, "kind": "oracle", "sample": desc,
+                                "seconds": secs}
+    return line
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
@@ -431,10 +547,14 @@ def main(argv=None):
     ap.add_argument("--reference-seconds", type=float, default=120.0,
                     help="total CPU time budget of the reference arm")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--pass", dest="which", default="fwd", choices=["fwd", "bwd"],
+                    help="fwd: the forward pass (the headline); bwd: the backward pass (fa2_bwd)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     w = workloads.WORKLOADS[args.workload]
+    if args.impl == "reference" and args.which == "bwd":
+        ap.error("--impl reference times the forward oracle; the backward's CPU baseline is in its gb300 line")
     if args.impl == "reference":
         # the CPU oracle runs on rank 0 only; other ranks exit without work
         rank, world = int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1"))
@@ -445,7 +565,7 @@ def main(argv=None):
     rank, world, local = dist_setup()
     if world != args.gpus and rank == 0:
         print(f"note: --gpus {args.gpus} but WORLD_SIZE {world}", file=sys.stderr)
-    line = run_gb300(args, w, rank, world, local)
+    line = (run_gb300_bwd if args.which == "bwd" else run_gb300)(args, w, rank, world, local)
     if rank == 0 and line is not None:
         print(json.dumps(line), flush=True)
     if world > 1:
