@@ -119,7 +119,7 @@ __global__ void __launch_bounds__(kElemThreads) fa2_bwd_dq_convert(const float4*
 }
 
 using BwdLaunchFn = cudaError_t (*)(const CUtensorMap&, const CUtensorMap&, const CUtensorMap&, const CUtensorMap&,
-                                    const BwdParams&, int, cudaStream_t);
+                                    const CUtensorMap&, const BwdParams&, int, cudaStream_t);
 
 BwdLaunchFn pick_bwd(int d, int dtype, int causal) {
   const bool bf = dtype == FA2_BF16, c = causal != 0;
@@ -210,6 +210,8 @@ extern "C" int fa2_bwd(const void* Q, const void* K, const void* V, const void* 
   const int npad = (N + kBwdRows - 1) / kBwdRows * kBwdRows;
   char* ws = static_cast<char*>(workspace);
   float* dq_acc = reinterpret_cast<float*>(ws);
+  CUtensorMap mdq;  // the kernel adds blocks of 32 rows of dQ into the accumulator
+  if (!encode_f32_rows_map(&mdq, dq_acc, (int)bh, N, D, 32)) return record_cuda_error(cudaErrorInvalidValue);
   float* lse2 = reinterpret_cast<float*>(ws + wl.dq_bytes);
   float* delta = reinterpret_cast<float*>(ws + wl.dq_bytes + wl.stat_bytes);
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
@@ -238,7 +240,7 @@ extern "C" int fa2_bwd(const void* Q, const void* K, const void* V, const void* 
   p.scale_log2 = scale * 1.4426950408889634f;
   p.scale = scale;
   const int grid = p.num_units < sms ? p.num_units : sms;
-  e = pick_bwd(D, dtype, is_causal)(mk, mv, mq, mdo, p, grid, s);
+  e = pick_bwd(D, dtype, is_causal)(mk, mv, mq, mdo, mdq, p, grid, s);
   if (e != cudaSuccess) return record_cuda_error(e);
 
   const long long n8 = bh * N * (D / 8);

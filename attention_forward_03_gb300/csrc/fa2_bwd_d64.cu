@@ -3,11 +3,15 @@
 
 namespace fa2 {
 template cudaError_t launch_bwd<64, false, false>(const CUtensorMap&, const CUtensorMap&, const CUtensorMap&,
-                                                 const CUtensorMap&, const BwdParams&, int, cudaStream_t);
+                                                 const CUtensorMap&, const CUtensorMap&, const BwdParams&, int,
+                                                 cudaStream_t);
 template cudaError_t launch_bwd<64, false, true>(const CUtensorMap&, const CUtensorMap&, const CUtensorMap&,
-                                                const CUtensorMap&, const BwdParams&, int, cudaStream_t);
+                                                const CUtensorMap&, const CUtensorMap&, const BwdParams&, int,
+                                                 cudaStream_t);
 template cudaError_t launch_bwd<64, true, false>(const CUtensorMap&, const CUtensorMap&, const CUtensorMap&,
-                                                const CUtensorMap&, const BwdParams&, int, cudaStream_t);
+                                                const CUtensorMap&, const CUtensorMap&, const BwdParams&, int,
+                                                 cudaStream_t);
 template cudaError_t launch_bwd<64, true, true>(const CUtensorMap&, const CUtensorMap&, const CUtensorMap&,
-                                               const CUtensorMap&, const BwdParams&, int, cudaStream_t);
+                                               const CUtensorMap&, const CUtensorMap&, const BwdParams&, int,
+                                                 cudaStream_t);
 }  // namespace fa2

@@ -13,6 +13,7 @@
 //   dP^T = V dO_i^T           dS^T = P^T * (dP^T - Delta_i),  Delta_i = <dO_i, O_i>
 //   dV  += P^T dO_i           dK  += dS^T Q_i        (in TMEM for the whole tile)
 //   dQ_i^T = K^T dS^T         added into an fp32 dQ accumulator in global memory
+//                             (a TMA bulk reduce-add per warpgroup and step)
 //
 // and at the end of the tile dK *= scale; dQ = scale * accumulator is
 // converted to the dtype by a separate elementwise kernel.
@@ -30,8 +31,10 @@
 //                   MMA runs with M = 128 and lanes 64-127 are discarded)
 // Shared memory (128-byte swizzled, 64-element panels): K and V of the tile
 // (resident for the unit), a ring of query steps (Q_i, dO_i, and the 64
-// LSE*log2(e) and Delta values), and the 16-bit P^T and dS^T of the step
-// (written by the compute threads, read by the tensor core).
+// LSE*log2(e) and Delta values), the 16-bit P^T and dS^T of the step
+// (written by the compute threads, read by the tensor core), and an fp32
+// staging tile for dQ (64 rows x D) that TMA reduce-adds into the global
+// accumulator, 32 rows per compute warpgroup.
 //
 // Pipelining: the issuer computes S^T, dP^T of step i+1 as soon as the
 // compute threads have loaded those of step i into registers, so the tensor
@@ -64,6 +67,8 @@ enum : int {
   kSiteBwdDqFull = 31,
   kSiteBwdAccFull = 32,
   kSiteBwdDrain = 33,
+  kSiteBwdDqsFree = 34,
+  kSiteBwdDqsReady = 35,
 };
 
 template <int D>
@@ -78,11 +83,12 @@ struct BwdLayout {
   static constexpr int kRing = 2 * kKVBytes;
   static constexpr int kP = kRing + kStages * kStageBytes;
   static constexpr int kDS = kP + kBwdPTileBytes;
-  static constexpr int kStats = kDS + kBwdPTileBytes;
+  static constexpr int kDQS = kDS + kBwdPTileBytes;           // dQ staging: 64 rows x D fp32
+  static constexpr int kStats = kDQS + kBwdRows * D * 4;
   static constexpr int kBars = kStats + kStages * kBwdStatBytes;
   // kv_full, kv_empty, stage_full[S], stage_empty[S], s_full, s_free, p_full,
-  // p_free, dq_full, dq_free, acc_full, acc_free, drain
-  static constexpr int kNumBars = 2 + 2 * kStages + 9;
+  // p_free, dq_full, dq_free, acc_full, acc_free, drain, dqs_ready[2], dqs_free[2]
+  static constexpr int kNumBars = 2 + 2 * kStages + 13;
   static constexpr int kMisc = kBars + kNumBars * 8;
   static constexpr int kSmemBytes = kMisc + 16 + 1024;  // + slack for 1 KB alignment
   static constexpr uint32_t kColDV = 0;
@@ -126,7 +132,7 @@ template <int D, bool kBf16, bool kCausal>
 __global__ void __launch_bounds__(kBwdThreads, 1)
     fa2_bwd_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                    const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmDO,
-                   const BwdParams p) {
+                   const __grid_constant__ CUtensorMap tmDQ, const BwdParams p) {
   using L = BwdLayout<D>;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   const uint32_t raw = smem_addr(smem_raw);
@@ -154,6 +160,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   const uint32_t bar_acc_full = bar_s_full + 48;              // dV, dK of a unit complete
   const uint32_t bar_acc_free = bar_s_full + 56;              // ... loaded by the compute threads
   const uint32_t bar_drain = bar_s_full + 64;
+  // per compute warpgroup: its 32 staged dQ rows are written / have been read by TMA
+  auto bar_dqs_ready = [&](int w) { return bar_s_full + 72 + 8u * w; };
+  auto bar_dqs_free = [&](int w) { return bar_s_full + 88 + 8u * w; };
+  const uint32_t sDQS = base + L::kDQS;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kMisc + 4);
 
@@ -176,6 +186,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     mbar_init(bar_acc_full, 1);
     mbar_init(bar_acc_free, kBwdComputeThreads);
     mbar_init(bar_drain, 1);
+    for (int w = 0; w < 2; ++w) {
+      mbar_init(bar_dqs_ready(w), 128);
+      mbar_init(bar_dqs_free(w), 1);
+    }
     *abort_flag = 0;
     mbar_init_fence();
   }
@@ -202,6 +216,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       tma_prefetch_map(&tmV);
       tma_prefetch_map(&tmQ);
       tma_prefetch_map(&tmDO);
+      tma_prefetch_map(&tmDQ);
       const uint64_t once = l2_policy_evict_first();  // K, V: read by one unit
       const uint64_t keep = l2_policy_evict_last();   // Q, dO: read by every K/V tile of the head
       int slot = 0;
@@ -414,7 +429,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 
     // dQ^T of global step `step` (head pend_bh, rows pend_q0 + [32wg, 32wg+32))
     // from TMEM into the fp32 accumulator: this thread holds head-dim index
-    // rr of 32 query rows; the 32 lanes of a warp add 32 consecutive floats.
+    // rr of 32 query rows. The warpgroup writes them into its 32 x D staging
+    // rows (row-major, the accumulator's layout) and its leader thread adds
+    // the block into global memory with one TMA reduce-add; the staging rows
+    // are rewritten once that TMA has read them.
+    const bool leader = (threadIdx.x & 127) == 0;
+    const uint32_t stage_rows = sDQS + static_cast<uint32_t>(wg * 32 * D * 4);
+    uint32_t drains = 0;
     auto drain_dq = [&](uint32_t step) -> bool {
       bool got = wait_bounded(bar_dq_full, step & 1u, wd, kSiteBwdDqFull);
       got = __all_sync(0xffffffffu, got);
@@ -424,14 +445,37 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       if (dq_rows) tmem_ld32x32_wait(tDQ, v);
       tc_fence_before_sync();
       mbar_arrive(bar_dq_free);
+      if (drains > 0) {
+        if (leader) {
+          bulk_wait_read_all();
+          mbar_arrive(bar_dqs_free(wg));
+        }
+        bool fr = wait_bounded(bar_dqs_free(wg), (drains - 1) & 1u, wd, kSiteBwdDqsFree);
+        fr = __all_sync(0xffffffffu, fr);
+        if (!fr) return false;
+      }
       if (dq_rows) {
-        const int q0 = pend_q0 + 32 * wg;
-        const int rows = min(32, p.N - q0);
-        float* dst = p.dq_acc + (static_cast<size_t>(pend_bh) * p.N + q0) * D + rr;
 #pragma unroll
         for (int i = 0; i < 32; ++i)
-          if (i < rows) atomicAdd(dst + static_cast<size_t>(i) * D, __uint_as_float(v[i]));
+          asm volatile("st.shared.f32 [%0], %1;" ::"r"(stage_rows + static_cast<uint32_t>((i * D + rr) * 4)),
+                       "f"(__uint_as_float(v[i]))
+                       : "memory");
       }
+      fence_proxy_async_shared();
+      mbar_arrive(bar_dqs_ready(wg));
+      if (quarter == 0) {  // the leader's warp waits as a whole, so its lanes agree on the outcome
+        bool rd = wait_bounded(bar_dqs_ready(wg), drains & 1u, wd, kSiteBwdDqsReady);
+        rd = __all_sync(0xffffffffu, rd);
+        if (!rd) return false;
+      }
+      if (leader) {
+        const int q0 = pend_q0 + 32 * wg;
+        if (q0 < p.N) {  // rows past N are outside the map and skipped
+          tma_reduce_add_3d(&tmDQ, stage_rows, 0, q0, pend_bh);
+          bulk_commit_group();
+        }
+      }
+      ++drains;
       return true;
     };
 
@@ -541,8 +585,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       }
       ++units;
     }
-    // the last step's dQ^T
+    // the last step's dQ^T; the staged blocks must be read (and added)
+    // before the CTA's shared memory goes away
     if (ok && g > 0) drain_dq(g - 1);
+    if (leader) bulk_wait_all();
   }
 
   tc_fence_before_sync();
@@ -555,12 +601,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 
 template <int D, bool kBf16, bool kCausal>
 cudaError_t launch_bwd(const CUtensorMap& k, const CUtensorMap& v, const CUtensorMap& q, const CUtensorMap& dout,
-                       const BwdParams& p, int grid, cudaStream_t stream) {
+                       const CUtensorMap& dq_acc, const BwdParams& p, int grid, cudaStream_t stream) {
   auto kern = fa2_bwd_kernel<D, kBf16, kCausal>;
   const int smem = BwdLayout<D>::kSmemBytes;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  kern<<<grid, kBwdThreads, smem, stream>>>(k, v, q, dout, p);
+  kern<<<grid, kBwdThreads, smem, stream>>>(k, v, q, dout, dq_acc, p);
   return cudaGetLastError();
 }
 

@@ -43,7 +43,8 @@ constexpr int kBwdRows = 64;        // query rows per backward step
 struct BwdParams {
   void* dk;                 // [B,H,N,D] 16-bit outputs
   void* dv;
-  float* dq_acc;            // [B,H,N,D] fp32 dQ accumulator (zeroed by the prologue kernel)
+  float* dq_acc;            // [B,H,N,D] fp32 dQ accumulator (zeroed by the prologue kernel; the
+                            // kernel adds into it through a tensor map)
   const float* lse2;        // [B*H, Npad] LSE * log2(e); +inf for rows >= N
   const float* delta;       // [B*H, Npad] <dO_i, O_i>; 0 for rows >= N
   int* status;              // device watchdog word
@@ -82,11 +83,13 @@ int record_cuda_error(cudaError_t e);
 int current_device_facts(int* sms, int** status);
 bool encode_tile_map(CUtensorMap* map, const void* ptr, int bh, int n, int d, int dtype, unsigned rows);
 unsigned long long watchdog_limit_ns();
+// fp32 [B*H, N, D] map with boxes of `rows` whole rows (D elements), no swizzle.
+bool encode_f32_rows_map(CUtensorMap* map, float* ptr, int bh, int n, int d, unsigned rows);
 bool ranges_overlap(const void* a, size_t na, const void* b, size_t nb);
 
 template <int D, bool kBf16, bool kCausal>
 cudaError_t launch_bwd(const CUtensorMap& k, const CUtensorMap& v, const CUtensorMap& q, const CUtensorMap& dout,
-                       const BwdParams& p, int grid, cudaStream_t stream);
+                       const CUtensorMap& dq_acc, const BwdParams& p, int grid, cudaStream_t stream);
 
 template <int D, bool kBf16, bool kCausal>
 cudaError_t launch_fwd(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v, const Params& p,
