@@ -50,11 +50,14 @@ KERNEL_SOURCES = os.path.join(ROOT, "attention_forward_03_gb300", "csrc")
 # host-memory pipeline and the no-allocation entry point do not change either)
 KERNEL_FILES = ("fa2_kernel.cuh", "fa2_launch.h", "sm103_ptx.cuh", "tmem_io.cuh", "fa2_fwd_d64.cu", "fa2_fwd_d128.cu",
                 "fa2_api.cu")
+# the same for the backward pass (its three kernels and their launch)
+BWD_KERNEL_FILES = ("fa2_bwd_kernel.cuh", "fa2_kernel.cuh", "fa2_launch.h", "sm103_ptx.cuh", "tmem_io.cuh",
+                    "fa2_bwd_d64.cu", "fa2_bwd_d128.cu", "fa2_bwd_api.cu", "fa2_api.cu")
 
 
-def kernel_source_hash() -> str:
+def kernel_source_hash(files=KERNEL_FILES) -> str:
     h = hashlib.sha256()
-    for f in sorted(KERNEL_FILES):
+    for f in sorted(files):
         with open(os.path.join(KERNEL_SOURCES, f), "rb") as fh:
             h.update(f.encode() + b"\0" + fh.read())
     return h.hexdigest()[:16]
@@ -70,15 +73,16 @@ def load_peaks():
         return dict(FALLBACK_PEAKS), "fallback"
 
 
-def traffic_per_launch(workload_name: str):
-    """DRAM bytes per launch from a committed ncu capture, if it matches the current kernel source."""
+def traffic_per_launch(workload_name: str, files=KERNEL_FILES):
+    """DRAM bytes per launch from a committed ncu capture, if it matches the current kernel source.
+    Backward entries are keyed "bwd:<workload>"."""
     try:
         with open(PROFILE_TRAFFIC) as fh:
             t = json.load(fh)
     except (OSError, ValueError):
         return None
     entry = t.get(workload_name)
-    if not entry or entry.get("kernel_source_hash") != kernel_source_hash():
+    if not entry or entry.get("kernel_source_hash") != kernel_source_hash(files):
         return None
     return entry.get("dram_bytes_per_launch")
 
@@ -518,7 +522,9 @@ def run_gb300_bwd(args, w, rank, world, local):
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                      "frac": achieved / peak, "peak_source": f"{peak_src} bf16 dense (burst)",
                      "timed": "the whole fa2_bwd call (prologue, backward kernel and dQ conversion)",
-                     "traffic": None, "algorithmic_bytes": set_bytes,
+                     "traffic": traffic_per_launch("bwd:" + w.name, BWD_KERNEL_FILES),
+                     "traffic_of": "fa2_bwd_kernel (97.5% of the call's device time)",
+                     "algorithmic_bytes": set_bytes,
                      "achieved_hbm_gbs": set_bytes / per_call / 1e9},
         "gpu_launches": 3 * args.steps,
         "clocks": clock_info,
