@@ -79,7 +79,8 @@ EncodeTiledFn encode_fn() {
 }
 
 // [B*H, N, D] view of a [B,H,N,D] tensor; `rows` rows x 64 elements per box,
-// 128-byte swizzle; rows past N read as zeros.
+// 128-byte swizzle; rows past N, and columns past D (D = 32, or the second
+// panel at D = 96), read as zeros.
 bool make_rows_map(CUtensorMap* map, const void* ptr, int bh, int n, int d, int dtype, unsigned rows) {
   EncodeTiledFn enc = encode_fn();
   if (!enc) return false;
@@ -106,14 +107,20 @@ bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
 using LaunchFn = cudaError_t (*)(const CUtensorMap&, const CUtensorMap&, const CUtensorMap&, const Params&, int,
                                  cudaStream_t);
 
+template <int D>
+LaunchFn pick_d(bool bf, bool c) {
+  if (bf) return c ? launch_fwd<D, true, true> : launch_fwd<D, true, false>;
+  return c ? launch_fwd<D, false, true> : launch_fwd<D, false, false>;
+}
+
 LaunchFn pick(int d, int dtype, int causal) {
   const bool bf = dtype == FA2_BF16, c = causal != 0;
-  if (d == 64) {
-    if (bf) return c ? launch_fwd<64, true, true> : launch_fwd<64, true, false>;
-    return c ? launch_fwd<64, false, true> : launch_fwd<64, false, false>;
+  switch (d) {
+    case 32: return pick_d<32>(bf, c);
+    case 64: return pick_d<64>(bf, c);
+    case 96: return pick_d<96>(bf, c);
+    default: return pick_d<128>(bf, c);
   }
-  if (bf) return c ? launch_fwd<128, true, true> : launch_fwd<128, true, false>;
-  return c ? launch_fwd<128, false, true> : launch_fwd<128, false, false>;
 }
 
 }  // namespace
@@ -142,7 +149,7 @@ unsigned long long next_epoch() {
 int launch(const void* Q, const void* K, const void* V, void* O, float* LSE, int B, int H, int N, int D,
            float scale, int is_causal, int dtype, void* workspace, size_t workspace_bytes, cudaStream_t stream) {
   if (B < 0 || H < 0 || N < 0) return FA2_ERR_INVALID_ARG;
-  if (D != 64 && D != 128) return FA2_ERR_UNSUPPORTED;
+  if (!fwd_head_dim_ok(D)) return FA2_ERR_UNSUPPORTED;
   if (dtype != FA2_F16 && dtype != FA2_BF16) return FA2_ERR_UNSUPPORTED;
   if (!std::isfinite(scale) || !(scale > 0.f)) return FA2_ERR_INVALID_ARG;
   if (B == 0 || H == 0 || N == 0) return FA2_OK;
@@ -276,7 +283,7 @@ extern "C" int fa2_fwd(const void* Q, const void* K, const void* V, void* O, flo
 
 extern "C" int fa2_fwd_workspace_bytes(int D, size_t* bytes) {
   if (!bytes) return FA2_ERR_INVALID_ARG;
-  if (D != 64 && D != 128) return FA2_ERR_UNSUPPORTED;
+  if (!fwd_head_dim_ok(D)) return FA2_ERR_UNSUPPORTED;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return record_cuda(e);

@@ -1,0 +1,13 @@
+// Instantiations of the sm_103a forward kernel for head dimension 96 (in the layout of 128).
+#include "fa2_kernel.cuh"
+
+namespace fa2 {
+template cudaError_t launch_fwd<96, false, false>(const CUtensorMap&, const CUtensorMap&, const CUtensorMap&,
+                                                  const Params&, int, cudaStream_t);
+template cudaError_t launch_fwd<96, false, true>(const CUtensorMap&, const CUtensorMap&, const CUtensorMap&,
+                                                 const Params&, int, cudaStream_t);
+template cudaError_t launch_fwd<96, true, false>(const CUtensorMap&, const CUtensorMap&, const CUtensorMap&,
+                                                 const Params&, int, cudaStream_t);
+template cudaError_t launch_fwd<96, true, true>(const CUtensorMap&, const CUtensorMap&, const CUtensorMap&,
+                                                const Params&, int, cudaStream_t);
+}  // namespace fa2

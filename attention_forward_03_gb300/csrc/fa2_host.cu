@@ -49,7 +49,7 @@ struct BufferLayout {
 
 int buffer_layout(int B, int H, int N, int D, BufferLayout* L) {
   if (B < 0 || H < 0 || N < 0) return FA2_ERR_INVALID_ARG;
-  if (D != 64 && D != 128) return FA2_ERR_UNSUPPORTED;
+  if (!fa2::fwd_head_dim_ok(D)) return FA2_ERR_UNSUPPORTED;
   const int64_t bh = static_cast<int64_t>(B) * H;
   if (bh > INT32_MAX) return FA2_ERR_INVALID_ARG;
   const size_t t = round256(static_cast<size_t>(bh) * N * D * 2);
@@ -95,7 +95,7 @@ extern "C" int fa2_fwd_host(const void* Q, const void* K, const void* V, void* O
                             int D, float scale, int is_causal, int dtype, int heads_per_chunk, int balanced,
                             void* dev_buffer, size_t dev_bytes, struct CUstream_st* stream_handle) {
   if (B < 0 || H < 0 || N < 0 || heads_per_chunk < 0) return FA2_ERR_INVALID_ARG;
-  if (D != 64 && D != 128) return FA2_ERR_UNSUPPORTED;
+  if (!fa2::fwd_head_dim_ok(D)) return FA2_ERR_UNSUPPORTED;
   if (dtype != FA2_F16 && dtype != FA2_BF16) return FA2_ERR_UNSUPPORTED;
   if (!std::isfinite(scale) || !(scale > 0.f)) return FA2_ERR_INVALID_ARG;
   if (B == 0 || H == 0 || N == 0) return FA2_OK;

@@ -15,22 +15,25 @@
 //   work unit  = 256 query rows of one (batch, head): two 128-row sub-tiles.
 //   warps 0-3  softmax warpgroup for sub-tile 0 (thread = query row = TMEM lane)
 //   warps 4-7  softmax warpgroup for sub-tile 1
-//   warps 8-9  tcgen05 MMA issuers (one thread each): at head dim 128 warp 8
-//              issues every S and warp 9 every P.V; at head dim 64 warp 8 + t
-//              issues both of sub-tile t. Warp 8 also owns the TMEM
+//   warps 8-9  tcgen05 MMA issuers (one thread each): at head dim 96 and 128
+//              warp 8 issues every S and warp 9 every P.V; at head dim 32
+//              and 64 warp 8 + t issues both of sub-tile t. Warp 8 also owns the TMEM
 //              allocation. The issuers and the producer sleep briefly between
 //              barrier polls, leaving issue slots to the softmax warps that
 //              share their SM sub-partitions.
 //   warp  10   TMA producer (one thread); warp 11 idle. Warps 8-11 form the
 //              third warpgroup, which gives registers to the softmax ones.
+// Head dims 32 and 96 run in the layout of 64 and 128 (Dp below): their
+// tiles are loaded 64 columns wide, the columns past D filled with zeros by
+// the copy engine, and Q.K^T takes only the D/16 steps that cover real data.
 // Tensor memory (512 columns x 128 lanes of 32 bits):
 //   [128t, 128t+128)      S of sub-tile t (fp32 scores)
-//   [256+tD, 256+tD+D)    O accumulator of sub-tile t (fp32)
-//   [384+64t, 448+64t)    D = 64 only: P of sub-tile t (16-bit pairs)
-// Shared memory: Q (2 sub-tiles, resident for the segment), at D = 128 P
+//   [256+tDp, 256+tDp+D)  O accumulator of sub-tile t (fp32)
+//   [384+64t, 448+64t)    Dp = 64 only: P of sub-tile t (16-bit pairs)
+// Shared memory: Q (2 sub-tiles, resident for the segment), at Dp = 128 P
 // (2 sub-tiles, 16-bit), and a ring of K/V tiles; all 128-byte swizzled in
 // 64-element-wide panels, the operand layout the MMAs read (TMA writes Q/K/V
-// that way; the softmax threads write P that way). At D = 64 the O
+// that way; the softmax threads write P that way). At Dp = 64 the O
 // accumulators leave room for P in tensor memory, where the P.V MMA reads it
 // as its A operand (the faster form of the instruction) and its shared
 // memory goes to a deeper K/V ring.
@@ -107,10 +110,17 @@ enum : int {
 
 template <int D>
 struct Layout {
-  static constexpr int kPanels = D / 64;
-  static constexpr int kTileBytes = kPanels * kPanelBytes;  // 128 rows x D (Q sub-tile, K or V tile)
-  static constexpr bool kPInTmem = (D == 64);
-  static constexpr int kStages = (D == 128) ? 3 : 12;
+  static_assert(fwd_head_dim_ok(D), "head dimension");
+  // D = 32 and 96 use the tiles of 64 and 128 (their padded columns are zero)
+  static constexpr int kPanels = (D + 63) / 64;
+  static constexpr int kDp = kPanels * 64;                    // padded head dimension
+  static constexpr int kTileBytes = kPanels * kPanelBytes;  // 128 rows x kDp (Q sub-tile, K or V tile)
+  static constexpr bool kPInTmem = (kPanels == 1);
+  static constexpr int kStages = (kPanels == 2) ? 3 : 12;
+  // N of the P.V product = O columns accumulated. At D = 32 it stays 64: a
+  // 32-wide B operand would cover half of a 128-byte swizzle row, a form the
+  // operand layouts do not describe; the extra columns are P times zero.
+  static constexpr int kNpv = (D == 32) ? 64 : D;
   static constexpr int kQBytes = kSubTiles * kTileBytes;
   static constexpr int kPOffset = kQBytes;
   static constexpr int kRingOffset = kPOffset + (kPInTmem ? 0 : kSubTiles * kPTileBytes);
@@ -120,9 +130,9 @@ struct Layout {
   static constexpr int kNumBars = 2 + 3 * kStages + 2 * 7;
   static constexpr int kMiscOffset = kBarOffset + kNumBars * 8;
   static constexpr int kSmemBytes = kMiscOffset + 16 + 1024;  // + slack for 1 KB alignment
-  static constexpr uint32_t kColO = 2 * kKeys;                 // O0 at 256, O1 at 256 + D
-  static constexpr uint32_t kColP = kColO + 2 * D;              // D = 64: P0 at 384, P1 at 448
-  static_assert(kColO + 2 * D + (kPInTmem ? 2 * kKeys / 2 : 0) <= kTmemCols, "TMEM budget");
+  static constexpr uint32_t kColO = 2 * kKeys;                 // O0 at 256, O1 at 256 + kDp
+  static constexpr uint32_t kColP = kColO + 2 * kDp;            // kDp = 64: P0 at 384, P1 at 448
+  static_assert(kColO + 2 * kDp + (kPInTmem ? 2 * kKeys / 2 : 0) <= kTmemCols, "TMEM budget");
   static_assert(kSmemBytes <= 232448, "shared memory budget");
 };
 
@@ -288,7 +298,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   // every P.V) or by sub-tile (each thread S and P.V of one sub-tile). Both
   // measured (with the issuers sleeping between polls): by type is 10-15 %
   // faster at head dim 128, by sub-tile 2-6 % faster at head dim 64.
-  constexpr bool kTypeSplit = D == 128;
+  constexpr bool kTypeSplit = L::kPanels == 2;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   const uint32_t raw = smem_addr(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
@@ -427,7 +437,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (lane == 0) {
         const int me = warp - kMmaWarp;  // split by type: 0 issues every S, 1 every P.V; else sub-tile me
         constexpr uint32_t idesc_s = make_idesc_f16(kBf16, kKeys, false);
-        constexpr uint32_t idesc_o = make_idesc_f16(kBf16, D, true);
+        constexpr uint32_t idesc_o = make_idesc_f16(kBf16, L::kNpv, true);
         // Descriptor low words advance by compile-time offsets (the start
         // address field never carries: shared memory stays below 256 KB);
         // the high words are constants.
@@ -445,14 +455,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             mma_ss_w(dt, qa + off, kHi, ka + off, kHi, idesc_s, kk > 0 ? 1u : 0u);
           }
         };
-        // O_t (+)= P_t V : P (K-major, shared memory; D = 64: tensor memory)
+        // O_t (+)= P_t V : P (K-major, shared memory; Dp = 64: tensor memory)
         // and V (MN-major, shared memory), 8 steps of 16 keys.
         auto issue_pv = [&](int t, int slot, bool acc) {
           const uint32_t p_lo = desc_lo_sw128(sP, 16);
           const uint32_t ring_lo_v = desc_lo_sw128(sRing, kPanelBytes);  // V: 64-column panels 16 KB apart
           const uint32_t pa = p_lo + static_cast<uint32_t>((t * kPTileBytes) >> 4);
           const uint32_t va = ring_lo_v + static_cast<uint32_t>(slot * (L::kTileBytes >> 4));
-          const uint32_t dt = tmem + L::kColO + static_cast<uint32_t>(t * D);
+          const uint32_t dt = tmem + L::kColO + static_cast<uint32_t>(t * L::kDp);
           const uint32_t pt = tmem + L::kColP + static_cast<uint32_t>(t * (kKeys / 2));
 #pragma unroll
           for (int kk = 0; kk < kKeys / 16; ++kk) {
@@ -599,7 +609,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int rr = wr * 32 + lane;           // row within the sub-tile
     const uint32_t lane_off = static_cast<uint32_t>(wr * 32) << 16;
     const uint32_t tS = tmem + lane_off + static_cast<uint32_t>(t * kKeys);
-    const uint32_t tO = tmem + lane_off + L::kColO + static_cast<uint32_t>(t * D);
+    const uint32_t tO = tmem + lane_off + L::kColO + static_cast<uint32_t>(t * L::kDp);
     const uint32_t bar_s = bar_s_full0 + 8 * t;
     const uint32_t bar_sf = bar_s_free0 + 8 * t;
     const uint32_t bar_p = bar_p_full0 + 8 * t;

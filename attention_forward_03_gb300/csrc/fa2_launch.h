@@ -1,6 +1,7 @@
 // Host-visible pieces of the forward and backward kernels: tile constants,
 // the parameter blocks, and the launcher templates (instantiated in
-// fa2_fwd_d64.cu, fa2_fwd_d128.cu, fa2_bwd_d64.cu and fa2_bwd_d128.cu).
+// fa2_fwd_d32.cu, fa2_fwd_d64.cu, fa2_fwd_d96.cu, fa2_fwd_d128.cu,
+// fa2_bwd_d64.cu and fa2_bwd_d128.cu).
 #pragma once
 #include <cuda.h>
 #include <cuda_runtime.h>
@@ -12,6 +13,12 @@ constexpr int kRows = 128;          // query rows per sub-tile (= TMEM lanes)
 constexpr int kSubTiles = 2;        // sub-tiles per work unit
 constexpr int kUnitRows = kRows * kSubTiles;
 constexpr int kKeys = 128;          // keys per K/V tile
+
+// Head dimensions of the forward kernel. 64 and 128 are native; 32 and 96
+// run in the layout of the next multiple of 64, the padded columns of every
+// Q/K/V tile read as zeros (the copy engine's out-of-bounds fill), so they
+// add nothing to Q.K^T and P.V.
+constexpr bool fwd_head_dim_ok(int d) { return d == 32 || d == 64 || d == 96 || d == 128; }
 
 struct Params {
   void* o;                  // [B,H,N,D] 16-bit

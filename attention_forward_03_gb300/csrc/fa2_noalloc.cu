@@ -12,7 +12,7 @@
 namespace {
 
 // Largest configuration the static scratch covers: 160 CTAs (one per SM) at
-// head dimension 128 (head dimension 64 needs less).
+// head dimension 128 (smaller head dimensions need less).
 constexpr int kMaxCtas = 160;
 constexpr size_t kScratchBytes = fa2::stream_k_workspace_bytes(kMaxCtas, 128);
 constexpr int kMaxDevices = 64;
@@ -37,7 +37,7 @@ extern "C" int fa2_fwd_noalloc(const void* Q, const void* K, const void* V, void
                                int N, int D, float scale, int is_causal, int dtype, struct CUstream_st* stream) {
   // the same argument checks fa2_fwd makes before it touches the device
   if (B < 0 || H < 0 || N < 0) return FA2_ERR_INVALID_ARG;
-  if (D != 64 && D != 128) return FA2_ERR_UNSUPPORTED;
+  if (!fa2::fwd_head_dim_ok(D)) return FA2_ERR_UNSUPPORTED;
   if (dtype != FA2_F16 && dtype != FA2_BF16) return FA2_ERR_UNSUPPORTED;
   if (B == 0 || H == 0 || N == 0) return FA2_OK;
 

@@ -39,7 +39,7 @@ struct CUstream_st; /* the same type as cudaStream_t / CUstream */
 /* status codes (0 = success, negative = error) */
 #define FA2_OK 0
 #define FA2_ERR_INVALID_ARG (-1) /* null pointer, negative size, bad scale, overlapping O/LSE/inputs, size overflow */
-#define FA2_ERR_UNSUPPORTED (-2) /* head dim not 64 or 128, unknown dtype, device is not sm_103 */
+#define FA2_ERR_UNSUPPORTED (-2) /* head dim not supported, unknown dtype, device is not sm_103 */
 #define FA2_ERR_ALIGN (-3)       /* a tensor pointer is not 16-byte aligned */
 #define FA2_ERR_CUDA (-4)        /* a CUDA runtime/driver call failed (see fa2_last_cuda_error) */
 #define FA2_ERR_TIMEOUT (-5)     /* the device watchdog fired (reported by fa2_device_status) */
@@ -58,7 +58,11 @@ struct CUstream_st; /* the same type as cudaStream_t / CUstream */
  * B, H, N : batch, heads, sequence length (queries and keys), each >= 0. If
  *           any is 0 the call does nothing and returns FA2_OK (pointers may
  *           then be NULL).
- * D       : head dimension; 64 or 128.
+ * D       : head dimension; 32, 64, 96 or 128. 64 and 128 are the native
+ *           tile widths; 32 and 96 run in the tiles of 64 and 128, whose
+ *           columns past D the kernel reads as zeros. These are the head
+ *           dims the split-Q launcher of "FlashAttention-2 MMA 代码学习"
+ *           dispatches (its host function at the end of the page).
  * scale   : multiplier on Q.K; finite and > 0 (the usual value is 1/sqrt(D)).
  * is_causal: nonzero keeps only keys j <= i for query i.
  * dtype   : FA2_F16 or FA2_BF16.
@@ -78,7 +82,7 @@ int fa2_fwd(const void* Q, const void* K, const void* V, void* O, float* LSE,
 
 /*
  * fa2_fwd_workspace_bytes — bytes of device workspace fa2_fwd_ws needs on the
- * current device for head dimension D (64 or 128): one fp32 partial result of
+ * current device for head dimension D (32, 64, 96 or 128): one fp32 partial result of
  * a 256-row work unit per SM plus one 8-byte flag per 128-row half. It does
  * not depend on B, H or N. Returns FA2_OK, FA2_ERR_INVALID_ARG (bytes NULL),
  * FA2_ERR_UNSUPPORTED (D) or FA2_ERR_CUDA.
@@ -119,7 +123,7 @@ int fa2_fwd_ws(const void* Q, const void* K, const void* V, void* O, float* LSE,
  *
  * Its scratch is one static device array of this library, 21,465,600 bytes,
  * held on every GPU that loads the library until the process exits. It
- * covers devices of up to 160 SMs at head dimension 64 or 128; a device with
+ * covers devices of up to 160 SMs at every supported head dimension; a device with
  * more SMs is refused with FA2_ERR_UNSUPPORTED.
  * The first call on each device looks up the array's device address (with
  * that device current); make that first call before any stream capture.
@@ -220,7 +224,7 @@ int fa2_bwd_workspace_bytes(int B, int H, int N, int D, size_t* bytes);
  *           rounded to nearest-even. Must not overlap each other, an input
  *           or the workspace.
  * B, H, N, D, scale, is_causal, dtype: as for fa2_fwd (the same values the
- *           forward was called with).
+ *           forward was called with), except that D is 64 or 128 only.
  * workspace: device memory of at least fa2_bwd_workspace_bytes(B, H, N, D)
  *           bytes, 256-byte aligned, owned by the caller. Its contents on
  *           entry do not matter; it is scratch for the duration of the call

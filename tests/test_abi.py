@@ -70,7 +70,7 @@ def call(lib, **over):
 
 @pytest.mark.parametrize("over,code", [
     (dict(B=-1), -1), (dict(H=-3), -1), (dict(N=-1), -1),
-    (dict(D=96), -2), (dict(D=256), -2), (dict(D=0), -2),
+    (dict(D=48), -2), (dict(D=256), -2), (dict(D=0), -2), (dict(D=16), -2), (dict(D=160), -2),
     (dict(dtype=2), -2), (dict(dtype=-1), -2),
     (dict(scale=0.0), -1), (dict(scale=-0.5), -1), (dict(scale=float("nan")), -1), (dict(scale=float("inf")), -1),
     (dict(Q=None), -1), (dict(K=None), -1), (dict(V=None), -1), (dict(O=None), -1), (dict(LSE=None), -1),
@@ -93,10 +93,10 @@ def call_ws(lib, ws, ws_bytes, **over):
 def test_workspace_variant_checks_its_arguments(lib):
     assert call_ws(lib, A * 80 + 8, 1 << 20) == lib.FA2_ERR_ALIGN           # misaligned workspace
     assert call_ws(lib, A * 48 + 256, 1 << 20) == lib.FA2_ERR_INVALID_ARG   # workspace overlaps O
-    assert call_ws(lib, A * 80, 1 << 20, D=96) == lib.FA2_ERR_UNSUPPORTED
+    assert call_ws(lib, A * 80, 1 << 20, D=48) == lib.FA2_ERR_UNSUPPORTED
     assert call_ws(lib, None, 0, B=0) == lib.FA2_OK
     n = ctypes.c_size_t(0)
-    assert lib.library().fa2_fwd_workspace_bytes(96, ctypes.byref(n)) == lib.FA2_ERR_UNSUPPORTED
+    assert lib.library().fa2_fwd_workspace_bytes(256, ctypes.byref(n)) == lib.FA2_ERR_UNSUPPORTED
     assert lib.library().fa2_fwd_workspace_bytes(64, None) == lib.FA2_ERR_INVALID_ARG
 
 
@@ -106,7 +106,7 @@ def test_no_alloc_entry_point_checks_arguments_first(lib):
     args = lambda **o: [dict(a, **o)[x] for x in ("Q", "K", "V", "O", "LSE", "B", "H", "N", "D", "scale",
                                                    "is_causal", "dtype", "stream")]  # noqa: E731
     assert so.fa2_fwd_noalloc(*args(B=-1)) == lib.FA2_ERR_INVALID_ARG
-    assert so.fa2_fwd_noalloc(*args(D=96)) == lib.FA2_ERR_UNSUPPORTED
+    assert so.fa2_fwd_noalloc(*args(D=80)) == lib.FA2_ERR_UNSUPPORTED
     assert so.fa2_fwd_noalloc(*args(dtype=5)) == lib.FA2_ERR_UNSUPPORTED
     assert so.fa2_fwd_noalloc(*args(N=0)) == lib.FA2_OK
 
@@ -123,7 +123,7 @@ def test_host_entry_point_checks_arguments_first(lib):
                                                 "dtype", "hpc", "balanced", "buf", "nbuf", "stream")])
     assert host(B=-1) == lib.FA2_ERR_INVALID_ARG
     assert host(hpc=-2) == lib.FA2_ERR_INVALID_ARG
-    assert host(D=96) == lib.FA2_ERR_UNSUPPORTED
+    assert host(D=48) == lib.FA2_ERR_UNSUPPORTED
     assert host(dtype=3) == lib.FA2_ERR_UNSUPPORTED
     assert host(scale=0.0) == lib.FA2_ERR_INVALID_ARG
     assert host(Q=None) == lib.FA2_ERR_INVALID_ARG
@@ -134,7 +134,7 @@ def test_host_entry_point_checks_arguments_first(lib):
     assert host(B=0) == lib.FA2_OK and host(N=0, Q=None, buf=None) == lib.FA2_OK
     n = ctypes.c_size_t(0)
     assert so.fa2_fwd_host_buffer_bytes(1, 2, 64, 64, None) == lib.FA2_ERR_INVALID_ARG
-    assert so.fa2_fwd_host_buffer_bytes(1, 2, 64, 96, ctypes.byref(n)) == lib.FA2_ERR_UNSUPPORTED
+    assert so.fa2_fwd_host_buffer_bytes(1, 2, 64, 256, ctypes.byref(n)) == lib.FA2_ERR_UNSUPPORTED
     assert so.fa2_fwd_host_buffer_bytes(-1, 2, 64, 64, ctypes.byref(n)) == lib.FA2_ERR_INVALID_ARG
 
 
@@ -164,6 +164,10 @@ def test_empty_problem_is_a_no_op(lib, over):
 @pytest.mark.skipif(torch.cuda.is_available(), reason="only meaningful on a host without a GPU")
 def test_valid_call_without_a_gpu_fails_loudly(lib):
     assert call(lib) == lib.FA2_ERR_CUDA
+    # every supported head dimension passes the argument checks and reaches the device query
+    for d in (32, 64, 96, 128):
+        assert call(lib, D=d) == lib.FA2_ERR_CUDA
+        assert call_ws(lib, A * 80, 1 << 24, D=d) == lib.FA2_ERR_CUDA
     assert lib.library().fa2_last_cuda_error().decode() != ""
     with pytest.raises(lib.Fa2Error):
         lib._check(call(lib), "fa2_fwd")

@@ -81,6 +81,28 @@ def test_edge_shapes_every_element(fa2, oracle_mod, N, D, dtype, causal, schedul
     compare(fa2, oracle_mod, w, schedule=schedule)
 
 
+EDGE_N_PADDED = [1, 63, 129, 256, 257, 1000]
+
+
+@pytest.mark.parametrize("N", EDGE_N_PADDED)
+@pytest.mark.parametrize("D", [32, 96])
+@pytest.mark.parametrize("dtype", ["f16", "bf16"])
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("schedule", SCHEDULES)
+def test_padded_head_dims_every_element(fa2, oracle_mod, N, D, dtype, causal, schedule):
+    # Head dims 32 and 96 run in the tiles of 64 and 128 with zero-filled
+    # columns; a column past D read from memory (the next row's first
+    # elements) instead of as zero would change every score of its row.
+    w = workloads.custom(2, 3, N, D, dtype, causal, seed=N * 11 + D)
+    compare(fa2, oracle_mod, w, schedule=schedule)
+
+
+@pytest.mark.parametrize("schedule", SCHEDULES)
+@pytest.mark.parametrize("name", ["pages_d32", "target_d96"])
+def test_padded_head_dim_workloads_full_size(fa2, oracle_mod, name, schedule):
+    compare(fa2, oracle_mod, workloads.WORKLOADS[name], sample=600, schedule=schedule)
+
+
 @pytest.mark.parametrize("schedule", SCHEDULES)
 def test_ragged_tail_does_not_read_the_next_head(fa2, oracle_mod, schedule):
     # Rows past N of one head must read as zeros, never as the next head's rows.

@@ -19,6 +19,10 @@ Q/K/V i.i.d. normal, cast to the 16-bit type with round-to-nearest-even):
   target_f16  same shape as target in fp16, seed 5
   target_b4   B=4 H=16 N=8192 D=128 bf16 non-causal, seed 6 (supplementary: more
               units per SM, less wave-quantisation tail)
+  pages_d32   B=1 H=8 N=8192 D=32 fp16 non-causal, seed 7 (the pages' shape at
+              the smallest head dimension the tiling_qk page lists)
+  target_d96  B=1 H=8 N=8192 D=96 bf16 non-causal, seed 8 (the target shape at
+              head dimension 96)
 
 Scale is 1/sqrt(D) everywhere. Draw order: Q, then K, then V, each
 ``torch.randn(shape, dtype=float32, generator=g) * sigma`` from a CPU
@@ -67,6 +71,8 @@ WORKLOADS = {
     "target": Workload("target", 1, 8, 8192, 128, "bf16", False, 5),
     "target_f16": Workload("target_f16", 1, 8, 8192, 128, "f16", False, 5),
     "target_b4": Workload("target_b4", 4, 16, 8192, 128, "bf16", False, 6),
+    "pages_d32": Workload("pages_d32", 1, 8, 8192, 32, "f16", False, 7),
+    "target_d96": Workload("target_d96", 1, 8, 8192, 96, "bf16", False, 8),
 }
 
 # The five workloads the parity contract names, in their stated order.
