@@ -172,20 +172,27 @@ def workspace_for(device, D: int):
     return ws
 
 
-UNIT_ROWS = 256  # query rows per work unit of the kernel
+UNIT_ROWS = 256  # query rows per work unit of the kernel (head dims up to 128)
 KV_TILE = 128    # keys per K/V tile
 SPLIT_COST_STEPS = 4  # measured cost of a split unit (partial write, merge), in K/V-tile steps
 
 
-def steps_per_head(N: int, is_causal: bool) -> int:
-    """K/V-tile steps (one 256-row unit against one 128-key tile) of one head."""
-    n_qt, nkv = -(-N // UNIT_ROWS), -(-N // KV_TILE)
+def unit_rows(D: int = 128) -> int:
+    """Query rows per work unit: 256 (two 128-row sub-tiles), or 128 at head dim 256."""
+    return KV_TILE if D == 256 else UNIT_ROWS
+
+
+def steps_per_head(N: int, is_causal: bool, D: int = 128) -> int:
+    """K/V-tile steps (one work unit against one 128-key tile) of one head."""
+    rows = unit_rows(D)
+    sub = rows // KV_TILE
+    n_qt, nkv = -(-N // rows), -(-N // KV_TILE)
     if not is_causal:
         return n_qt * nkv
-    return sum(min(2 * qt + 2, nkv) for qt in range(n_qt))
+    return sum(min(sub * (qt + 1), nkv) for qt in range(n_qt))
 
 
-def choose_schedule(B: int, H: int, N: int, is_causal: bool, sms: int) -> str:
+def choose_schedule(B: int, H: int, N: int, is_causal: bool, sms: int, D: int = 128) -> str:
     """Pick the kernel schedule for a problem (a choice between two C entry points).
 
     Cost in K/V-tile steps of the busiest SM: the round schedule (fa2_fwd)
@@ -195,7 +202,7 @@ def choose_schedule(B: int, H: int, N: int, is_causal: bool, sms: int) -> str:
     cheaper. Causal work stays on the round schedule, whose heaviest-first
     zig-zag measured faster than the split on every causal workload.
     """
-    units = B * H * -(-N // UNIT_ROWS)
+    units = B * H * -(-N // unit_rows(D))
     if is_causal or units == 0:
         return "units"
     nkv = -(-N // KV_TILE)
@@ -231,7 +238,7 @@ def attention_forward(q, k, v, scale: float | None = None, is_causal: bool = Fal
     B, H, N, D = q.shape
     if schedule == "auto":
         sms = torch.cuda.get_device_properties(q.device).multi_processor_count
-        schedule = choose_schedule(B, H, N, is_causal, sms)
+        schedule = choose_schedule(B, H, N, is_causal, sms, D)
     if scale is None:
         scale = 1.0 / math.sqrt(D)
     if out is None:
@@ -261,7 +268,7 @@ HOST_CHUNKS = 16           # target number of head chunks of attention_forward_h
 HOST_CHUNK_MIN_STEPS = 4096  # K/V-tile steps a chunk needs to keep the GPU busy (~27 per SM)
 
 
-def host_chunk_heads(B: int, H: int, N: int, is_causal: bool, sms: int) -> int:
+def host_chunk_heads(B: int, H: int, N: int, is_causal: bool, sms: int, D: int = 128) -> int:
     """Heads per chunk of the host-memory pipeline.
 
     The copies are the bottleneck end to end, so the pipeline wants many
@@ -274,9 +281,9 @@ def host_chunk_heads(B: int, H: int, N: int, is_causal: bool, sms: int) -> int:
     bh = B * H
     if bh <= 0:
         return 1
-    hpc = max(-(-bh // HOST_CHUNKS), -(-HOST_CHUNK_MIN_STEPS // max(1, steps_per_head(N, is_causal))))
+    hpc = max(-(-bh // HOST_CHUNKS), -(-HOST_CHUNK_MIN_STEPS // max(1, steps_per_head(N, is_causal, D))))
     if is_causal:
-        hpc = max(hpc, -(-sms // -(-N // UNIT_ROWS)))
+        hpc = max(hpc, -(-sms // -(-N // unit_rows(D))))
     return max(1, min(hpc, bh))
 
 
@@ -310,11 +317,11 @@ def attention_forward_host(q, k, v, scale: float | None = None, is_causal: bool 
     B, H, N, D = q.shape
     dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
     sms = torch.cuda.get_device_properties(dev).multi_processor_count
-    hpc = host_chunk_heads(B, H, N, is_causal, sms) if heads_per_chunk is None else int(heads_per_chunk)
+    hpc = host_chunk_heads(B, H, N, is_causal, sms, D) if heads_per_chunk is None else int(heads_per_chunk)
     if hpc < 1:
         raise ValueError("heads_per_chunk must be >= 1")
     if schedule == "auto":
-        schedule = choose_schedule(1, min(hpc, B * H), N, is_causal, sms)
+        schedule = choose_schedule(1, min(hpc, B * H), N, is_causal, sms, D)
     if scale is None:
         scale = 1.0 / math.sqrt(D)
     if out is None:

@@ -119,7 +119,10 @@ LaunchFn pick(int d, int dtype, int causal) {
     case 32: return pick_d<32>(bf, c);
     case 64: return pick_d<64>(bf, c);
     case 96: return pick_d<96>(bf, c);
-    default: return pick_d<128>(bf, c);
+    case 128: return pick_d<128>(bf, c);
+    default:
+      if (bf) return c ? launch_fwd_wide<256, true, true> : launch_fwd_wide<256, true, false>;
+      return c ? launch_fwd_wide<256, false, true> : launch_fwd_wide<256, false, false>;
   }
 }
 
@@ -155,7 +158,8 @@ int launch(const void* Q, const void* K, const void* V, void* O, float* LSE, int
   if (B == 0 || H == 0 || N == 0) return FA2_OK;
   if (!Q || !K || !V || !O || !LSE) return FA2_ERR_INVALID_ARG;
   const int64_t bh = static_cast<int64_t>(B) * H;
-  const int64_t n_qt = (static_cast<int64_t>(N) + kUnitRows - 1) / kUnitRows;
+  const int unit_rows = fwd_unit_rows(D), unit_subtiles = fwd_unit_subtiles(D);
+  const int64_t n_qt = (static_cast<int64_t>(N) + unit_rows - 1) / unit_rows;
   if (bh > INT32_MAX || bh * n_qt > INT32_MAX) return FA2_ERR_INVALID_ARG;
   const uintptr_t mis = reinterpret_cast<uintptr_t>(Q) | reinterpret_cast<uintptr_t>(K) |
                         reinterpret_cast<uintptr_t>(V) | reinterpret_cast<uintptr_t>(O) |
@@ -200,10 +204,11 @@ int launch(const void* Q, const void* K, const void* V, void* O, float* LSE, int
   p.scale_log2 = scale * 1.4426950408889634f;
   p.test_withhold = g_test_withhold.exchange(0, std::memory_order_relaxed);
   // K/V-tile steps of one head: non-causal n_qt * nkv_full; causal sum of
-  // min(2qt+2, nkv_full) over the head's query units.
+  // min(T*(qt+1), nkv_full) over the head's query units (T sub-tiles per unit).
   long long per_head = 0;
   if (is_causal) {
-    for (int64_t qt = 0; qt < n_qt; ++qt) per_head += std::min<long long>(2 * qt + 2, p.nkv_full);
+    for (int64_t qt = 0; qt < n_qt; ++qt)
+      per_head += std::min<long long>(unit_subtiles * (qt + 1), p.nkv_full);
   } else {
     per_head = n_qt * static_cast<long long>(p.nkv_full);
   }
@@ -213,7 +218,7 @@ int launch(const void* Q, const void* K, const void* V, void* O, float* LSE, int
   if (workspace) {
     p.stream_k = 1;
     grid = static_cast<int>(std::min<long long>(info->sms, p.total_steps));
-    const size_t slots = static_cast<size_t>(info->sms) * 2;
+    const size_t slots = static_cast<size_t>(info->sms) * unit_subtiles;
     char* ws = static_cast<char*>(workspace);
     p.ws_o = reinterpret_cast<float*>(ws);
     p.ws_stats = p.ws_o + slots * D * 128;

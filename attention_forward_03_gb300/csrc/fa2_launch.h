@@ -1,7 +1,7 @@
 // Host-visible pieces of the forward and backward kernels: tile constants,
 // the parameter blocks, and the launcher templates (instantiated in
 // fa2_fwd_d32.cu, fa2_fwd_d64.cu, fa2_fwd_d96.cu, fa2_fwd_d128.cu,
-// fa2_bwd_d64.cu and fa2_bwd_d128.cu).
+// fa2_fwd_d256.cu, fa2_bwd_d64.cu and fa2_bwd_d128.cu).
 #pragma once
 #include <cuda.h>
 #include <cuda_runtime.h>
@@ -14,11 +14,15 @@ constexpr int kSubTiles = 2;        // sub-tiles per work unit
 constexpr int kUnitRows = kRows * kSubTiles;
 constexpr int kKeys = 128;          // keys per K/V tile
 
-// Head dimensions of the forward kernel. 64 and 128 are native; 32 and 96
+// Head dimensions of the forward kernels. 64 and 128 are native; 32 and 96
 // run in the layout of the next multiple of 64, the padded columns of every
 // Q/K/V tile read as zeros (the copy engine's out-of-bounds fill), so they
-// add nothing to Q.K^T and P.V.
-constexpr bool fwd_head_dim_ok(int d) { return d == 32 || d == 64 || d == 96 || d == 128; }
+// add nothing to Q.K^T and P.V. 256 has a kernel of its own with one
+// 128-row query sub-tile per work unit (its O accumulator takes half of the
+// tensor memory).
+constexpr bool fwd_head_dim_ok(int d) { return d == 32 || d == 64 || d == 96 || d == 128 || d == 256; }
+constexpr int fwd_unit_subtiles(int d) { return d == 256 ? 1 : kSubTiles; }
+constexpr int fwd_unit_rows(int d) { return kRows * fwd_unit_subtiles(d); }
 
 struct Params {
   void* o;                  // [B,H,N,D] 16-bit
@@ -27,7 +31,7 @@ struct Params {
   unsigned long long watchdog_ns;
   int N;
   int BH;
-  int n_qt;                 // query work units per head = ceil(N / 256)
+  int n_qt;                 // query work units per head = ceil(N / unit rows)
   int num_units;            // BH * n_qt
   int nkv_full;             // K/V tiles of a full row = ceil(N / 128)
   float scale_log2;         // scale * log2(e)
@@ -37,9 +41,10 @@ struct Params {
   int stream_k;
   long long steps_per_head; // K/V-tile steps of all units of one head
   long long total_steps;    // BH * steps_per_head
-  float* ws_o;              // [G][2][D][128] fp32 partial O (unnormalised)
-  float* ws_stats;          // [G][2][3][128] base, l, l_o of each partial row
-  unsigned long long* ws_flags;  // [G][2] = epoch once that partial is written
+  // (T = sub-tiles per unit: 2, or 1 at head dim 256)
+  float* ws_o;              // [G][T][D][128] fp32 partial O (unnormalised)
+  float* ws_stats;          // [G][T][3][128] base, l, l_o of each partial row
+  unsigned long long* ws_flags;  // [G][T] = epoch once that partial is written
   unsigned long long epoch; // unique tag of this launch
   int test_withhold;        // test hook: the producer withholds its first K/V tile
 };
@@ -68,9 +73,9 @@ struct BwdParams {
 
 // Bytes of stream-K workspace for `grid` CTAs at head dimension d.
 constexpr size_t stream_k_workspace_bytes(int grid, int d) {
-  return (static_cast<size_t>(grid) * (2ull * (static_cast<size_t>(d) * 128 + 3 * 128) * sizeof(float)) + 255) /
-             256 * 256 +
-         static_cast<size_t>(grid) * 2 * 8;
+  return (static_cast<size_t>(grid) * fwd_unit_subtiles(d) * ((static_cast<size_t>(d) * 128 + 3 * 128) * sizeof(float)) +
+          255) / 256 * 256 +
+         static_cast<size_t>(grid) * fwd_unit_subtiles(d) * 8;
 }
 
 // The full forward call (validation, tensor maps, launch) with an optional
@@ -101,5 +106,10 @@ cudaError_t launch_bwd(const CUtensorMap& k, const CUtensorMap& v, const CUtenso
 template <int D, bool kBf16, bool kCausal>
 cudaError_t launch_fwd(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v, const Params& p,
                        int grid, cudaStream_t stream);
+
+// Head dim 256 (fa2_kernel_wide.cuh, instantiated in fa2_fwd_d256.cu).
+template <int D, bool kBf16, bool kCausal>
+cudaError_t launch_fwd_wide(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v, const Params& p,
+                            int grid, cudaStream_t stream);
 
 }  // namespace fa2

@@ -48,11 +48,18 @@ KERNEL_SOURCES = os.path.join(ROOT, "attention_forward_03_gb300", "csrc")
 # ------------------------------------------------------------------ helpers
 # the files that define the kernel and its device-resident launch (the
 # host-memory pipeline and the no-allocation entry point do not change either)
-KERNEL_FILES = ("fa2_kernel.cuh", "fa2_launch.h", "sm103_ptx.cuh", "tmem_io.cuh", "fa2_fwd_d64.cu", "fa2_fwd_d128.cu",
-                "fa2_api.cu")
+KERNEL_FILES = ("fa2_kernel.cuh", "fa2_fwd_common.cuh", "fa2_launch.h", "sm103_ptx.cuh", "tmem_io.cuh",
+                "fa2_fwd_d32.cu", "fa2_fwd_d64.cu", "fa2_fwd_d96.cu", "fa2_fwd_d128.cu", "fa2_api.cu")
+# the head-dim-256 forward kernel
+WIDE_KERNEL_FILES = ("fa2_kernel_wide.cuh", "fa2_fwd_common.cuh", "fa2_launch.h", "sm103_ptx.cuh", "tmem_io.cuh",
+                     "fa2_fwd_d256.cu", "fa2_api.cu")
 # the same for the backward pass (its three kernels and their launch)
-BWD_KERNEL_FILES = ("fa2_bwd_kernel.cuh", "fa2_kernel.cuh", "fa2_launch.h", "sm103_ptx.cuh", "tmem_io.cuh",
-                    "fa2_bwd_d64.cu", "fa2_bwd_d128.cu", "fa2_bwd_api.cu", "fa2_api.cu")
+BWD_KERNEL_FILES = ("fa2_bwd_kernel.cuh", "fa2_kernel.cuh", "fa2_fwd_common.cuh", "fa2_launch.h", "sm103_ptx.cuh",
+                    "tmem_io.cuh", "fa2_bwd_d64.cu", "fa2_bwd_d128.cu", "fa2_bwd_api.cu", "fa2_api.cu")
+
+
+def fwd_kernel_files(D: int):
+    return WIDE_KERNEL_FILES if D == 256 else KERNEL_FILES
 
 
 def kernel_source_hash(files=KERNEL_FILES) -> str:
@@ -300,7 +307,8 @@ def run_gb300(args, w, rank, world, local):
     resolved_schedule = args.schedule
     if resolved_schedule == "auto":
         resolved_schedule = fa2.binding.choose_schedule(w.B, w.H, w.N, w.causal,
-                                                        torch.cuda.get_device_properties(dev).multi_processor_count)
+                                                        torch.cuda.get_device_properties(dev).multi_processor_count,
+                                                        w.D)
     set_bytes = workloads.algorithmic_bytes(w)
     l2 = getattr(torch.cuda.get_device_properties(dev), "L2_cache_size", 128 * 2 ** 20)
     nsets = max(2, math.ceil(2 * l2 / set_bytes))
@@ -363,10 +371,10 @@ def run_gb300(args, w, rank, world, local):
     torch.cuda.empty_cache()
     host_buf = torch.empty(fa2.fa2_fwd_host_buffer_bytes(w.B, w.H, w.N, w.D), dtype=torch.uint8, device=dev)
     sms = torch.cuda.get_device_properties(dev).multi_processor_count
-    hpc = args.e2e_heads_per_chunk or fa2.binding.host_chunk_heads(w.B, w.H, w.N, w.causal, sms)
+    hpc = args.e2e_heads_per_chunk or fa2.binding.host_chunk_heads(w.B, w.H, w.N, w.causal, sms, w.D)
     chunk_schedule = args.schedule
     if chunk_schedule == "auto":
-        chunk_schedule = fa2.binding.choose_schedule(1, min(hpc, w.B * w.H), w.N, w.causal, sms)
+        chunk_schedule = fa2.binding.choose_schedule(1, min(hpc, w.B * w.H), w.N, w.causal, sms, w.D)
 
     def e2e_step():
         fa2.attention_forward_host(qh, kh, vh, scale=w.scale, is_causal=w.causal, out=oh, lse=lh, stream=stream,
@@ -405,7 +413,7 @@ def run_gb300(args, w, rank, world, local):
         "pct_of_peak": 100.0 * achieved / peak,
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                      "frac": achieved / peak, "peak_source": f"{peak_src} bf16 dense (burst)",
-                     "traffic": traffic_per_launch(w.name),
+                     "traffic": traffic_per_launch(w.name, fwd_kernel_files(w.D)),
                      "algorithmic_bytes": workloads.algorithmic_bytes(w),
                      "achieved_hbm_gbs": workloads.algorithmic_bytes(w) / per_launch / 1e9},
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,

@@ -70,7 +70,7 @@ def call(lib, **over):
 
 @pytest.mark.parametrize("over,code", [
     (dict(B=-1), -1), (dict(H=-3), -1), (dict(N=-1), -1),
-    (dict(D=48), -2), (dict(D=256), -2), (dict(D=0), -2), (dict(D=16), -2), (dict(D=160), -2),
+    (dict(D=48), -2), (dict(D=512), -2), (dict(D=0), -2), (dict(D=16), -2), (dict(D=160), -2), (dict(D=192), -2),
     (dict(dtype=2), -2), (dict(dtype=-1), -2),
     (dict(scale=0.0), -1), (dict(scale=-0.5), -1), (dict(scale=float("nan")), -1), (dict(scale=float("inf")), -1),
     (dict(Q=None), -1), (dict(K=None), -1), (dict(V=None), -1), (dict(O=None), -1), (dict(LSE=None), -1),
@@ -96,7 +96,7 @@ def test_workspace_variant_checks_its_arguments(lib):
     assert call_ws(lib, A * 80, 1 << 20, D=48) == lib.FA2_ERR_UNSUPPORTED
     assert call_ws(lib, None, 0, B=0) == lib.FA2_OK
     n = ctypes.c_size_t(0)
-    assert lib.library().fa2_fwd_workspace_bytes(256, ctypes.byref(n)) == lib.FA2_ERR_UNSUPPORTED
+    assert lib.library().fa2_fwd_workspace_bytes(512, ctypes.byref(n)) == lib.FA2_ERR_UNSUPPORTED
     assert lib.library().fa2_fwd_workspace_bytes(64, None) == lib.FA2_ERR_INVALID_ARG
 
 
@@ -134,7 +134,7 @@ def test_host_entry_point_checks_arguments_first(lib):
     assert host(B=0) == lib.FA2_OK and host(N=0, Q=None, buf=None) == lib.FA2_OK
     n = ctypes.c_size_t(0)
     assert so.fa2_fwd_host_buffer_bytes(1, 2, 64, 64, None) == lib.FA2_ERR_INVALID_ARG
-    assert so.fa2_fwd_host_buffer_bytes(1, 2, 64, 256, ctypes.byref(n)) == lib.FA2_ERR_UNSUPPORTED
+    assert so.fa2_fwd_host_buffer_bytes(1, 2, 64, 512, ctypes.byref(n)) == lib.FA2_ERR_UNSUPPORTED
     assert so.fa2_fwd_host_buffer_bytes(-1, 2, 64, 64, ctypes.byref(n)) == lib.FA2_ERR_INVALID_ARG
 
 
@@ -143,6 +143,8 @@ def test_host_chunking_rule():
     # one K/V tile per 128 keys, one unit per 256 queries; causal unit qt sees 2qt+2 tiles
     assert steps_per_head(8192, False) == 32 * 64
     assert steps_per_head(512, True) == 2 + 4 and steps_per_head(300, True) == 2 + 3
+    assert steps_per_head(8192, False, 256) == 64 * 64
+    assert steps_per_head(512, True, 256) == 1 + 2 + 3 + 4 and steps_per_head(300, True, 256) == 1 + 2 + 3
     assert host_chunk_heads(1, 1, 128, False, 152) == 1
     # the shapes the host pipeline was measured on, and the fastest chunking found
     assert host_chunk_heads(1, 8, 8192, False, 152) == 2
@@ -165,7 +167,7 @@ def test_empty_problem_is_a_no_op(lib, over):
 def test_valid_call_without_a_gpu_fails_loudly(lib):
     assert call(lib) == lib.FA2_ERR_CUDA
     # every supported head dimension passes the argument checks and reaches the device query
-    for d in (32, 64, 96, 128):
+    for d in (32, 64, 96, 128, 256):
         assert call(lib, D=d) == lib.FA2_ERR_CUDA
         assert call_ws(lib, A * 80, 1 << 24, D=d) == lib.FA2_ERR_CUDA
     assert lib.library().fa2_last_cuda_error().decode() != ""
@@ -207,6 +209,9 @@ def test_schedule_choice():
     assert choose_schedule(1, 1, 8192, False, 152) == "balanced"   # 32 long units on 152 SMs
     assert choose_schedule(1, 1, 128, False, 152) == "units"       # one tiny unit
     assert choose_schedule(0, 8, 8192, False, 152) == "units"      # empty
+    # head dim 256: 128-row units (one sub-tile)
+    assert choose_schedule(1, 8, 8192, False, 152, 256) == "balanced"  # 512 units: 4 rounds of 64 vs 220 steps
+    assert choose_schedule(1, 19, 1024, False, 152, 256) == "units"    # exactly one full round
 
 
 BWD = dict(Q=A, K=A * 16, V=A * 32, O=A * 48, dO=A * 64, LSE=A * 80, dQ=A * 96, dK=A * 112, dV=A * 128, B=1, H=2,

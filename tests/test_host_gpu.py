@@ -56,7 +56,7 @@ def test_chunked_host_path_matches_oracle(fa2, oracle_mod, heads_per_chunk, sche
     check_against_oracle(oracle_mod, w, q, k, v, O, L)
 
 
-@pytest.mark.parametrize("D,dtype", [(128, "bf16"), (64, "f16"), (96, "bf16"), (32, "f16")])
+@pytest.mark.parametrize("D,dtype", [(128, "bf16"), (64, "f16"), (96, "bf16"), (32, "f16"), (256, "bf16")])
 def test_causal_host_path_matches_oracle(fa2, oracle_mod, D, dtype):
     w = workloads.custom(1, 5, 520, D, dtype, True, seed=42)
     q, k, v = (t.pin_memory() for t in workloads.make_inputs(w))

@@ -98,9 +98,47 @@ def test_padded_head_dims_every_element(fa2, oracle_mod, N, D, dtype, causal, sc
 
 
 @pytest.mark.parametrize("schedule", SCHEDULES)
-@pytest.mark.parametrize("name", ["pages_d32", "target_d96"])
-def test_padded_head_dim_workloads_full_size(fa2, oracle_mod, name, schedule):
+@pytest.mark.parametrize("name", ["pages_d32", "target_d96", "target_d256"])
+def test_other_head_dim_workloads_full_size(fa2, oracle_mod, name, schedule):
     compare(fa2, oracle_mod, workloads.WORKLOADS[name], sample=600, schedule=schedule)
+
+
+EDGE_N_256 = [1, 63, 127, 128, 129, 255, 256, 257, 1000]
+
+
+@pytest.mark.parametrize("N", EDGE_N_256)
+@pytest.mark.parametrize("dtype", ["f16", "bf16"])
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("schedule", SCHEDULES)
+def test_head_dim_256_every_element(fa2, oracle_mod, N, dtype, causal, schedule):
+    # Head dim 256 runs on its own kernel: 128-row work units, two S buffers.
+    w = workloads.custom(2, 3, N, 256, dtype, causal, seed=N * 13 + 256)
+    compare(fa2, oracle_mod, w, schedule=schedule)
+
+
+@pytest.mark.parametrize("shape", [(1, 1, 4096, False), (1, 2, 3000, True), (1, 3, 2049, False),
+                                   (2, 1, 8192, False), (1, 1, 8192, True)])
+def test_head_dim_256_units_cut_across_many_ctas(fa2, oracle_mod, shape):
+    # Few K/V-tile steps per CTA at head dim 256: units split over several
+    # CTAs, each owner merging several partials (every row checked).
+    B, H, N, causal = shape
+    w = workloads.custom(B, H, N, 256, "bf16", causal, seed=N + 256)
+    compare(fa2, oracle_mod, w, schedule="balanced")
+
+
+@pytest.mark.parametrize("schedule", SCHEDULES)
+def test_head_dim_256_many_units_per_cta(fa2, oracle_mod, schedule):
+    w = workloads.custom(3, 50, 700, 256, "f16", True, seed=61)
+    compare(fa2, oracle_mod, w, sample=400, schedule=schedule)
+    w = workloads.custom(2, 90, 640, 256, "bf16", False, seed=62)
+    compare(fa2, oracle_mod, w, sample=400, schedule=schedule)
+
+
+@pytest.mark.parametrize("schedule", SCHEDULES)
+def test_head_dim_256_peaked_logits(fa2, oracle_mod, schedule):
+    # Q/K ~ N(0, 3^2) as in the ragged workload: sharply peaked rows in fp16.
+    w = workloads.custom(2, 2, 1000, 256, "f16", False, seed=63, sigma_qk=3.0)
+    compare(fa2, oracle_mod, w, schedule=schedule)
 
 
 @pytest.mark.parametrize("schedule", SCHEDULES)

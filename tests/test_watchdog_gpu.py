@@ -26,8 +26,9 @@ def fa2():
     return m
 
 
-def test_withheld_tile_times_out_and_the_context_stays_usable(fa2, oracle_mod):
-    w = workloads.custom(1, 4, 512, 128, "bf16", False, seed=77)
+@pytest.mark.parametrize("D", [128, 256])
+def test_withheld_tile_times_out_and_the_context_stays_usable(fa2, oracle_mod, D):
+    w = workloads.custom(1, 4, 512, D, "bf16", False, seed=77)
     q, k, v = (t.cuda() for t in workloads.make_inputs(w))
     lib = fa2.library()
     try:

@@ -23,6 +23,8 @@ Q/K/V i.i.d. normal, cast to the 16-bit type with round-to-nearest-even):
               the smallest head dimension the tiling_qk page lists)
   target_d96  B=1 H=8 N=8192 D=96 bf16 non-causal, seed 8 (the target shape at
               head dimension 96)
+  target_d256 B=1 H=8 N=8192 D=256 bf16 non-causal, seed 9 (the target shape at
+              the first head dimension of the tiling_qk page's d-tiled range)
 
 Scale is 1/sqrt(D) everywhere. Draw order: Q, then K, then V, each
 ``torch.randn(shape, dtype=float32, generator=g) * sigma`` from a CPU
@@ -73,6 +75,7 @@ WORKLOADS = {
     "target_b4": Workload("target_b4", 4, 16, 8192, 128, "bf16", False, 6),
     "pages_d32": Workload("pages_d32", 1, 8, 8192, 32, "f16", False, 7),
     "target_d96": Workload("target_d96", 1, 8, 8192, 96, "bf16", False, 8),
+    "target_d256": Workload("target_d256", 1, 8, 8192, 256, "bf16", False, 9),
 }
 
 # The five workloads the parity contract names, in their stated order.
