@@ -186,8 +186,10 @@ int launch(const void* Q, const void* K, const void* V, void* O, float* LSE, int
   if (workspace && workspace_bytes < stream_k_workspace_bytes(info->sms, D)) return FA2_ERR_INVALID_ARG;
 
   CUtensorMap mq, mk, mv;
+  // V boxes: 128 rows, or at head dim 256 64 rows (the kernel streams V in
+  // halves of 64 keys there)
   if (!make_map(&mq, Q, (int)bh, N, D, dtype) || !make_map(&mk, K, (int)bh, N, D, dtype) ||
-      !make_map(&mv, V, (int)bh, N, D, dtype)) {
+      !make_rows_map(&mv, V, (int)bh, N, D, dtype, D == 256 ? 64u : 128u)) {
     std::snprintf(t_last_cuda_error, sizeof(t_last_cuda_error), "cuTensorMapEncodeTiled failed");
     return FA2_ERR_CUDA;
   }

@@ -21,11 +21,15 @@
 //   warp 10    TMA producer; warp 11 idle
 // Tensor memory: [0,128) S buffer 0, [128,256) S buffer 1, [256,512) O.
 // Shared memory: Q (64 KB, resident for the segment), P (32 KB, 16-bit,
-// K-major), and a two-slot ring of K/V tiles (64 KB each); all 128-byte
-// swizzled in 64-element-wide panels, the layout the MMAs read. The ring's
-// load order per segment [b, e) is K_b, then for each j: K_{j+1}, V_j; with
-// two slots the K tiles cycle through one slot and the V tiles through the
-// other, each reloaded while the tensor core runs the other product.
+// K-major), and a four-slot ring of K/V half tiles (32 KB each); all
+// 128-byte swizzled in 64-element-wide panels, the layout the MMAs read. The
+// ring's load order per segment [b, e) is K_b, then for each j: K_{j+1},
+// V_j, each tile as two halves: K split along the head dimension (the first
+// and last 8 K-steps of Q.K^T), V along the keys (the first and last 4
+// K-steps of P.V). Each half is released as soon as the MMAs that read it
+// have completed, so the next tile's first half loads while the second half
+// is still in use (with whole-tile slots the loads of a type and its MMAs
+// ran one after the other).
 //
 // Both schedules of the other forward kernel are supported (rounds of whole
 // units; stream-K shares of K/V-tile steps with a cross-CTA (m, l) merge of
@@ -40,11 +44,17 @@ struct WideLayout {
   static_assert(D == 256, "the wide kernel is built for head dimension 256");
   static constexpr int kPanels = D / 64;
   static constexpr int kTileBytes = kPanels * kPanelBytes;  // 128 rows x 256 (Q, K or V tile): 64 KB
-  static constexpr int kStages = 2;
+  // The ring holds half tiles: a K half is 128 keys x 128 head-dim columns
+  // (two 16 KB panels, the operand of 8 of the 16 K-steps of Q.K^T); a V half
+  // is 64 keys x 256 columns (four 8 KB panels of 64 rows, the operand of 4
+  // of the 8 K-steps of P.V).
+  static constexpr int kHalfBytes = kTileBytes / 2;
+  static constexpr int kVPanelBytes = kHalfBytes / kPanels;  // 64 rows x 64 elements
+  static constexpr int kStages = 4;
   static constexpr int kQBytes = kTileBytes;
   static constexpr int kPOffset = kQBytes;
   static constexpr int kRingOffset = kPOffset + kPTileBytes;
-  static constexpr int kBarOffset = kRingOffset + kStages * kTileBytes;
+  static constexpr int kBarOffset = kRingOffset + kStages * kHalfBytes;
   // barriers: q_full, q_empty, ring full (K tile)[S], ring full (V tile)[S], ring empty[S],
   // s_full[2], s_free[2], p_full, p_free, o_full, drain[2], part_done
   static constexpr int kNumBars = 2 + 3 * kStages + 2 + 2 + 3 + 2 + 1;
@@ -140,21 +150,29 @@ __global__ void __launch_bounds__(kThreads, 1)
         bool ok = true;
         SegCursor cur = first_cursor(p);
         Segment w;
+        // Loads both halves of tile j, each into the next ring slot.
         auto load_tile = [&](const CUtensorMap* map, int j, uint32_t is_v) -> bool {
-          if (!wait_bounded(bar_empty(slot), ring_ph ^ 1u, wd, kSiteLoadRingEmpty, true, kNapNs)) return false;
-          const uint32_t full = bar_full(slot, is_v);
-          if (!(p.test_withhold && issued == 0)) {  // test hook: the first tile never arrives
-            mbar_arrive_expect_tx(full, L::kTileBytes);
-            for (int pn = 0; pn < L::kPanels; ++pn)
-              tma_load_3d_hint(sRing + slot * L::kTileBytes + pn * kPanelBytes, map, full, pn * 64, j * kKeys,
-                               w.bh, keep);
-          }
-          types = (types & ~(1u << slot)) | (is_v << slot);
-          if (is_v) vbits ^= 1u << slot; else kbits ^= 1u << slot;
-          ++issued;
-          if (++slot == L::kStages) {
-            slot = 0;
-            ring_ph ^= 1u;
+          for (int h = 0; h < 2; ++h) {
+            if (!wait_bounded(bar_empty(slot), ring_ph ^ 1u, wd, kSiteLoadRingEmpty, true, kNapNs)) return false;
+            const uint32_t full = bar_full(slot, is_v);
+            const uint32_t dst = sRing + static_cast<uint32_t>(slot * L::kHalfBytes);
+            if (!(p.test_withhold && issued == 0)) {  // test hook: the first half tile never arrives
+              mbar_arrive_expect_tx(full, L::kHalfBytes);
+              if (is_v) {  // keys [64h, 64h+64) of the tile, four 64-column panels (the V map's box is 64 rows)
+                for (int pn = 0; pn < L::kPanels; ++pn)
+                  tma_load_3d_hint(dst + pn * L::kVPanelBytes, map, full, pn * 64, j * kKeys + 64 * h, w.bh, keep);
+              } else {     // head-dim columns [128h, 128h+128): two panels of 128 keys
+                for (int pn = 0; pn < 2; ++pn)
+                  tma_load_3d_hint(dst + pn * kPanelBytes, map, full, 128 * h + 64 * pn, j * kKeys, w.bh, keep);
+              }
+            }
+            types = (types & ~(1u << slot)) | (is_v << slot);
+            if (is_v) vbits ^= 1u << slot; else kbits ^= 1u << slot;
+            ++issued;
+            if (++slot == L::kStages) {
+              slot = 0;
+              ring_ph ^= 1u;
+            }
           }
           return true;
         };
@@ -191,32 +209,36 @@ __global__ void __launch_bounds__(kThreads, 1)
         constexpr uint32_t idesc_s = make_idesc_f16(kBf16, kKeys, false);
         constexpr uint32_t idesc_o = make_idesc_f16(kBf16, D, true);
         constexpr uint32_t kHi = desc_hi_sw128(1024);  // 8-row (K-major) / 8-key (MN-major) groups 1 KB apart
-        // S(buffer) = Q K^T : D/16 steps of K=16 along the head dimension.
-        auto issue_s = [&](int buf, int slot) {
-          const uint32_t qa = desc_lo_sw128(sQ, 16);
-          const uint32_t ka = desc_lo_sw128(sRing, 16) + static_cast<uint32_t>(slot * (L::kTileBytes >> 4));
+        // Half h of S(buffer) = Q K^T: the 8 K-steps over head-dim columns
+        // [128h, 128h+128), B from the K half tile in `slot`.
+        auto issue_s_half = [&](int buf, int h, int slot) {
+          const uint32_t qa = desc_lo_sw128(sQ, 16) + static_cast<uint32_t>((h * 2 * kPanelBytes) >> 4);
+          const uint32_t ka = desc_lo_sw128(sRing, 16) + static_cast<uint32_t>(slot * (L::kHalfBytes >> 4));
           const uint32_t dt = tmem + static_cast<uint32_t>(buf * kKeys);
 #pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk) {
+          for (int kk = 0; kk < 8; ++kk) {
             const uint32_t off = static_cast<uint32_t>(((kk >> 2) * kPanelBytes + (kk & 3) * 32) >> 4);
-            mma_ss_w(dt, qa + off, kHi, ka + off, kHi, idesc_s, kk > 0 ? 1u : 0u);
+            mma_ss_w(dt, qa + off, kHi, ka + off, kHi, idesc_s, (h > 0 || kk > 0) ? 1u : 0u);
           }
         };
-        // O (+)= P V : P (K-major, shared memory) and V (MN-major, N = 256
-        // across four 64-column panels 16 KB apart), 8 steps of 16 keys.
-        auto issue_pv = [&](int slot, bool acc) {
-          const uint32_t pa = desc_lo_sw128(sP, 16);
-          const uint32_t va = desc_lo_sw128(sRing, kPanelBytes) + static_cast<uint32_t>(slot * (L::kTileBytes >> 4));
+        // Half h of O (+)= P V: keys [64h, 64h+64), 4 K-steps of 16 keys. P
+        // is K-major in shared memory; V is MN-major, N = 256 across the half
+        // tile's four 64-column panels 8 KB apart.
+        auto issue_pv_half = [&](int h, int slot, bool acc) {
+          const uint32_t pa = desc_lo_sw128(sP, 16) + static_cast<uint32_t>((h * kPanelBytes) >> 4);
+          const uint32_t va = desc_lo_sw128(sRing, L::kVPanelBytes) + static_cast<uint32_t>(slot * (L::kHalfBytes >> 4));
           const uint32_t dt = tmem + L::kColO;
 #pragma unroll
-          for (int kk = 0; kk < kKeys / 16; ++kk) {
+          for (int kk = 0; kk < 4; ++kk) {
             const uint32_t vb = va + static_cast<uint32_t>((kk * 16 * 128) >> 4);
-            const uint32_t po = static_cast<uint32_t>(((kk >> 2) * kPanelBytes + (kk & 3) * 32) >> 4);
-            mma_ss_w(dt, pa + po, kHi, vb, kHi, idesc_o, (acc || kk > 0) ? 1u : 0u);
+            const uint32_t po = static_cast<uint32_t>((kk * 32) >> 4);
+            mma_ss_w(dt, pa + po, kHi, vb, kHi, idesc_o, (acc || h > 0 || kk > 0) ? 1u : 0u);
           }
         };
-        auto k_index = [](int j, int b) { return j == b ? 0 : 2 * (j - b) - 1; };
-        auto v_index = [](int j, int b, int e) { return j == e - 1 ? 2 * (j - b) + 1 : 2 * (j - b) + 2; };
+        // Ring index of half 0 of a tile: two halves per tile, in the load
+        // order K_b, then for each j: K_{j+1}, V_j.
+        auto k_index = [](int j, int b) { return 2 * (j == b ? 0 : 2 * (j - b) - 1); };
+        auto v_index = [](int j, int b, int e) { return 2 * (j == e - 1 ? 2 * (j - b) + 1 : 2 * (j - b) + 2); };
         uint32_t bits[2] = {0u, 0u};
         auto take = [&](uint32_t idx, uint32_t is_v) -> int {
           const int s = static_cast<int>(idx % L::kStages);
@@ -250,14 +272,19 @@ __global__ void __launch_bounds__(kThreads, 1)
                 s_free_ph ^= 1u << buf;
               }
               tc_fence_after_sync();
-              issue_s(buf, slot_k);
+              issue_s_half(buf, 0, slot_k);
+              mma_commit(bar_empty(slot_k));
+              const int slot_k1 = take(base_idx + k_index(j, b) + 1, 0u);
+              if (slot_k1 < 0) { ok = false; break; }
+              tc_fence_after_sync();
+              issue_s_half(buf, 1, slot_k1);
               mma_commit(bar_s_full0 + 8 * buf);
               s_out |= 1u << buf;
               ++n_s;
-              mma_commit(bar_empty(slot_k));
+              mma_commit(bar_empty(slot_k1));
               if (j == e - 1) mma_commit(bar_q_empty);
             }
-            base_idx += 2u * static_cast<uint32_t>(e - b);
+            base_idx += 4u * static_cast<uint32_t>(e - b);
           }
         } else {
           // P.V issuer: O += P(j) V_j as soon as V_j has landed and the
@@ -271,12 +298,17 @@ __global__ void __launch_bounds__(kThreads, 1)
               if (!wait_bounded(bar_p_full, p_full_ph, wd, kSiteMmaPFull, true, kNapNs)) { ok = false; break; }
               p_full_ph ^= 1u;
               tc_fence_after_sync();
-              issue_pv(slot_v, j > b);
+              issue_pv_half(0, slot_v, j > b);
+              mma_commit(bar_empty(slot_v));
+              const int slot_v1 = take(base_idx + v_index(j, b, e) + 1, 1u);
+              if (slot_v1 < 0) { ok = false; break; }
+              tc_fence_after_sync();
+              issue_pv_half(1, slot_v1, true);
               mma_commit(bar_p_free);
               if (j == e - 1) mma_commit(bar_o_full);
-              mma_commit(bar_empty(slot_v));
+              mma_commit(bar_empty(slot_v1));
             }
-            base_idx += 2u * static_cast<uint32_t>(e - b);
+            base_idx += 4u * static_cast<uint32_t>(e - b);
           }
         }
         // Drain: all issued tensor-core work completes before TMEM is released.
