@@ -22,6 +22,10 @@ FA2_ERR_UNSUPPORTED = -2
 FA2_ERR_ALIGN = -3
 FA2_ERR_CUDA = -4
 FA2_ERR_TIMEOUT = -5
+FA2_SCHED_AUTO = 0
+FA2_SCHED_UNITS = 1
+FA2_SCHED_BALANCED = 2
+_SCHEDULES = {"auto": FA2_SCHED_AUTO, "units": FA2_SCHED_UNITS, "balanced": FA2_SCHED_BALANCED}
 
 # every symbol include/fa2.h declares, with its ctypes signature
 _VP = ctypes.c_void_p
@@ -44,6 +48,9 @@ SIGNATURES = {
     "fa2_bwd": (ctypes.c_int, [_VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, ctypes.c_int, ctypes.c_int,
                                ctypes.c_int, ctypes.c_int, ctypes.c_float, ctypes.c_int, ctypes.c_int, _VP,
                                ctypes.c_size_t, _VP]),
+    "fa2_bwd_sched": (ctypes.c_int, [_VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, ctypes.c_int, ctypes.c_int,
+                                     ctypes.c_int, ctypes.c_int, ctypes.c_float, ctypes.c_int, ctypes.c_int, _VP,
+                                     ctypes.c_size_t, ctypes.c_int, _VP]),
     "fa2_device_status": (ctypes.c_int, [_VP, ctypes.POINTER(ctypes.c_int), ctypes.c_int]),
     "fa2_set_watchdog_ns": (ctypes.c_int, [ctypes.c_ulonglong]),
     "fa2_test_withhold_next_load": (ctypes.c_int, [ctypes.c_int]),
@@ -129,6 +136,14 @@ def fa2_bwd(Q: int, K: int, V: int, O: int, dO: int, LSE: int, dQ: int, dK: int,
     """Pointer-level call of the backward pass; returns the raw status code."""
     return library().fa2_bwd(Q, K, V, O, dO, LSE, dQ, dK, dV, B, H, N, D, float(scale), int(is_causal),
                              int(dtype), workspace, int(workspace_bytes), stream)
+
+
+def fa2_bwd_sched(Q: int, K: int, V: int, O: int, dO: int, LSE: int, dQ: int, dK: int, dV: int, B: int, H: int,
+                  N: int, D: int, scale: float, is_causal: int, dtype: int, workspace: int | None,
+                  workspace_bytes: int, schedule: int, stream: int | None) -> int:
+    """Pointer-level call of the backward pass with an explicit schedule code; returns the raw status."""
+    return library().fa2_bwd_sched(Q, K, V, O, dO, LSE, dQ, dK, dV, B, H, N, D, float(scale), int(is_causal),
+                                   int(dtype), workspace, int(workspace_bytes), int(schedule), stream)
 
 
 def fa2_device_status(stream: int | None = None, clear: bool = False) -> int:
@@ -351,8 +366,8 @@ def attention_forward_host(q, k, v, scale: float | None = None, is_causal: bool 
 
 
 def attention_backward(q, k, v, o, lse, do, scale: float | None = None, is_causal: bool = False, dq=None, dk=None,
-                       dv=None, workspace=None, stream=None):
-    """Gradient of attention_forward w.r.t. q, k, v for an upstream gradient `do` (fa2_bwd).
+                       dv=None, workspace=None, stream=None, schedule: str = "auto"):
+    """Gradient of attention_forward w.r.t. q, k, v for an upstream gradient `do` (fa2_bwd_sched).
 
     q, k, v, o, do: contiguous CUDA tensors [B, H, N, D] of one dtype (fp16/bf16);
     o and lse are the forward's outputs for q, k, v (same scale and mask).
@@ -360,8 +375,12 @@ def attention_backward(q, k, v, o, lse, do, scale: float | None = None, is_causa
     outputs; `workspace` an optional uint8 CUDA tensor of at least
     fa2_bwd_workspace_bytes(B, H, N, D) bytes (allocated per call otherwise).
     Runs on `stream` (a torch.cuda.Stream) or the current stream.
+    schedule: "auto" (the library's choice, as fa2_bwd), "units" (whole K/V
+    tiles per SM in rounds) or "balanced" (equal query steps per SM).
     """
     import torch
+    if schedule not in _SCHEDULES:
+        raise ValueError("schedule must be 'auto', 'balanced' or 'units'")
     ts = (q, k, v, o, do)
     if not all(t.is_cuda for t in ts) or not lse.is_cuda:
         raise ValueError("q, k, v, o, do and lse must be CUDA tensors")
@@ -390,9 +409,9 @@ def attention_backward(q, k, v, o, lse, do, scale: float | None = None, is_causa
         raise ValueError(f"workspace must be a CUDA tensor of at least {need} bytes")
     s = stream if stream is not None else torch.cuda.current_stream(q.device)
     with torch.cuda.device(q.device):
-        code = fa2_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), do.data_ptr(), lse.data_ptr(),
-                       outs[0].data_ptr(), outs[1].data_ptr(), outs[2].data_ptr(), B, H, N, D, scale,
-                       int(bool(is_causal)), _dtype_code(q), workspace.data_ptr(),
-                       workspace.numel() * workspace.element_size(), s.cuda_stream)
-        _check(code, "fa2_bwd")
+        code = fa2_bwd_sched(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), do.data_ptr(),
+                             lse.data_ptr(), outs[0].data_ptr(), outs[1].data_ptr(), outs[2].data_ptr(), B, H, N,
+                             D, scale, int(bool(is_causal)), _dtype_code(q), workspace.data_ptr(),
+                             workspace.numel() * workspace.element_size(), _SCHEDULES[schedule], s.cuda_stream)
+        _check(code, "fa2_bwd_sched")
     return tuple(outs)

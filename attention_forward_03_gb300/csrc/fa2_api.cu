@@ -241,6 +241,8 @@ int launch(const void* Q, const void* K, const void* V, void* O, float* LSE, int
 namespace fa2 {
 int record_cuda_error(cudaError_t e) { return record_cuda(e); }
 
+unsigned long long next_launch_epoch() { return next_epoch(); }
+
 int current_device_facts(int* sms, int** status) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);

@@ -9,6 +9,7 @@
 #include <cuda_runtime.h>
 #include <math_constants.h>
 
+#include <algorithm>
 #include <cmath>
 #include <cstdint>
 
@@ -23,8 +24,10 @@ constexpr int kElemBlocksPerSm = 8;
 
 size_t round256(size_t x) { return (x + 255) / 256 * 256; }
 
+// Workspace: dQ accumulator | LSE*log2(e) | Delta | stream-K partial dV, dK
+// (one [2][D][128] fp32 slot per CTA, kBwdMaxCtas slots) | their flags.
 struct BwdWorkspace {
-  size_t dq_bytes, stat_bytes, total;
+  size_t dq_bytes, stat_bytes, part_bytes, flag_bytes, total;
 };
 
 BwdWorkspace workspace_layout(int64_t bh, int N, int D) {
@@ -32,9 +35,35 @@ BwdWorkspace workspace_layout(int64_t bh, int N, int D) {
   BwdWorkspace w;
   w.dq_bytes = round256(static_cast<size_t>(bh) * N * D * sizeof(float));
   w.stat_bytes = round256(static_cast<size_t>(bh) * npad * sizeof(float));
-  w.total = w.dq_bytes + 2 * w.stat_bytes;
+  w.part_bytes = round256(static_cast<size_t>(kBwdMaxCtas) * 2 * D * 128 * sizeof(float));
+  w.flag_bytes = round256(static_cast<size_t>(kBwdMaxCtas) * sizeof(unsigned long long));
+  w.total = w.dq_bytes + 2 * w.stat_bytes + w.part_bytes + w.flag_bytes;
   return w;
 }
+
+// Cost of the busiest CTA in query steps under the round schedule (units
+// dealt in rounds, zig-zag when causal: the kernel's bwd_round_unit and
+// bwd_unit), or -1 when there are too many units to count here.
+long long round_schedule_cost(long long units, int bh, int nkv, int nq, bool causal, int grid) {
+  if (!causal) return (units + grid - 1) / grid * nq;
+  if (units > (1ll << 22)) return -1;
+  long long worst = 0;
+  for (int b = 0; b < grid; ++b) {
+    long long sum = 0;
+    for (long long r = 0;; ++r) {
+      const long long u = r * grid + ((r & 1) ? (grid - 1 - b) : b);
+      if (u >= units) break;
+      const long long kv = u / bh;  // causal: K/V tile major over all heads
+      sum += nq - 2 * kv;
+    }
+    worst = sum > worst ? sum : worst;
+  }
+  return worst;
+}
+
+// Partial-result write and merge of a cut unit, in query steps (its 2*128*D
+// fp32 values go out once and are read once by the owner).
+constexpr long long kBwdSplitCostSteps = 2;
 
 __device__ __forceinline__ void unpack8(const uint4& u, float (&f)[8], bool bf16) {
   const uint32_t w[4] = {u.x, u.y, u.z, u.w};
@@ -161,10 +190,13 @@ extern "C" int fa2_bwd_workspace_bytes(int B, int H, int N, int D, size_t* bytes
   return FA2_OK;
 }
 
-extern "C" int fa2_bwd(const void* Q, const void* K, const void* V, const void* O, const void* dO, const float* LSE,
-                       void* dQ, void* dK, void* dV, int B, int H, int N, int D, float scale, int is_causal,
-                       int dtype, void* workspace, size_t workspace_bytes, struct CUstream_st* stream) {
+extern "C" int fa2_bwd_sched(const void* Q, const void* K, const void* V, const void* O, const void* dO,
+                             const float* LSE, void* dQ, void* dK, void* dV, int B, int H, int N, int D, float scale,
+                             int is_causal, int dtype, void* workspace, size_t workspace_bytes, int schedule,
+                             struct CUstream_st* stream) {
   if (B < 0 || H < 0 || N < 0) return FA2_ERR_INVALID_ARG;
+  if (schedule != FA2_SCHED_AUTO && schedule != FA2_SCHED_UNITS && schedule != FA2_SCHED_BALANCED)
+    return FA2_ERR_INVALID_ARG;
   if (D != 64 && D != 128) return FA2_ERR_UNSUPPORTED;
   if (dtype != FA2_F16 && dtype != FA2_BF16) return FA2_ERR_UNSUPPORTED;
   if (!std::isfinite(scale) || !(scale > 0.f)) return FA2_ERR_INVALID_ARG;
@@ -239,7 +271,30 @@ extern "C" int fa2_bwd(const void* Q, const void* K, const void* V, const void* 
   p.num_units = (int)(bh * nkv);
   p.scale_log2 = scale * 1.4426950408889634f;
   p.scale = scale;
-  const int grid = p.num_units < sms ? p.num_units : sms;
+  // Query steps of one head: non-causal nkv * nq; causal, K/V tile kv sees
+  // the steps from 2*kv on.
+  long long per_head = 0;
+  for (int64_t kv = 0; kv < nkv; ++kv) per_head += is_causal ? p.nq - 2 * kv : p.nq;
+  p.steps_per_head = per_head;
+  p.total_steps = per_head * bh;
+  const int round_grid = p.num_units < sms ? p.num_units : sms;
+  const int sk_grid = static_cast<int>(std::min<long long>(std::min(sms, kBwdMaxCtas), p.total_steps));
+  bool balanced = schedule == FA2_SCHED_BALANCED;
+  if (schedule == FA2_SCHED_AUTO) {
+    // the schedule whose busiest CTA has fewer steps, balanced only when it
+    // saves at least 5 %
+    const long long rounds = round_schedule_cost(p.num_units, p.BH, p.nkv, p.nq, is_causal != 0, round_grid);
+    const long long split = (p.total_steps + sk_grid - 1) / sk_grid + kBwdSplitCostSteps;
+    balanced = rounds > 0 && 100 * split < 95 * rounds;
+  }
+  int grid = round_grid;
+  if (balanced) {
+    p.stream_k = 1;
+    grid = sk_grid;
+    p.ws_part = reinterpret_cast<float*>(ws + wl.dq_bytes + 2 * wl.stat_bytes);
+    p.ws_flags = reinterpret_cast<unsigned long long*>(ws + wl.dq_bytes + 2 * wl.stat_bytes + wl.part_bytes);
+    p.epoch = next_launch_epoch();
+  }
   e = pick_bwd(D, dtype, is_causal)(mk, mv, mq, mdo, mdq, p, grid, s);
   if (e != cudaSuccess) return record_cuda_error(e);
 
@@ -254,4 +309,11 @@ extern "C" int fa2_bwd(const void* Q, const void* K, const void* V, const void* 
   e = cudaGetLastError();
   if (e != cudaSuccess) return record_cuda_error(e);
   return FA2_OK;
+}
+
+extern "C" int fa2_bwd(const void* Q, const void* K, const void* V, const void* O, const void* dO, const float* LSE,
+                       void* dQ, void* dK, void* dV, int B, int H, int N, int D, float scale, int is_causal,
+                       int dtype, void* workspace, size_t workspace_bytes, struct CUstream_st* stream) {
+  return fa2_bwd_sched(Q, K, V, O, dO, LSE, dQ, dK, dV, B, H, N, D, scale, is_causal, dtype, workspace,
+                       workspace_bytes, FA2_SCHED_AUTO, stream);
 }

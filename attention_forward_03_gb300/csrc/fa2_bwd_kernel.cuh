@@ -18,7 +18,8 @@
 // and at the end of the tile dK *= scale; dQ = scale * accumulator is
 // converted to the dtype by a separate elementwise kernel.
 //
-// Layout of one CTA (one per SM, persistent over work units = K/V tiles):
+// Layout of one CTA (one per SM, persistent over work units = K/V tiles, or
+// over segments of them, see below):
 //   warps 0-7  two compute warpgroups; thread = key row = TMEM lane, warpgroup
 //              g takes query columns [32g, 32g+32) of every step (and the
 //              halves [gD/2, (g+1)D/2) of the dK / dV rows in the epilogue)
@@ -41,6 +42,14 @@
 // (written by the compute threads, read by the tensor core), and an fp32
 // staging tile for dQ (64 rows x D) that TMA reduce-adds into the global
 // accumulator, 32 rows per compute warpgroup.
+//
+// Schedules: whole units dealt to the CTAs in rounds (zig-zag when causal),
+// or stream-K: every CTA takes an equal share of all query steps, so a unit
+// may be cut between consecutive CTAs; the CTA holding a unit's first steps
+// (for which it is the last segment of its share) adds the fp32 partial dV,
+// dK that the following CTAs wrote (each as the first segment of its share)
+// before it writes dV and dK. dQ needs no merge: every step adds into the
+// accumulator whichever CTA runs it.
 //
 // Pipelining: the issuer computes S^T, dP^T of step i+1 as soon as the
 // compute threads have loaded those of step i into registers, so the tensor
@@ -76,6 +85,8 @@ enum : int {
   kSiteBwdDrain = 33,
   kSiteBwdDqsFree = 34,
   kSiteBwdDqsReady = 35,
+  kSiteBwdPartWrite = 36,
+  kSiteBwdPartFlag = 37,
 };
 
 template <int D>
@@ -94,8 +105,8 @@ struct BwdLayout {
   static constexpr int kStats = kDQS + kBwdRows * D * 4;
   static constexpr int kBars = kStats + kStages * kBwdStatBytes;
   // kv_full, kv_empty, stage_full[S], stage_empty[S], s_full, s_free, p_full,
-  // p_free, dq_full, dq_free, acc_full, acc_free, drain, dqs_ready[2], dqs_free[2], drain2
-  static constexpr int kNumBars = 2 + 2 * kStages + 14;
+  // p_free, dq_full, dq_free, acc_full, acc_free, drain, dqs_ready[2], dqs_free[2], drain2, part_done
+  static constexpr int kNumBars = 2 + 2 * kStages + 15;
   static constexpr int kMisc = kBars + kNumBars * 8;
   static constexpr int kSmemBytes = kMisc + 16 + 1024;  // + slack for 1 KB alignment
   static constexpr uint32_t kColDV = 0;
@@ -133,6 +144,78 @@ template <bool kCausal>
 __device__ __forceinline__ int bwd_round_unit(int r) {
   const int g = gridDim.x, b = blockIdx.x;
   return r * g + ((kCausal && (r & 1)) ? (g - 1 - b) : b);
+}
+
+// A segment: query steps [i_begin, i_end) of unit (bh, kv). With the round
+// schedule every segment is a whole unit; with stream-K a unit may be cut
+// between consecutive CTAs.
+struct BwdSegment {
+  int bh, kv;
+  int i_begin, i_end;
+  long long unit_end;  // stream-K: global step one past the unit's last step
+};
+
+struct BwdCursor {
+  int round;
+  long long step, end;
+};
+
+__device__ __forceinline__ long long bwd_share_begin(const BwdParams& p, int b) {
+  return p.total_steps * b / gridDim.x;
+}
+
+__device__ __forceinline__ BwdCursor bwd_first_cursor(const BwdParams& p) {
+  BwdCursor c;
+  c.round = 0;
+  c.step = p.stream_k ? bwd_share_begin(p, blockIdx.x) : 0;
+  c.end = p.stream_k ? bwd_share_begin(p, blockIdx.x + 1) : 0;
+  return c;
+}
+
+// First step of causal unit kv within its head: units k < kv have
+// nq - 2k steps each, kv*nq - kv*(kv-1) in all.
+__device__ __forceinline__ long long bwd_causal_start(int kv, int nq) {
+  return static_cast<long long>(kv) * nq - static_cast<long long>(kv) * (kv - 1);
+}
+
+// Next segment of this CTA. Every role walks the same sequence.
+template <bool kCausal>
+__device__ __forceinline__ bool bwd_next_segment(BwdCursor& c, BwdSegment& s, const BwdParams& p) {
+  if (!p.stream_k) {
+    const int u = bwd_round_unit<kCausal>(c.round++);
+    if (u >= p.num_units) return false;
+    bwd_unit<kCausal>(u, p, s.bh, s.kv);
+    s.i_begin = bwd_first_step<kCausal>(s.kv);
+    s.i_end = p.nq;
+    s.unit_end = 0;
+    return true;
+  }
+  if (c.step >= c.end) return false;
+  // Units in order: heads, then K/V tiles ascending.
+  const long long bh = c.step / p.steps_per_head;
+  const long long r = c.step - bh * p.steps_per_head;
+  int kv;
+  long long start;
+  if (kCausal) {
+    const float a = static_cast<float>(p.nq) + 1.f;
+    kv = static_cast<int>((a - sqrtf(fmaxf(a * a - 4.f * static_cast<float>(r), 0.f))) * 0.5f);
+    kv = min(max(kv, 0), p.nkv - 1);
+    while (kv > 0 && bwd_causal_start(kv, p.nq) > r) --kv;
+    while (kv + 1 < p.nkv && bwd_causal_start(kv + 1, p.nq) <= r) ++kv;
+    start = bwd_causal_start(kv, p.nq);
+  } else {
+    kv = static_cast<int>(r / p.nq);
+    start = static_cast<long long>(kv) * p.nq;
+  }
+  const int first = bwd_first_step<kCausal>(kv);
+  s.bh = static_cast<int>(bh);
+  s.kv = kv;
+  s.i_begin = first + static_cast<int>(r - start);
+  const long long left = c.end - c.step;
+  s.i_end = static_cast<int>(min(static_cast<long long>(p.nq), s.i_begin + left));
+  s.unit_end = c.step - (s.i_begin - first) + (p.nq - first);
+  c.step += s.i_end - s.i_begin;
+  return true;
 }
 
 template <int D, bool kBf16, bool kCausal>
@@ -173,6 +256,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   auto bar_dqs_ready = [&](int w) { return bar_s_full + 72 + 8u * w; };
   auto bar_dqs_free = [&](int w) { return bar_s_full + 88 + 8u * w; };
   const uint32_t bar_drain2 = bar_s_full + 104;                // second issuer
+  const uint32_t bar_part = bar_s_full + 112;                  // stream-K partial dV, dK written
   const uint32_t sDQS = base + L::kDQS;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kMisc + 4);
@@ -201,6 +285,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       mbar_init(bar_dqs_ready(w), 128);
       mbar_init(bar_dqs_free(w), 1);
     }
+    mbar_init(bar_part, kBwdComputeThreads);
     *abort_flag = 0;
     mbar_init_fence();
   }
@@ -233,11 +318,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       int slot = 0;
       uint32_t ph = 0, units = 0, loads = 0;
       bool ok = true;
-      for (int r = 0; ok; ++r) {
-        const int u = bwd_round_unit<kCausal>(r);
-        if (u >= p.num_units) break;
-        int bh, kv;
-        bwd_unit<kCausal>(u, p, bh, kv);
+      BwdCursor cur = bwd_first_cursor(p);
+      BwdSegment sg;
+      while (ok && bwd_next_segment<kCausal>(cur, sg, p)) {
+        const int bh = sg.bh, kv = sg.kv;
         if (units > 0 && !wait_bounded(bar_kv_empty, (units - 1) & 1u, wd, kSiteBwdKvEmpty, true, kNapNs)) {
           ok = false;
           break;
@@ -248,7 +332,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           tma_load_3d_hint(sV + pn * kPanelBytes, &tmV, bar_kv_full, pn * 64, kv * kBwdKeys, bh, once);
         }
         ++units;
-        for (int i = bwd_first_step<kCausal>(kv); i < p.nq; ++i) {
+        for (int i = sg.i_begin; i < sg.i_end; ++i) {
           if (!wait_bounded(bar_stage_empty(slot), ph ^ 1u, wd, kSiteBwdStageEmpty, true, kNapNs)) {
             ok = false;
             break;
@@ -350,12 +434,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         uint32_t g = 0;
         uint32_t units = 0;
         bool ok = true;
-        for (int r = 0; ok; ++r) {
-          const int u = bwd_round_unit<kCausal>(r);
-          if (u >= p.num_units) break;
-          int bh, kv;
-          bwd_unit<kCausal>(u, p, bh, kv);
-          const int n_steps = p.nq - bwd_first_step<kCausal>(kv);
+        BwdCursor cur = bwd_first_cursor(p);
+        BwdSegment sg;
+        while (ok && bwd_next_segment<kCausal>(cur, sg, p)) {
+          const int n_steps = sg.i_end - sg.i_begin;
           if (!wait_bounded(bar_kv_full, units & 1u, wd, kSiteBwdKvFull, true, kNapNs)) {
             ok = false;
             break;
@@ -427,12 +509,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           }
           return s;
         };
-        for (int r = 0; ok; ++r) {
-          const int u = bwd_round_unit<kCausal>(r);
-          if (u >= p.num_units) break;
-          int bh, kv;
-          bwd_unit<kCausal>(u, p, bh, kv);
-          const int n_steps = p.nq - bwd_first_step<kCausal>(kv);
+        BwdCursor wcur = bwd_first_cursor(p);
+        BwdSegment sg;
+        while (ok && bwd_next_segment<kCausal>(wcur, sg, p)) {
+          const int n_steps = sg.i_end - sg.i_begin;
           if (!wait_bounded(bar_kv_full, units & 1u, wd, kSiteBwdKvFull, true, kNapNs)) {
             ok = false;
             break;
@@ -502,7 +582,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const uint32_t xr = static_cast<uint32_t>(rr & 7);
     const bool dq_rows = quarter * 32 < D;    // warp-uniform: lanes >= D of dQ^T are discarded
     const float c = p.scale_log2;
-    uint32_t g = 0, units = 0, ph = 0;
+    uint32_t g = 0, units = 0, ph = 0, part_phase = 0;
     int slot = 0;
     bool ok = true;
     int pend_bh = 0, pend_q0 = 0;  // head and first row of the step whose dQ^T is pending
@@ -559,14 +639,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       return true;
     };
 
-    for (int r = 0; ok; ++r) {
-      const int u = bwd_round_unit<kCausal>(r);
-      if (u >= p.num_units) break;
-      int bh, kv;
-      bwd_unit<kCausal>(u, p, bh, kv);
+    BwdCursor cur = bwd_first_cursor(p);
+    BwdSegment sg;
+    while (ok && bwd_next_segment<kCausal>(cur, sg, p)) {
+      const int bh = sg.bh, kv = sg.kv;
       const int key = kv * kBwdKeys + rr;
       const bool key_ok = key < p.N;
-      for (int i = bwd_first_step<kCausal>(kv); i < p.nq; ++i, ++g) {
+      for (int i = sg.i_begin; i < sg.i_end; ++i, ++g) {
         bool got = wait_bounded(bar_s_full, g & 1u, wd, kSiteBwdSFull);
         got = got && wait_bounded(bar_stage_full(slot), ph, wd, kSiteBwdStageFull);
         got = __all_sync(0xffffffffu, got);
@@ -640,6 +719,97 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       }
       tc_fence_after_sync();
       constexpr int kHalf = D / 2;
+      const size_t out_off = (static_cast<size_t>(bh) * p.N + (key_ok ? key : 0)) * (D * 2) + wg * kHalf * 2;
+      if (p.stream_k && sg.i_begin > bwd_first_step<kCausal>(kv)) {
+        // Not the unit's first steps: hand this CTA's partial dV, dK to the
+        // unit's owner through its workspace slot ([2][D][128], column-major
+        // so that a warp's stores are contiguous), 32 columns at a time.
+        float* pv = p.ws_part + static_cast<size_t>(blockIdx.x) * 2 * D * 128;
+        float* pkk = pv + D * 128;
+#pragma unroll 1
+        for (int cc = 0; cc < kHalf; cc += 32) {
+          uint32_t a[32], b[32];
+          tmem_ld32x32_wait(tmem + lane_off + L::kColDV + wg * kHalf + cc, a);
+          tmem_ld32x32_wait(tmem + lane_off + L::kColDK + wg * kHalf + cc, b);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            const int col = wg * kHalf + cc + i;
+            __stcg(pv + col * 128 + rr, __uint_as_float(a[i]));
+            __stcg(pkk + col * 128 + rr, __uint_as_float(b[i]));
+          }
+        }
+        tc_fence_before_sync();
+        mbar_arrive(bar_acc_free);
+        __threadfence();
+        mbar_arrive(bar_part);
+        if (warp == 0) {  // the whole warp waits, so that it stays converged
+          bool done = wait_bounded(bar_part, part_phase, wd, kSiteBwdPartWrite);
+          done = __all_sync(0xffffffffu, done);
+          if (!done) {
+            ok = false;
+            break;
+          }
+          if (lane == 0) store_release(p.ws_flags + blockIdx.x, p.epoch);
+        }
+        part_phase ^= 1u;
+        ++units;
+        continue;
+      }
+      if (p.stream_k && sg.i_end < p.nq) {
+        // Owner of a cut unit: add the partials of the CTAs that took the
+        // rest of its steps, in CTA order (a fixed order: dV and dK do not
+        // depend on timing), 32 columns at a time, then write dV and dK.
+        int last_c = blockIdx.x;
+        while (last_c + 1 < static_cast<int>(gridDim.x) && bwd_share_begin(p, last_c + 1) < sg.unit_end) ++last_c;
+        bool fine = true;
+        for (int cb = blockIdx.x + 1; cb <= last_c && fine; ++cb)
+          fine = wait_flag(p.ws_flags + cb, p.epoch, wd, kSiteBwdPartFlag);
+        fine = __all_sync(0xffffffffu, fine);
+        if (!fine) {
+          ok = false;
+          break;
+        }
+#pragma unroll 1
+        for (int cc = 0; cc < kHalf; cc += 32) {
+          uint32_t a[32], b[32];
+          tmem_ld32x32_wait(tmem + lane_off + L::kColDV + wg * kHalf + cc, a);
+          tmem_ld32x32_wait(tmem + lane_off + L::kColDK + wg * kHalf + cc, b);
+          float fa[32], fb[32];
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            fa[i] = __uint_as_float(a[i]);
+            fb[i] = __uint_as_float(b[i]);
+          }
+#pragma unroll 1
+          for (int cb = blockIdx.x + 1; cb <= last_c; ++cb) {
+            const float* pv = p.ws_part + static_cast<size_t>(cb) * 2 * D * 128 + (wg * kHalf + cc) * 128 + rr;
+            const float* pkk = pv + D * 128;
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+              fa[i] += __ldcg(pv + i * 128);
+              fb[i] += __ldcg(pkk + i * 128);
+            }
+          }
+          if (key_ok) {
+            uint4* dvp = reinterpret_cast<uint4*>(reinterpret_cast<uint8_t*>(p.dv) + out_off + cc * 2);
+            uint4* dkp = reinterpret_cast<uint4*>(reinterpret_cast<uint8_t*>(p.dk) + out_off + cc * 2);
+            const float sc = p.scale;
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              const float* x = fa + 8 * q;
+              const float* y = fb + 8 * q;
+              dvp[q] = make_uint4(pack2(x[0], x[1], kBf16), pack2(x[2], x[3], kBf16), pack2(x[4], x[5], kBf16),
+                                  pack2(x[6], x[7], kBf16));
+              dkp[q] = make_uint4(pack2(y[0] * sc, y[1] * sc, kBf16), pack2(y[2] * sc, y[3] * sc, kBf16),
+                                  pack2(y[4] * sc, y[5] * sc, kBf16), pack2(y[6] * sc, y[7] * sc, kBf16));
+            }
+          }
+        }
+        tc_fence_before_sync();
+        mbar_arrive(bar_acc_free);
+        ++units;
+        continue;
+      }
       uint32_t dv[kHalf], dkr[kHalf];
 #pragma unroll
       for (int cc = 0; cc < kHalf; cc += 32) {
@@ -686,8 +856,19 @@ cudaError_t launch_bwd(const CUtensorMap& k, const CUtensorMap& v, const CUtenso
   const int smem = BwdLayout<D>::kSmemBytes;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  kern<<<grid, kBwdThreads, smem, stream>>>(k, v, q, dout, dq_acc, p);
-  return cudaGetLastError();
+  // The stream-K schedule waits across CTAs, so it is launched cooperatively
+  // (the whole grid resident at once, or the launch fails).
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(kBwdThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = p.stream_k ? 1 : 0;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, k, v, q, dout, dq_acc, p);
 }
 
 }  // namespace fa2

@@ -460,9 +460,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         __stcg(ps + 256 + rr, l_o);
         __threadfence();
         mbar_arrive(bar_part);
-        if (rr == 0) {
-          if (!wait_bounded(bar_part, part_phase, wd, kSitePartialWrite)) break;
-          store_release(p.ws_flags + slot, p.epoch);
+        if (rr < 32) {  // the first warp waits as a whole, so that it stays converged
+          bool done = wait_bounded(bar_part, part_phase, wd, kSitePartialWrite);
+          done = __all_sync(0xffffffffu, done);
+          if (!done) break;
+          if (rr == 0) store_release(p.ws_flags + slot, p.epoch);
         }
         part_phase ^= 1u;
         tc_fence_before_sync();

@@ -69,7 +69,22 @@ struct BwdParams {
   int num_units;            // BH * nkv
   float scale_log2;         // scale * log2(e)
   float scale;
+  // Schedule. 0: whole units dealt to CTAs in rounds. 1 (stream-K): CTA b
+  // takes query steps [total*b/G, total*(b+1)/G) of the unit sequence
+  // (heads in order, K/V tiles ascending); a unit cut between CTAs is
+  // finished by the CTA holding its first steps, which adds the partial dK,
+  // dV the following CTAs left in the workspace.
+  int stream_k;
+  long long steps_per_head; // query steps of all units of one head
+  long long total_steps;    // BH * steps_per_head
+  float* ws_part;           // [G][2][D][128] fp32 partial dV, dK (unscaled) of a cut unit
+  unsigned long long* ws_flags;  // [G] = epoch once that partial is written
+  unsigned long long epoch; // unique tag of this launch
 };
+
+// CTAs of the backward's stream-K schedule at most (its partial slots are
+// part of the caller's workspace, which is sized without a device).
+constexpr int kBwdMaxCtas = 160;
 
 // Bytes of stream-K workspace for `grid` CTAs at head dimension d.
 constexpr size_t stream_k_workspace_bytes(int grid, int d) {
@@ -87,6 +102,10 @@ int launch_forward(const void* Q, const void* K, const void* V, void* O, float* 
 // Records `e` as the calling thread's last CUDA error (fa2_last_cuda_error)
 // and returns FA2_ERR_CUDA.
 int record_cuda_error(cudaError_t e);
+
+// A tag no earlier launch of this process (or of another one) has used, for
+// the flags of cross-CTA partial results.
+unsigned long long next_launch_epoch();
 
 // Shared with the backward pass: the current device's SM count and watchdog
 // word (FA2_ERR_UNSUPPORTED unless it is a compute-capability 10.3 GPU), a

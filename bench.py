@@ -475,7 +475,7 @@ def run_gb300_bwd(args, w, rank, world, local):
     def step(i):
         qd, kd, vd, od, ld, dod, outs, ws = sets[i % nsets]
         fa2.attention_backward(qd, kd, vd, od, ld, dod, scale=w.scale, is_causal=w.causal, dq=outs[0], dk=outs[1],
-                               dv=outs[2], workspace=ws, stream=stream)
+                               dv=outs[2], workspace=ws, stream=stream, schedule=args.schedule)
 
     clocks = ClockSampler(local)
     clocks.start()
@@ -524,7 +524,9 @@ def run_gb300_bwd(args, w, rank, world, local):
         "data": "synthetic (seeded N(0, sigma^2) Q, K, V and dO, cast to the workload's 16-bit dtype; "
                 "O and LSE from fa2_fwd)",
         "config": {"workload": w.describe(), "B": w.B, "H": w.H, "N": w.N, "D": w.D, "causal": w.causal,
-                   "scale": "1/sqrt(D)", "parallelism": f"weak x{world} (one independent replica per GPU)",
+                   "scale": "1/sqrt(D)", "schedule": args.schedule + (" (the library's choice)"
+                                                                      if args.schedule == "auto" else ""),
+                   "parallelism": f"weak x{world} (one independent replica per GPU)",
                    "l2": f"inputs rotate over {nsets} copies ({nsets * set_bytes / 2**20:.0f} MiB > 2x L2)"},
         "pct_of_peak": 100.0 * achieved / peak,
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",

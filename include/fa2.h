@@ -36,6 +36,11 @@ struct CUstream_st; /* the same type as cudaStream_t / CUstream */
 #define FA2_F16 0  /* IEEE binary16 inputs and output */
 #define FA2_BF16 1 /* bfloat16 inputs and output      */
 
+/* schedule codes of fa2_bwd_sched */
+#define FA2_SCHED_AUTO 0     /* the one with less work on the busiest SM (what fa2_bwd uses) */
+#define FA2_SCHED_UNITS 1    /* whole K/V tiles dealt to the SMs in rounds */
+#define FA2_SCHED_BALANCED 2 /* equal query steps per SM; tiles cut between SMs are merged */
+
 /* status codes (0 = success, negative = error) */
 #define FA2_OK 0
 #define FA2_ERR_INVALID_ARG (-1) /* null pointer, negative size, bad scale, overlapping O/LSE/inputs, size overflow */
@@ -196,8 +201,10 @@ int fa2_fwd_host(const void* Q, const void* K, const void* V, void* O, float* LS
 
 /*
  * fa2_bwd_workspace_bytes — bytes of device workspace fa2_bwd needs for these
- * sizes: an fp32 dQ accumulator [B, H, N, D] and two fp32 row statistics of
- * B*H*ceil(N/64)*64 entries each, every part rounded up to 256 bytes.
+ * sizes: an fp32 dQ accumulator [B, H, N, D], two fp32 row statistics of
+ * B*H*ceil(N/64)*64 entries each, and the balanced schedule's partial
+ * results (160 slots of 2*128*D floats) and their 160 8-byte flags, every
+ * part rounded up to 256 bytes.
  * Returns FA2_OK, FA2_ERR_INVALID_ARG (bytes NULL or a negative size) or
  * FA2_ERR_UNSUPPORTED (D not 64 or 128). Needs no device.
  */
@@ -241,6 +248,29 @@ int fa2_bwd(const void* Q, const void* K, const void* V, const void* O, const vo
             const float* LSE, void* dQ, void* dK, void* dV,
             int B, int H, int N, int D, float scale, int is_causal, int dtype,
             void* workspace, size_t workspace_bytes, struct CUstream_st* stream);
+
+/*
+ * fa2_bwd_sched — fa2_bwd with the work schedule of its main kernel chosen
+ * by the caller (fa2_bwd is this call with FA2_SCHED_AUTO):
+ *   FA2_SCHED_UNITS: each SM takes whole K/V tiles (all their query steps)
+ *     in rounds; with B*H*ceil(N/128) tiles not a multiple of the SM count
+ *     the last round leaves SMs idle.
+ *   FA2_SCHED_BALANCED: each SM (at most 160 of them) takes an equal share
+ *     of all (K/V tile, query step) pairs; a tile cut between SMs is
+ *     finished by the SM holding its first steps, which adds the fp32
+ *     partial dK, dV of the others (left in the workspace) before writing
+ *     dK and dV. The launch is cooperative (all SMs' blocks resident); if
+ *     that cannot be arranged the call returns FA2_ERR_CUDA.
+ *   FA2_SCHED_AUTO: the one whose busiest SM has fewer query steps
+ *     (balanced only if at least 5 % fewer).
+ * The results are the same up to fp32 summation order; each schedule is
+ * deterministic for dK and dV. Errors as fa2_bwd, plus FA2_ERR_INVALID_ARG
+ * for an unknown schedule code.
+ */
+int fa2_bwd_sched(const void* Q, const void* K, const void* V, const void* O, const void* dO,
+                  const float* LSE, void* dQ, void* dK, void* dV,
+                  int B, int H, int N, int D, float scale, int is_causal, int dtype,
+                  void* workspace, size_t workspace_bytes, int schedule, struct CUstream_st* stream);
 
 /*
  * fa2_device_status — read the device-side watchdog word of the current

@@ -242,14 +242,30 @@ def test_backward_rejects_bad_arguments_before_any_gpu_work(lib, over, code):
 def test_backward_empty_problem_and_workspace_size(lib):
     assert call_bwd(lib, B=0) == lib.FA2_OK
     assert call_bwd(lib, N=0, Q=None, ws=None) == lib.FA2_OK
-    # fp32 dQ accumulator [B,H,N,D] + LSE*log2(e) and Delta rows padded to 64, each rounded to 256 bytes
+    # fp32 dQ accumulator [B,H,N,D] + LSE*log2(e) and Delta rows padded to 64 + the balanced schedule's
+    # 160 partial slots of 2*128*D floats and their 160 flags, each rounded to 256 bytes
     r256 = lambda x: -(-x // 256) * 256  # noqa: E731
     for (B, H, N, D) in ((1, 2, 64, 64), (2, 12, 1000, 64), (1, 8, 8192, 128), (1, 1, 1, 128)):
         npad = -(-N // 64) * 64
-        assert lib.fa2_bwd_workspace_bytes(B, H, N, D) == r256(B * H * N * D * 4) + 2 * r256(B * H * npad * 4)
+        assert lib.fa2_bwd_workspace_bytes(B, H, N, D) == (r256(B * H * N * D * 4) + 2 * r256(B * H * npad * 4)
+                                                           + r256(160 * 2 * 128 * D * 4) + r256(160 * 8))
     n = ctypes.c_size_t(0)
     assert lib.library().fa2_bwd_workspace_bytes(1, 1, 64, 96, ctypes.byref(n)) == lib.FA2_ERR_UNSUPPORTED
     assert lib.library().fa2_bwd_workspace_bytes(1, 1, 64, 64, None) == lib.FA2_ERR_INVALID_ARG
+
+
+def test_backward_schedule_codes(lib):
+    a = dict(BWD)
+    args = [a[x] for x in ("Q", "K", "V", "O", "dO", "LSE", "dQ", "dK", "dV", "B", "H", "N", "D", "scale",
+                           "is_causal", "dtype", "ws", "nws")]
+    so = lib.library()
+    for bad in (-1, 3, 7):
+        assert so.fa2_bwd_sched(*args, bad, None) == lib.FA2_ERR_INVALID_ARG
+    assert so.fa2_bwd_sched(*args[:9], 0, *args[10:], lib.FA2_SCHED_BALANCED, None) == lib.FA2_OK  # B = 0
+    assert (lib.FA2_SCHED_AUTO, lib.FA2_SCHED_UNITS, lib.FA2_SCHED_BALANCED) == (0, 1, 2)
+    q = torch.zeros(1, 1, 8, 64, dtype=torch.float16)
+    with pytest.raises(ValueError):
+        lib.attention_backward(q, q, q, q, torch.zeros(1, 1, 8), q, schedule="fastest")
 
 
 @pytest.mark.skipif(torch.cuda.is_available(), reason="only meaningful on a host without a GPU")

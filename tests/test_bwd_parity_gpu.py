@@ -36,14 +36,14 @@ def fa2():
     return m
 
 
-def run_gpu(fa2, w, q, k, v, do, stream=None, outs=None, workspace=None):
+def run_gpu(fa2, w, q, k, v, do, stream=None, outs=None, workspace=None, schedule="auto"):
     qd, kd, vd, dod = (t.cuda() for t in (q, k, v, do))
     O, L = fa2.attention_forward(qd, kd, vd, scale=w.scale, is_causal=w.causal)
     kw = {}
     if outs is not None:
         kw = dict(dq=outs[0], dk=outs[1], dv=outs[2])
     grads = fa2.attention_backward(qd, kd, vd, O, L, dod, scale=w.scale, is_causal=w.causal, stream=stream,
-                                   workspace=workspace, **kw)
+                                   workspace=workspace, schedule=schedule, **kw)
     torch.cuda.synchronize()
     assert fa2.fa2_device_status(clear=True) == 0, "device watchdog fired"
     return dict(zip(("dq", "dk", "dv"), grads))
@@ -67,10 +67,10 @@ def check(w, gpu, ref, heads=None):
     return worst
 
 
-def compare(fa2, oracle_mod, w, heads=None):
+def compare(fa2, oracle_mod, w, heads=None, schedule="auto"):
     q, k, v = workloads.make_inputs(w)
     do = workloads.make_grad_output(w)
-    gpu = run_gpu(fa2, w, q, k, v, do)
+    gpu = run_gpu(fa2, w, q, k, v, do, schedule=schedule)
     ref = oracle_mod.attention_bwd(q, k, v, do, w.scale, w.causal, heads=heads, magnitudes=True)
     return check(w, gpu, ref, heads)
 
@@ -82,18 +82,32 @@ def test_tiny_every_element(fa2, oracle_mod):
 EDGE_N = [1, 7, 63, 64, 65, 127, 128, 129, 255, 257, 1000]
 
 
+SCHEDULES = ("units", "balanced")
+
+
 @pytest.mark.parametrize("N", EDGE_N)
 @pytest.mark.parametrize("D", [64, 128])
 @pytest.mark.parametrize("dtype", ["f16", "bf16"])
 @pytest.mark.parametrize("causal", [False, True])
-def test_edge_shapes_every_element(fa2, oracle_mod, N, D, dtype, causal):
-    compare(fa2, oracle_mod, workloads.custom(1, 2, N, D, dtype, causal, seed=N * 11 + D))
+@pytest.mark.parametrize("schedule", SCHEDULES)
+def test_edge_shapes_every_element(fa2, oracle_mod, N, D, dtype, causal, schedule):
+    compare(fa2, oracle_mod, workloads.custom(1, 2, N, D, dtype, causal, seed=N * 11 + D), schedule=schedule)
 
 
 @pytest.mark.parametrize("causal", [False, True])
-def test_many_units_per_cta(fa2, oracle_mod, causal):
+@pytest.mark.parametrize("schedule", SCHEDULES)
+def test_many_units_per_cta(fa2, oracle_mod, causal, schedule):
     """160 K/V tiles on at most 152 CTAs: units after the first reuse TMEM, the ring and barriers."""
-    compare(fa2, oracle_mod, workloads.custom(1, 40, 512, 64, "bf16", causal, seed=77))
+    compare(fa2, oracle_mod, workloads.custom(1, 40, 512, 64, "bf16", causal, seed=77), schedule=schedule)
+
+
+@pytest.mark.parametrize("shape", [(1, 1, 4096, 128, False), (1, 2, 3000, 128, True), (1, 3, 2049, 64, False),
+                                   (2, 1, 8192, 64, True), (1, 1, 700, 128, False)])
+def test_units_cut_across_many_ctas(fa2, oracle_mod, shape):
+    """Balanced schedule with few query steps per CTA: one K/V tile's steps are split over several CTAs
+    and its owner adds several partial dK, dV (every element checked)."""
+    B, H, N, D, causal = shape
+    compare(fa2, oracle_mod, workloads.custom(B, H, N, D, "bf16", causal, seed=N + D + 5), schedule="balanced")
 
 
 @pytest.mark.parametrize("D", [64, 128])
@@ -116,9 +130,11 @@ def test_contract_workloads_full_size(fa2, oracle_mod, name):
     compare(fa2, oracle_mod, w, heads=heads)
 
 
-def test_workspace_and_outputs_may_hold_garbage(fa2, oracle_mod):
-    """The workspace (fp32 accumulator, row statistics) and the outputs start as NaN bytes:
-    every output element is written and the accumulator is cleared by the call itself."""
+@pytest.mark.parametrize("schedule", SCHEDULES)
+def test_workspace_and_outputs_may_hold_garbage(fa2, oracle_mod, schedule):
+    """The workspace (fp32 accumulator, row statistics, partial slots and flags) and the outputs start
+    as NaN bytes: every output element is written, the accumulator is cleared by the call itself and
+    no stale flag is taken for a partial of this call."""
     w = workloads.custom(1, 3, 333, 128, "bf16", True, seed=80)
     q, k, v = workloads.make_inputs(w)
     do = workloads.make_grad_output(w)
@@ -126,10 +142,10 @@ def test_workspace_and_outputs_may_hold_garbage(fa2, oracle_mod):
     ws = torch.full((need,), 0xFF, dtype=torch.uint8, device="cuda")
     outs = [torch.full(q.shape, float("nan"), dtype=q.dtype, device="cuda") for _ in range(3)]
     ref = oracle_mod.attention_bwd(q, k, v, do, w.scale, w.causal, magnitudes=True)
-    first = run_gpu(fa2, w, q, k, v, do, outs=outs, workspace=ws)
+    first = run_gpu(fa2, w, q, k, v, do, outs=outs, workspace=ws, schedule=schedule)
     check(w, first, ref)
     keep = {n: t.clone() for n, t in first.items()}
-    second = run_gpu(fa2, w, q, k, v, do, outs=outs, workspace=ws)
+    second = run_gpu(fa2, w, q, k, v, do, outs=outs, workspace=ws, schedule=schedule)
     check(w, second, ref)
     # dK and dV are summed in one fixed order; dQ by atomics (order may vary)
     assert torch.equal(keep["dk"], second["dk"]) and torch.equal(keep["dv"], second["dv"])
