@@ -93,8 +93,9 @@ __device__ __forceinline__ uint32_t pack_pair(float lo, float hi, bool bf16) {
 // Per row (b, h, i) of the padded [B*H, Npad] grid: Delta_i = <dO_i, O_i>
 // and LSE_i * log2(e) (rows >= N: 0 and +inf, so the main kernel's P is 0
 // there), and zeroes the row of the fp32 dQ accumulator. D/8 threads per
-// row, 8 elements (16 bytes) each; the loop bound is a multiple of 32 so that
-// whole warps take part in the row reduction.
+// row, 8 elements (16 bytes) each, in groups of kLanes (D/8 rounded up to a
+// power of two: the shuffle reduction's width; the extra lanes add zero);
+// the loop bound is a multiple of 32 so that whole warps take part.
 template <int D, bool kBf16>
 __global__ void __launch_bounds__(kElemThreads) fa2_bwd_prologue(const uint4* __restrict__ O,
                                                                  const uint4* __restrict__ dO,
@@ -102,17 +103,19 @@ __global__ void __launch_bounds__(kElemThreads) fa2_bwd_prologue(const uint4* __
                                                                  float* __restrict__ dq_acc, float* __restrict__ lse2,
                                                                  float* __restrict__ delta, int N, int Npad,
                                                                  long long rows) {
-  constexpr int kPer = D / 8;  // threads per row
-  const long long items = rows * kPer;
+  constexpr int kPer = D / 8;  // threads with data per row
+  constexpr int kLanes = kPer <= 4 ? 4 : (kPer <= 8 ? 8 : (kPer <= 16 ? 16 : 32));
+  static_assert(kPer <= 32, "head dimension");
+  const long long items = rows * kLanes;
   const long long bound = (items + 31) / 32 * 32;
   const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
   for (long long idx = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; idx < bound; idx += stride) {
-    const long long row = idx / kPer;
-    const int part = static_cast<int>(idx % kPer);
+    const long long row = idx / kLanes;
+    const int part = static_cast<int>(idx % kLanes);
     const bool live = idx < items;
     const long long bh = live ? row / Npad : 0;
     const int i = live ? static_cast<int>(row % Npad) : 0;
-    const bool real = live && i < N;
+    const bool real = live && i < N && part < kPer;
     float acc = 0.f;
     if (real) {
       const long long e = (bh * N + i) * kPer + part;  // in 16-byte units
@@ -126,10 +129,11 @@ __global__ void __launch_bounds__(kElemThreads) fa2_bwd_prologue(const uint4* __
       z[1] = make_float4(0.f, 0.f, 0.f, 0.f);
     }
 #pragma unroll
-    for (int off = kPer / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off, kPer);
+    for (int off = kLanes / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off, kLanes);
     if (live && part == 0) {
-      delta[row] = real ? acc : 0.f;
-      lse2[row] = real ? LSE[bh * N + i] * 1.4426950408889634f : CUDART_INF_F;
+      const bool in_range = i < N;
+      delta[row] = in_range ? acc : 0.f;
+      lse2[row] = in_range ? LSE[bh * N + i] * 1.4426950408889634f : CUDART_INF_F;
     }
   }
 }
@@ -150,14 +154,20 @@ __global__ void __launch_bounds__(kElemThreads) fa2_bwd_dq_convert(const float4*
 using BwdLaunchFn = cudaError_t (*)(const CUtensorMap&, const CUtensorMap&, const CUtensorMap&, const CUtensorMap&,
                                     const CUtensorMap&, const BwdParams&, int, cudaStream_t);
 
+template <int D>
+BwdLaunchFn pick_bwd_d(bool bf, bool c) {
+  if (bf) return c ? launch_bwd<D, true, true> : launch_bwd<D, true, false>;
+  return c ? launch_bwd<D, false, true> : launch_bwd<D, false, false>;
+}
+
 BwdLaunchFn pick_bwd(int d, int dtype, int causal) {
   const bool bf = dtype == FA2_BF16, c = causal != 0;
-  if (d == 64) {
-    if (bf) return c ? launch_bwd<64, true, true> : launch_bwd<64, true, false>;
-    return c ? launch_bwd<64, false, true> : launch_bwd<64, false, false>;
+  switch (d) {
+    case 32: return pick_bwd_d<32>(bf, c);
+    case 64: return pick_bwd_d<64>(bf, c);
+    case 96: return pick_bwd_d<96>(bf, c);
+    default: return pick_bwd_d<128>(bf, c);
   }
-  if (bf) return c ? launch_bwd<128, true, true> : launch_bwd<128, true, false>;
-  return c ? launch_bwd<128, false, true> : launch_bwd<128, false, false>;
 }
 
 template <int D>
@@ -185,7 +195,7 @@ using namespace fa2;
 
 extern "C" int fa2_bwd_workspace_bytes(int B, int H, int N, int D, size_t* bytes) {
   if (!bytes || B < 0 || H < 0 || N < 0) return FA2_ERR_INVALID_ARG;
-  if (D != 64 && D != 128) return FA2_ERR_UNSUPPORTED;
+  if (!bwd_head_dim_ok(D)) return FA2_ERR_UNSUPPORTED;
   *bytes = workspace_layout(static_cast<int64_t>(B) * H, N, D).total;
   return FA2_OK;
 }
@@ -197,7 +207,7 @@ extern "C" int fa2_bwd_sched(const void* Q, const void* K, const void* V, const 
   if (B < 0 || H < 0 || N < 0) return FA2_ERR_INVALID_ARG;
   if (schedule != FA2_SCHED_AUTO && schedule != FA2_SCHED_UNITS && schedule != FA2_SCHED_BALANCED)
     return FA2_ERR_INVALID_ARG;
-  if (D != 64 && D != 128) return FA2_ERR_UNSUPPORTED;
+  if (!bwd_head_dim_ok(D)) return FA2_ERR_UNSUPPORTED;
   if (dtype != FA2_F16 && dtype != FA2_BF16) return FA2_ERR_UNSUPPORTED;
   if (!std::isfinite(scale) || !(scale > 0.f)) return FA2_ERR_INVALID_ARG;
   if (B == 0 || H == 0 || N == 0) return FA2_OK;
@@ -251,8 +261,13 @@ extern "C" int fa2_bwd_sched(const void* Q, const void* K, const void* V, const 
 
   const long long rows = bh * npad;
   const int pgrid = grid_for(rows * (D / 8), sms);
-  cudaError_t e = D == 64 ? launch_prologue<64>(bf, O, dO, LSE, dq_acc, lse2, delta, N, npad, rows, pgrid, s)
-                          : launch_prologue<128>(bf, O, dO, LSE, dq_acc, lse2, delta, N, npad, rows, pgrid, s);
+  cudaError_t e;
+  switch (D) {
+    case 32: e = launch_prologue<32>(bf, O, dO, LSE, dq_acc, lse2, delta, N, npad, rows, pgrid, s); break;
+    case 64: e = launch_prologue<64>(bf, O, dO, LSE, dq_acc, lse2, delta, N, npad, rows, pgrid, s); break;
+    case 96: e = launch_prologue<96>(bf, O, dO, LSE, dq_acc, lse2, delta, N, npad, rows, pgrid, s); break;
+    default: e = launch_prologue<128>(bf, O, dO, LSE, dq_acc, lse2, delta, N, npad, rows, pgrid, s); break;
+  }
   if (e != cudaSuccess) return record_cuda_error(e);
 
   BwdParams p = {};

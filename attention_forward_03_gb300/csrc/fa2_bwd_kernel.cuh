@@ -21,8 +21,9 @@
 // Layout of one CTA (one per SM, persistent over work units = K/V tiles, or
 // over segments of them, see below):
 //   warps 0-7  two compute warpgroups; thread = key row = TMEM lane, warpgroup
-//              g takes query columns [32g, 32g+32) of every step (and the
-//              halves [gD/2, (g+1)D/2) of the dK / dV rows in the epilogue)
+//              g takes query columns [32g, 32g+32) of every step (and, in
+//              the epilogue, the dK / dV row's 32-column chunks: the first
+//              half of them, rounded up, for g = 0, the rest for g = 1)
 //   warp  8    tcgen05 MMA issuer (one thread), owns the TMEM allocation
 //   warp  9    non-causal launches: a second issuer. Warp 8 then issues the
 //              score products S^T, dP^T and warp 9 the gradient products dV,
@@ -31,11 +32,13 @@
 //              diagonal, keep one issuer that computes the next step's
 //              scores before the current step's gradients)
 //   warp  10   TMA producer (one thread)
+// Head dims 32 and 96 run in the tiles of 64 and 128 (Dp below): their
+// columns past D arrive as zeros from the copy engine, so they add nothing.
 // Tensor memory (fp32 columns x 128 lanes):
-//   [0, D)          dV accumulator        [D, 2D)        dK accumulator
-//   [2D, 2D+64)     S^T of the step       [2D+64, 2D+128) dP^T of the step
-//   [2D+128, 2D+192) dQ^T of the step (lane = head-dim index; at D = 64 the
-//                   MMA runs with M = 128 and lanes 64-127 are discarded)
+//   [0, D)          dV accumulator        [Dp, Dp+D)     dK accumulator
+//   [2Dp, 2Dp+64)   S^T of the step       [2Dp+64, 2Dp+128) dP^T of the step
+//   [2Dp+128, 2Dp+192) dQ^T of the step (lane = head-dim index; the MMA
+//                   runs with M = 128 and the lanes from D on are discarded)
 // Shared memory (128-byte swizzled, 64-element panels): K and V of the tile
 // (resident for the unit), a ring of query steps (Q_i, dO_i, and the 64
 // LSE*log2(e) and Delta values), the 16-bit P^T and dS^T of the step
@@ -91,10 +94,23 @@ enum : int {
 
 template <int D>
 struct BwdLayout {
-  static constexpr int kPanels = D / 64;
-  static constexpr int kKVBytes = kPanels * kPanelBytes;      // K or V tile: 128 rows x D
-  static constexpr int kQBytes = kPanels * kBwdQPanelBytes;   // Q or dO step: 64 rows x D
-  static constexpr int kStages = (D == 128) ? 3 : 6;
+  static_assert(bwd_head_dim_ok(D), "head dimension");
+  // D = 32 and 96 use the tiles of 64 and 128: their columns past D read as
+  // zeros (the copy engine's out-of-bounds fill) and add nothing
+  static constexpr int kPanels = (D + 63) / 64;
+  static constexpr int kDp = kPanels * 64;                    // padded head dimension
+  // N of the dV, dK products (the O columns accumulated). At D = 32 it stays
+  // 64: a 32-wide MN-major operand would cover half of a 128-byte swizzle
+  // row, a form the operand layouts do not describe.
+  static constexpr int kNacc = (D == 32) ? 64 : D;
+  static constexpr int kKVBytes = kPanels * kPanelBytes;      // K or V tile: 128 rows x Dp
+  static constexpr int kQBytes = kPanels * kBwdQPanelBytes;   // Q or dO step: 64 rows x Dp
+  static constexpr int kStages = (kPanels == 2) ? 3 : 6;
+  // Epilogue: a key row's D columns in chunks of 32, the first kChunksWg for
+  // compute warpgroup 0 and the rest for warpgroup 1.
+  static constexpr int kChunks = D / 32;
+  static constexpr int kChunksWg = (kChunks + 1) / 2;
+  static_assert(32 * 2 * kChunksWg <= kDp, "epilogue chunks stay inside the padded dV / dK columns");
   static constexpr int kStageBytes = 2 * kQBytes;             // Q then dO
   static constexpr int kK = 0;
   static constexpr int kV = kKVBytes;
@@ -110,10 +126,10 @@ struct BwdLayout {
   static constexpr int kMisc = kBars + kNumBars * 8;
   static constexpr int kSmemBytes = kMisc + 16 + 1024;  // + slack for 1 KB alignment
   static constexpr uint32_t kColDV = 0;
-  static constexpr uint32_t kColDK = D;
-  static constexpr uint32_t kColS = 2 * D;
-  static constexpr uint32_t kColDP = 2 * D + kBwdRows;
-  static constexpr uint32_t kColDQ = 2 * D + 2 * kBwdRows;
+  static constexpr uint32_t kColDK = kDp;
+  static constexpr uint32_t kColS = 2 * kDp;
+  static constexpr uint32_t kColDP = 2 * kDp + kBwdRows;
+  static constexpr uint32_t kColDQ = 2 * kDp + 2 * kBwdRows;
   static_assert(kColDQ + kBwdRows <= kTmemCols, "TMEM budget");
   static_assert(kSmemBytes <= 232448, "shared memory budget");
   static_assert(kRing % 1024 == 0 && kP % 1024 == 0 && kDS % 1024 == 0, "swizzled tiles need 1 KB alignment");
@@ -367,7 +383,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     // --------------------------------------------------------- MMA issuers
     if (lane == 0) {
       constexpr uint32_t idesc_s = make_idesc_f16(kBf16, kBwdRows, false);            // S^T, dP^T: N = 64
-      constexpr uint32_t idesc_acc = make_idesc_f16(kBf16, D, true);                  // dV, dK: N = D
+      constexpr uint32_t idesc_acc = make_idesc_f16(kBf16, L::kNacc, true);           // dV, dK: N = D (64 at D = 32)
       constexpr uint32_t idesc_dq = make_idesc_f16_ab(kBf16, kBwdRows, true, true);   // dQ^T: N = 64
       constexpr uint32_t kHi = desc_hi_sw128(1024);  // 8-row (K-major) / 8-row-of-K (MN-major) groups 1 KB apart
       // S^T = K Q_i^T and dP^T = V dO_i^T: A = K / V (K-major, 128-row
@@ -602,7 +618,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       if (!got) return false;
       tc_fence_after_sync();
       uint32_t v[32];
-      if (dq_rows) tmem_ld32x32_wait(tDQ, v);
+      // every warp loads (lanes from D on hold the discarded rows; a load
+      // guarded by dq_rows made the compiler spill at D = 32 and 96), only
+      // the warps with real head-dim rows store below
+      tmem_ld32x32_wait(tDQ, v);
       tc_fence_before_sync();
       mbar_arrive(bar_dq_free);
       if (drains > 0) {
@@ -718,8 +737,26 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         break;
       }
       tc_fence_after_sync();
-      constexpr int kHalf = D / 2;
-      const size_t out_off = (static_cast<size_t>(bh) * p.N + (key_ok ? key : 0)) * (D * 2) + wg * kHalf * 2;
+      // This warpgroup's share of the key row: 32-column chunks [c0, c0 + n_my).
+      constexpr int kMy = L::kChunksWg;
+      const int c0 = wg * kMy;
+      const int n_my = min(kMy, L::kChunks - c0);  // warp-uniform
+      const size_t out_row = (static_cast<size_t>(bh) * p.N + (key_ok ? key : 0)) * (D * 2);
+      // Writes 32 columns (chunk c) of this key row of dV and dK (dK scaled).
+      auto store_chunk = [&](int c, const float (&a)[32], const float (&b)[32]) {
+        uint4* dvp = reinterpret_cast<uint4*>(reinterpret_cast<uint8_t*>(p.dv) + out_row + c * 64);
+        uint4* dkp = reinterpret_cast<uint4*>(reinterpret_cast<uint8_t*>(p.dk) + out_row + c * 64);
+        const float sc = p.scale;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const float* x = a + 8 * q;
+          const float* y = b + 8 * q;
+          dvp[q] = make_uint4(pack2(x[0], x[1], kBf16), pack2(x[2], x[3], kBf16), pack2(x[4], x[5], kBf16),
+                              pack2(x[6], x[7], kBf16));
+          dkp[q] = make_uint4(pack2(y[0] * sc, y[1] * sc, kBf16), pack2(y[2] * sc, y[3] * sc, kBf16),
+                              pack2(y[4] * sc, y[5] * sc, kBf16), pack2(y[6] * sc, y[7] * sc, kBf16));
+        }
+      };
       if (p.stream_k && sg.i_begin > bwd_first_step<kCausal>(kv)) {
         // Not the unit's first steps: hand this CTA's partial dV, dK to the
         // unit's owner through its workspace slot ([2][D][128], column-major
@@ -727,15 +764,14 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         float* pv = p.ws_part + static_cast<size_t>(blockIdx.x) * 2 * D * 128;
         float* pkk = pv + D * 128;
 #pragma unroll 1
-        for (int cc = 0; cc < kHalf; cc += 32) {
+        for (int c = c0; c < c0 + n_my; ++c) {
           uint32_t a[32], b[32];
-          tmem_ld32x32_wait(tmem + lane_off + L::kColDV + wg * kHalf + cc, a);
-          tmem_ld32x32_wait(tmem + lane_off + L::kColDK + wg * kHalf + cc, b);
+          tmem_ld32x32_wait(tmem + lane_off + L::kColDV + 32 * c, a);
+          tmem_ld32x32_wait(tmem + lane_off + L::kColDK + 32 * c, b);
 #pragma unroll
           for (int i = 0; i < 32; ++i) {
-            const int col = wg * kHalf + cc + i;
-            __stcg(pv + col * 128 + rr, __uint_as_float(a[i]));
-            __stcg(pkk + col * 128 + rr, __uint_as_float(b[i]));
+            __stcg(pv + (32 * c + i) * 128 + rr, __uint_as_float(a[i]));
+            __stcg(pkk + (32 * c + i) * 128 + rr, __uint_as_float(b[i]));
           }
         }
         tc_fence_before_sync();
@@ -770,10 +806,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           break;
         }
 #pragma unroll 1
-        for (int cc = 0; cc < kHalf; cc += 32) {
+        for (int c = c0; c < c0 + n_my; ++c) {
           uint32_t a[32], b[32];
-          tmem_ld32x32_wait(tmem + lane_off + L::kColDV + wg * kHalf + cc, a);
-          tmem_ld32x32_wait(tmem + lane_off + L::kColDK + wg * kHalf + cc, b);
+          tmem_ld32x32_wait(tmem + lane_off + L::kColDV + 32 * c, a);
+          tmem_ld32x32_wait(tmem + lane_off + L::kColDK + 32 * c, b);
           float fa[32], fb[32];
 #pragma unroll
           for (int i = 0; i < 32; ++i) {
@@ -782,7 +818,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           }
 #pragma unroll 1
           for (int cb = blockIdx.x + 1; cb <= last_c; ++cb) {
-            const float* pv = p.ws_part + static_cast<size_t>(cb) * 2 * D * 128 + (wg * kHalf + cc) * 128 + rr;
+            const float* pv = p.ws_part + static_cast<size_t>(cb) * 2 * D * 128 + (32 * c) * 128 + rr;
             const float* pkk = pv + D * 128;
 #pragma unroll
             for (int i = 0; i < 32; ++i) {
@@ -790,47 +826,31 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
               fb[i] += __ldcg(pkk + i * 128);
             }
           }
-          if (key_ok) {
-            uint4* dvp = reinterpret_cast<uint4*>(reinterpret_cast<uint8_t*>(p.dv) + out_off + cc * 2);
-            uint4* dkp = reinterpret_cast<uint4*>(reinterpret_cast<uint8_t*>(p.dk) + out_off + cc * 2);
-            const float sc = p.scale;
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-              const float* x = fa + 8 * q;
-              const float* y = fb + 8 * q;
-              dvp[q] = make_uint4(pack2(x[0], x[1], kBf16), pack2(x[2], x[3], kBf16), pack2(x[4], x[5], kBf16),
-                                  pack2(x[6], x[7], kBf16));
-              dkp[q] = make_uint4(pack2(y[0] * sc, y[1] * sc, kBf16), pack2(y[2] * sc, y[3] * sc, kBf16),
-                                  pack2(y[4] * sc, y[5] * sc, kBf16), pack2(y[6] * sc, y[7] * sc, kBf16));
-            }
-          }
+          if (key_ok) store_chunk(c, fa, fb);
         }
         tc_fence_before_sync();
         mbar_arrive(bar_acc_free);
         ++units;
         continue;
       }
-      uint32_t dv[kHalf], dkr[kHalf];
+      uint32_t dv[32 * kMy], dkr[32 * kMy];
 #pragma unroll
-      for (int cc = 0; cc < kHalf; cc += 32) {
-        tmem_ld32x32_wait(tmem + lane_off + L::kColDV + wg * kHalf + cc, *reinterpret_cast<uint32_t(*)[32]>(dv + cc));
-        tmem_ld32x32_wait(tmem + lane_off + L::kColDK + wg * kHalf + cc, *reinterpret_cast<uint32_t(*)[32]>(dkr + cc));
+      for (int c = 0; c < kMy; ++c) {
+        // loads kMy chunks whatever n_my is: with an odd chunk count the
+        // last one of warpgroup 1 lies past D but inside the dV / dK region
+        // (columns [D, Dp), never stored), and an unguarded load keeps the
+        // arrays in registers
+        tmem_ld32x32_wait(tmem + lane_off + L::kColDV + 32 * (c0 + c), *reinterpret_cast<uint32_t(*)[32]>(dv + 32 * c));
+        tmem_ld32x32_wait(tmem + lane_off + L::kColDK + 32 * (c0 + c), *reinterpret_cast<uint32_t(*)[32]>(dkr + 32 * c));
       }
       tc_fence_before_sync();
       mbar_arrive(bar_acc_free);
       if (key_ok) {
-        const size_t off = (static_cast<size_t>(bh) * p.N + key) * (D * 2) + wg * kHalf * 2;
-        uint4* dvp = reinterpret_cast<uint4*>(reinterpret_cast<uint8_t*>(p.dv) + off);
-        uint4* dkp = reinterpret_cast<uint4*>(reinterpret_cast<uint8_t*>(p.dk) + off);
 #pragma unroll
-        for (int q = 0; q < kHalf / 8; ++q) {
-          const float* a = reinterpret_cast<const float*>(dv + 8 * q);
-          const float* b = reinterpret_cast<const float*>(dkr + 8 * q);
-          dvp[q] = make_uint4(pack2(a[0], a[1], kBf16), pack2(a[2], a[3], kBf16), pack2(a[4], a[5], kBf16),
-                              pack2(a[6], a[7], kBf16));
-          const float s = p.scale;
-          dkp[q] = make_uint4(pack2(b[0] * s, b[1] * s, kBf16), pack2(b[2] * s, b[3] * s, kBf16),
-                              pack2(b[4] * s, b[5] * s, kBf16), pack2(b[6] * s, b[7] * s, kBf16));
+        for (int c = 0; c < kMy; ++c) {
+          if (c < n_my)
+            store_chunk(c0 + c, *reinterpret_cast<const float(*)[32]>(dv + 32 * c),
+                        *reinterpret_cast<const float(*)[32]>(dkr + 32 * c));
         }
       }
       ++units;

@@ -1,7 +1,7 @@
 // Host-visible pieces of the forward and backward kernels: tile constants,
 // the parameter blocks, and the launcher templates (instantiated in
 // fa2_fwd_d32.cu, fa2_fwd_d64.cu, fa2_fwd_d96.cu, fa2_fwd_d128.cu,
-// fa2_fwd_d256.cu, fa2_bwd_d64.cu and fa2_bwd_d128.cu).
+// fa2_fwd_d256.cu and fa2_bwd_d{32,64,96,128}.cu).
 #pragma once
 #include <cuda.h>
 #include <cuda_runtime.h>
@@ -50,6 +50,8 @@ struct Params {
 };
 
 constexpr int kBwdKeys = 128;       // keys per backward work unit (= TMEM lanes)
+// Head dimensions of the backward kernel (32 and 96 in the tiles of 64 and 128).
+constexpr bool bwd_head_dim_ok(int d) { return d == 32 || d == 64 || d == 96 || d == 128; }
 constexpr int kBwdRows = 64;        // query rows per backward step
 
 struct BwdParams {

@@ -206,7 +206,7 @@ int fa2_fwd_host(const void* Q, const void* K, const void* V, void* O, float* LS
  * results (160 slots of 2*128*D floats) and their 160 8-byte flags, every
  * part rounded up to 256 bytes.
  * Returns FA2_OK, FA2_ERR_INVALID_ARG (bytes NULL or a negative size) or
- * FA2_ERR_UNSUPPORTED (D not 64 or 128). Needs no device.
+ * FA2_ERR_UNSUPPORTED (D not 32, 64, 96 or 128). Needs no device.
  */
 int fa2_bwd_workspace_bytes(int B, int H, int N, int D, size_t* bytes);
 
@@ -231,7 +231,8 @@ int fa2_bwd_workspace_bytes(int B, int H, int N, int D, size_t* bytes);
  *           rounded to nearest-even. Must not overlap each other, an input
  *           or the workspace.
  * B, H, N, D, scale, is_causal, dtype: as for fa2_fwd (the same values the
- *           forward was called with), except that D is 64 or 128 only.
+ *           forward was called with), except that D is 32, 64, 96 or 128
+ *           (32 and 96 run in the tiles of 64 and 128, as in the forward).
  * workspace: device memory of at least fa2_bwd_workspace_bytes(B, H, N, D)
  *           bytes, 256-byte aligned, owned by the caller. Its contents on
  *           entry do not matter; it is scratch for the duration of the call

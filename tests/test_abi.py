@@ -225,7 +225,7 @@ def call_bwd(lib, **over):
 
 
 @pytest.mark.parametrize("over,code", [
-    (dict(B=-1), -1), (dict(N=-2), -1), (dict(D=96), -2), (dict(dtype=7), -2),
+    (dict(B=-1), -1), (dict(N=-2), -1), (dict(D=48), -2), (dict(D=256), -2), (dict(dtype=7), -2),
     (dict(scale=0.0), -1), (dict(scale=float("nan")), -1),
     (dict(Q=None), -1), (dict(dO=None), -1), (dict(LSE=None), -1), (dict(dK=None), -1), (dict(ws=None), -1),
     (dict(dO=A * 64 + 8), -3), (dict(dV=A * 128 + 4), -3), (dict(ws=A * 144 + 16), -3),
@@ -250,7 +250,10 @@ def test_backward_empty_problem_and_workspace_size(lib):
         assert lib.fa2_bwd_workspace_bytes(B, H, N, D) == (r256(B * H * N * D * 4) + 2 * r256(B * H * npad * 4)
                                                            + r256(160 * 2 * 128 * D * 4) + r256(160 * 8))
     n = ctypes.c_size_t(0)
-    assert lib.library().fa2_bwd_workspace_bytes(1, 1, 64, 96, ctypes.byref(n)) == lib.FA2_ERR_UNSUPPORTED
+    assert lib.library().fa2_bwd_workspace_bytes(1, 1, 64, 256, ctypes.byref(n)) == lib.FA2_ERR_UNSUPPORTED
+    for D in (32, 96):  # the padded head dims
+        assert lib.fa2_bwd_workspace_bytes(1, 1, 64, D) == (r256(64 * D * 4) + 2 * r256(64 * 4)
+                                                            + r256(160 * 2 * 128 * D * 4) + r256(160 * 8))
     assert lib.library().fa2_bwd_workspace_bytes(1, 1, 64, 64, None) == lib.FA2_ERR_INVALID_ARG
 
 

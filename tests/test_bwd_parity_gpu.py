@@ -94,6 +94,26 @@ def test_edge_shapes_every_element(fa2, oracle_mod, N, D, dtype, causal, schedul
     compare(fa2, oracle_mod, workloads.custom(1, 2, N, D, dtype, causal, seed=N * 11 + D), schedule=schedule)
 
 
+EDGE_N_PADDED = [1, 63, 129, 257, 1000]
+
+
+@pytest.mark.parametrize("N", EDGE_N_PADDED)
+@pytest.mark.parametrize("D", [32, 96])
+@pytest.mark.parametrize("dtype", ["f16", "bf16"])
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("schedule", SCHEDULES)
+def test_padded_head_dims_every_element(fa2, oracle_mod, N, D, dtype, causal, schedule):
+    """Head dims 32 and 96 run in the tiles of 64 and 128 with zero-filled columns."""
+    compare(fa2, oracle_mod, workloads.custom(2, 2, N, D, dtype, causal, seed=N * 13 + D), schedule=schedule)
+
+
+@pytest.mark.parametrize("D", [32, 96])
+@pytest.mark.parametrize("causal", [False, True])
+def test_padded_head_dims_long_rows(fa2, oracle_mod, D, causal):
+    """Many query steps per K/V tile and several tiles per CTA, auto schedule."""
+    compare(fa2, oracle_mod, workloads.custom(1, 3, 2500, D, "bf16", causal, seed=D + 90))
+
+
 @pytest.mark.parametrize("causal", [False, True])
 @pytest.mark.parametrize("schedule", SCHEDULES)
 def test_many_units_per_cta(fa2, oracle_mod, causal, schedule):
