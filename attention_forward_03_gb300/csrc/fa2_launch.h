@@ -11,7 +11,6 @@ namespace fa2 {
 
 constexpr int kRows = 128;          // query rows per sub-tile (= TMEM lanes)
 constexpr int kSubTiles = 2;        // sub-tiles per work unit
-constexpr int kUnitRows = kRows * kSubTiles;
 constexpr int kKeys = 128;          // keys per K/V tile
 
 // Head dimensions of the forward kernels. 64 and 128 are native; 32 and 96

@@ -63,11 +63,13 @@ struct CUstream_st; /* the same type as cudaStream_t / CUstream */
  * B, H, N : batch, heads, sequence length (queries and keys), each >= 0. If
  *           any is 0 the call does nothing and returns FA2_OK (pointers may
  *           then be NULL).
- * D       : head dimension; 32, 64, 96 or 128. 64 and 128 are the native
- *           tile widths; 32 and 96 run in the tiles of 64 and 128, whose
- *           columns past D the kernel reads as zeros. These are the head
- *           dims the split-Q launcher of "FlashAttention-2 MMA 代码学习"
- *           dispatches (its host function at the end of the page).
+ * D       : head dimension; 32, 64, 96, 128 or 256. 64 and 128 are the
+ *           native tile widths; 32 and 96 run in the tiles of 64 and 128,
+ *           whose columns past D the kernel reads as zeros. These four are
+ *           the head dims the split-Q launcher of "FlashAttention-2 MMA
+ *           代码学习" dispatches (its host function at the end of the page);
+ *           256, the first of the tiling_qk page's larger ones, runs on a
+ *           kernel of its own with 128-row work units.
  * scale   : multiplier on Q.K; finite and > 0 (the usual value is 1/sqrt(D)).
  * is_causal: nonzero keeps only keys j <= i for query i.
  * dtype   : FA2_F16 or FA2_BF16.
@@ -87,8 +89,9 @@ int fa2_fwd(const void* Q, const void* K, const void* V, void* O, float* LSE,
 
 /*
  * fa2_fwd_workspace_bytes — bytes of device workspace fa2_fwd_ws needs on the
- * current device for head dimension D (32, 64, 96 or 128): one fp32 partial result of
- * a 256-row work unit per SM plus one 8-byte flag per 128-row half. It does
+ * current device for head dimension D (32, 64, 96, 128 or 256): one fp32
+ * partial result of a work unit per SM (256 rows, or 128 at head dim 256)
+ * plus one 8-byte flag per 128-row sub-tile. It does
  * not depend on B, H or N. Returns FA2_OK, FA2_ERR_INVALID_ARG (bytes NULL),
  * FA2_ERR_UNSUPPORTED (D) or FA2_ERR_CUDA.
  */
