@@ -24,14 +24,16 @@ constexpr int kElemBlocksPerSm = 8;
 
 size_t round256(size_t x) { return (x + 255) / 256 * 256; }
 
-// Workspace: dQ accumulator | LSE*log2(e) | Delta | stream-K partial dV, dK
+// Workspace: dQ accumulator | LSE*log2(e) | Delta (rows padded to a multiple
+// of the step rows) | stream-K partial dV, dK
 // (one [2][D][128] fp32 slot per CTA, kBwdMaxCtas slots) | their flags.
 struct BwdWorkspace {
   size_t dq_bytes, stat_bytes, part_bytes, flag_bytes, total;
 };
 
 BwdWorkspace workspace_layout(int64_t bh, int N, int D) {
-  const int64_t npad = (static_cast<int64_t>(N) + kBwdRows - 1) / kBwdRows * kBwdRows;
+  const int64_t sr = bwd_step_rows(D);
+  const int64_t npad = (static_cast<int64_t>(N) + sr - 1) / sr * sr;
   BwdWorkspace w;
   w.dq_bytes = round256(static_cast<size_t>(bh) * N * D * sizeof(float));
   w.stat_bytes = round256(static_cast<size_t>(bh) * npad * sizeof(float));
@@ -44,7 +46,7 @@ BwdWorkspace workspace_layout(int64_t bh, int N, int D) {
 // Cost of the busiest CTA in query steps under the round schedule (units
 // dealt in rounds, zig-zag when causal: the kernel's bwd_round_unit and
 // bwd_unit), or -1 when there are too many units to count here.
-long long round_schedule_cost(long long units, int bh, int nkv, int nq, bool causal, int grid) {
+long long round_schedule_cost(long long units, int bh, int nkv, int nq, int steps_per_tile, bool causal, int grid) {
   if (!causal) return (units + grid - 1) / grid * nq;
   if (units > (1ll << 22)) return -1;
   long long worst = 0;
@@ -54,7 +56,7 @@ long long round_schedule_cost(long long units, int bh, int nkv, int nq, bool cau
       const long long u = r * grid + ((r & 1) ? (grid - 1 - b) : b);
       if (u >= units) break;
       const long long kv = u / bh;  // causal: K/V tile major over all heads
-      sum += nq - 2 * kv;
+      sum += nq - steps_per_tile * kv;
     }
     worst = sum > worst ? sum : worst;
   }
@@ -245,11 +247,12 @@ extern "C" int fa2_bwd_sched(const void* Q, const void* K, const void* V, const 
   CUtensorMap mk, mv, mq, mdo;
   if (!encode_tile_map(&mk, K, (int)bh, N, D, dtype, kBwdKeys) ||
       !encode_tile_map(&mv, V, (int)bh, N, D, dtype, kBwdKeys) ||
-      !encode_tile_map(&mq, Q, (int)bh, N, D, dtype, kBwdRows) ||
-      !encode_tile_map(&mdo, dO, (int)bh, N, D, dtype, kBwdRows))
+      !encode_tile_map(&mq, Q, (int)bh, N, D, dtype, static_cast<unsigned>(bwd_step_rows(D))) ||
+      !encode_tile_map(&mdo, dO, (int)bh, N, D, dtype, static_cast<unsigned>(bwd_step_rows(D))))
     return record_cuda_error(cudaErrorInvalidValue);
 
-  const int npad = (N + kBwdRows - 1) / kBwdRows * kBwdRows;
+  const int sr = bwd_step_rows(D);
+  const int npad = (N + sr - 1) / sr * sr;
   char* ws = static_cast<char*>(workspace);
   float* dq_acc = reinterpret_cast<float*>(ws);
   CUtensorMap mdq;  // the kernel adds blocks of 32 rows of dQ into the accumulator
@@ -282,14 +285,15 @@ extern "C" int fa2_bwd_sched(const void* Q, const void* K, const void* V, const 
   p.Npad = npad;
   p.BH = (int)bh;
   p.nkv = (int)nkv;
-  p.nq = npad / kBwdRows;
+  p.nq = npad / sr;
   p.num_units = (int)(bh * nkv);
   p.scale_log2 = scale * 1.4426950408889634f;
   p.scale = scale;
   // Query steps of one head: non-causal nkv * nq; causal, K/V tile kv sees
-  // the steps from 2*kv on.
+  // the steps from kv * (128 / step rows) on.
+  const int steps_per_tile = kBwdKeys / sr;
   long long per_head = 0;
-  for (int64_t kv = 0; kv < nkv; ++kv) per_head += is_causal ? p.nq - 2 * kv : p.nq;
+  for (int64_t kv = 0; kv < nkv; ++kv) per_head += is_causal ? p.nq - steps_per_tile * kv : p.nq;
   p.steps_per_head = per_head;
   p.total_steps = per_head * bh;
   const int round_grid = p.num_units < sms ? p.num_units : sms;
@@ -298,7 +302,8 @@ extern "C" int fa2_bwd_sched(const void* Q, const void* K, const void* V, const 
   if (schedule == FA2_SCHED_AUTO) {
     // the schedule whose busiest CTA has fewer steps, balanced only when it
     // saves at least 5 %
-    const long long rounds = round_schedule_cost(p.num_units, p.BH, p.nkv, p.nq, is_causal != 0, round_grid);
+    const long long rounds =
+        round_schedule_cost(p.num_units, p.BH, p.nkv, p.nq, steps_per_tile, is_causal != 0, round_grid);
     const long long split = (p.total_steps + sk_grid - 1) / sk_grid + kBwdSplitCostSteps;
     balanced = rounds > 0 && 100 * split < 95 * rounds;
   }

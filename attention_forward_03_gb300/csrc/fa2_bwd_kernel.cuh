@@ -68,9 +68,6 @@ constexpr int kBwdMmaWarp = 8;      // MMA issuer (all products, or S^T / dP^T);
 constexpr int kBwdGradWarp = 9;     // second MMA issuer (dV, dK, dQ^T) of non-causal launches
 constexpr int kBwdLoadWarp = 10;
 constexpr int kBwdComputeThreads = 256;
-constexpr int kBwdQPanelBytes = kBwdRows * 128;   // 64 rows x 64 16-bit elements
-constexpr int kBwdPTileBytes = kBwdKeys * 128;    // 128 keys x 64 query columns (16-bit)
-constexpr int kBwdStatBytes = 2 * kBwdRows * 4;   // LSE*log2(e) and Delta of one step
 
 enum : int {
   kSiteBwdKvEmpty = 21,
@@ -103,9 +100,20 @@ struct BwdLayout {
   // 64: a 32-wide MN-major operand would cover half of a 128-byte swizzle
   // row, a form the operand layouts do not describe.
   static constexpr int kNacc = (D == 32) ? 64 : D;
+  // Query rows per step (SR): 128 where the tensor memory has room for
+  // 128-column S^T, dP^T and dQ^T next to dV and dK (Dp = 64: 64 + 64 + 3 x
+  // 128 = 512 columns), else 64. Each compute warpgroup takes SR/2 query
+  // columns of a step, in halves of 32.
+  static constexpr int kSR = bwd_step_rows(D);
+  static constexpr int kR = kBwdKeys / kSR;                   // steps per 128 query rows
+  static constexpr int kCW = kSR / 2;                         // query columns per warpgroup
+  static constexpr int kHalves = kCW / 32;
   static constexpr int kKVBytes = kPanels * kPanelBytes;      // K or V tile: 128 rows x Dp
-  static constexpr int kQBytes = kPanels * kBwdQPanelBytes;   // Q or dO step: 64 rows x Dp
-  static constexpr int kStages = (kPanels == 2) ? 3 : 6;
+  static constexpr int kQPanelBytes = kSR * 128;              // SR rows x 64 16-bit elements
+  static constexpr int kQBytes = kPanels * kQPanelBytes;      // Q or dO step: SR rows x Dp
+  static constexpr int kPTileBytes = (kSR / 64) * kPanelBytes;  // P^T or dS^T: 128 keys x SR queries
+  static constexpr int kStatBytes = 2 * kSR * 4;              // LSE*log2(e) and Delta of one step
+  static constexpr int kStages = (kSR == 128) ? 2 : (kPanels == 2 ? 3 : 6);
   // Epilogue: a key row's D columns in chunks of 32, the first kChunksWg for
   // compute warpgroup 0 and the rest for warpgroup 1.
   static constexpr int kChunks = D / 32;
@@ -116,10 +124,10 @@ struct BwdLayout {
   static constexpr int kV = kKVBytes;
   static constexpr int kRing = 2 * kKVBytes;
   static constexpr int kP = kRing + kStages * kStageBytes;
-  static constexpr int kDS = kP + kBwdPTileBytes;
-  static constexpr int kDQS = kDS + kBwdPTileBytes;           // dQ staging: 64 rows x D fp32
-  static constexpr int kStats = kDQS + kBwdRows * D * 4;
-  static constexpr int kBars = kStats + kStages * kBwdStatBytes;
+  static constexpr int kDS = kP + kPTileBytes;
+  static constexpr int kDQS = kDS + kPTileBytes;              // dQ staging: SR rows x D fp32
+  static constexpr int kStats = kDQS + kSR * D * 4;
+  static constexpr int kBars = kStats + kStages * kStatBytes;
   // kv_full, kv_empty, stage_full[S], stage_empty[S], s_full, s_free, p_full,
   // p_free, dq_full, dq_free, acc_full, acc_free, drain, dqs_ready[2], dqs_free[2], drain2, part_done
   static constexpr int kNumBars = 2 + 2 * kStages + 15;
@@ -128,9 +136,9 @@ struct BwdLayout {
   static constexpr uint32_t kColDV = 0;
   static constexpr uint32_t kColDK = kDp;
   static constexpr uint32_t kColS = 2 * kDp;
-  static constexpr uint32_t kColDP = 2 * kDp + kBwdRows;
-  static constexpr uint32_t kColDQ = 2 * kDp + 2 * kBwdRows;
-  static_assert(kColDQ + kBwdRows <= kTmemCols, "TMEM budget");
+  static constexpr uint32_t kColDP = 2 * kDp + kSR;
+  static constexpr uint32_t kColDQ = 2 * kDp + 2 * kSR;
+  static_assert(kColDQ + kSR <= kTmemCols, "TMEM budget");
   static_assert(kSmemBytes <= 232448, "shared memory budget");
   static_assert(kRing % 1024 == 0 && kP % 1024 == 0 && kDS % 1024 == 0, "swizzled tiles need 1 KB alignment");
 };
@@ -149,10 +157,10 @@ __device__ __forceinline__ void bwd_unit(int u, const BwdParams& p, int& bh, int
   }
 }
 
-// Query steps [first, nq) that see keys of tile kv.
-template <bool kCausal>
+// Query steps [first, nq) that see keys of tile kv (kR steps per 128 rows).
+template <bool kCausal, int kR>
 __device__ __forceinline__ int bwd_first_step(int kv) {
-  return kCausal ? kv * (kBwdKeys / kBwdRows) : 0;
+  return kCausal ? kv * kR : 0;
 }
 
 // Unit of this CTA in round r (zig-zag when causal, as in the forward).
@@ -189,19 +197,20 @@ __device__ __forceinline__ BwdCursor bwd_first_cursor(const BwdParams& p) {
 }
 
 // First step of causal unit kv within its head: units k < kv have
-// nq - 2k steps each, kv*nq - kv*(kv-1) in all.
+// nq - kR*k steps each, kv*nq - kR*kv*(kv-1)/2 in all.
+template <int kR>
 __device__ __forceinline__ long long bwd_causal_start(int kv, int nq) {
-  return static_cast<long long>(kv) * nq - static_cast<long long>(kv) * (kv - 1);
+  return static_cast<long long>(kv) * nq - static_cast<long long>(kR) * kv * (kv - 1) / 2;
 }
 
 // Next segment of this CTA. Every role walks the same sequence.
-template <bool kCausal>
+template <bool kCausal, int kR>
 __device__ __forceinline__ bool bwd_next_segment(BwdCursor& c, BwdSegment& s, const BwdParams& p) {
   if (!p.stream_k) {
     const int u = bwd_round_unit<kCausal>(c.round++);
     if (u >= p.num_units) return false;
     bwd_unit<kCausal>(u, p, s.bh, s.kv);
-    s.i_begin = bwd_first_step<kCausal>(s.kv);
+    s.i_begin = bwd_first_step<kCausal, kR>(s.kv);
     s.i_end = p.nq;
     s.unit_end = 0;
     return true;
@@ -213,17 +222,18 @@ __device__ __forceinline__ bool bwd_next_segment(BwdCursor& c, BwdSegment& s, co
   int kv;
   long long start;
   if (kCausal) {
-    const float a = static_cast<float>(p.nq) + 1.f;
-    kv = static_cast<int>((a - sqrtf(fmaxf(a * a - 4.f * static_cast<float>(r), 0.f))) * 0.5f);
+    // the root of (kR/2) kv^2 - (nq + kR/2) kv + r = 0, then corrected
+    const float a = static_cast<float>(p.nq) + 0.5f * kR;
+    kv = static_cast<int>((a - sqrtf(fmaxf(a * a - 2.f * kR * static_cast<float>(r), 0.f))) / kR);
     kv = min(max(kv, 0), p.nkv - 1);
-    while (kv > 0 && bwd_causal_start(kv, p.nq) > r) --kv;
-    while (kv + 1 < p.nkv && bwd_causal_start(kv + 1, p.nq) <= r) ++kv;
-    start = bwd_causal_start(kv, p.nq);
+    while (kv > 0 && bwd_causal_start<kR>(kv, p.nq) > r) --kv;
+    while (kv + 1 < p.nkv && bwd_causal_start<kR>(kv + 1, p.nq) <= r) ++kv;
+    start = bwd_causal_start<kR>(kv, p.nq);
   } else {
     kv = static_cast<int>(r / p.nq);
     start = static_cast<long long>(kv) * p.nq;
   }
-  const int first = bwd_first_step<kCausal>(kv);
+  const int first = bwd_first_step<kCausal, kR>(kv);
   s.bh = static_cast<int>(bh);
   s.kv = kv;
   s.i_begin = first + static_cast<int>(r - start);
@@ -336,7 +346,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       bool ok = true;
       BwdCursor cur = bwd_first_cursor(p);
       BwdSegment sg;
-      while (ok && bwd_next_segment<kCausal>(cur, sg, p)) {
+      while (ok && bwd_next_segment<kCausal, L::kR>(cur, sg, p)) {
         const int bh = sg.bh, kv = sg.kv;
         if (units > 0 && !wait_bounded(bar_kv_empty, (units - 1) & 1u, wd, kSiteBwdKvEmpty, true, kNapNs)) {
           ok = false;
@@ -355,15 +365,15 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           }
           const uint32_t full = bar_stage_full(slot);
           const uint32_t st = sRing + static_cast<uint32_t>(slot * L::kStageBytes);
-          mbar_arrive_expect_tx(full, L::kStageBytes + kBwdStatBytes);
+          mbar_arrive_expect_tx(full, L::kStageBytes + L::kStatBytes);
           for (int pn = 0; pn < L::kPanels; ++pn) {
-            tma_load_3d_hint(st + pn * kBwdQPanelBytes, &tmQ, full, pn * 64, i * kBwdRows, bh, keep);
-            tma_load_3d_hint(st + L::kQBytes + pn * kBwdQPanelBytes, &tmDO, full, pn * 64, i * kBwdRows, bh, keep);
+            tma_load_3d_hint(st + pn * L::kQPanelBytes, &tmQ, full, pn * 64, i * L::kSR, bh, keep);
+            tma_load_3d_hint(st + L::kQBytes + pn * L::kQPanelBytes, &tmDO, full, pn * 64, i * L::kSR, bh, keep);
           }
-          const size_t off = static_cast<size_t>(bh) * p.Npad + static_cast<size_t>(i) * kBwdRows;
-          const uint32_t sst = sStats + static_cast<uint32_t>(slot * kBwdStatBytes);
-          bulk_load(sst, p.lse2 + off, kBwdRows * 4, full);
-          bulk_load(sst + kBwdRows * 4, p.delta + off, kBwdRows * 4, full);
+          const size_t off = static_cast<size_t>(bh) * p.Npad + static_cast<size_t>(i) * L::kSR;
+          const uint32_t sst = sStats + static_cast<uint32_t>(slot * L::kStatBytes);
+          bulk_load(sst, p.lse2 + off, L::kSR * 4, full);
+          bulk_load(sst + L::kSR * 4, p.delta + off, L::kSR * 4, full);
           ++loads;
           if (++slot == L::kStages) {
             slot = 0;
@@ -382,12 +392,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   } else if (warp == kBwdMmaWarp || (kTwoIssuers && warp == kBwdGradWarp)) {
     // --------------------------------------------------------- MMA issuers
     if (lane == 0) {
-      constexpr uint32_t idesc_s = make_idesc_f16(kBf16, kBwdRows, false);            // S^T, dP^T: N = 64
+      constexpr uint32_t idesc_s = make_idesc_f16(kBf16, L::kSR, false);              // S^T, dP^T: N = SR
       constexpr uint32_t idesc_acc = make_idesc_f16(kBf16, L::kNacc, true);           // dV, dK: N = D (64 at D = 32)
-      constexpr uint32_t idesc_dq = make_idesc_f16_ab(kBf16, kBwdRows, true, true);   // dQ^T: N = 64
+      constexpr uint32_t idesc_dq = make_idesc_f16_ab(kBf16, L::kSR, true, true);     // dQ^T: N = SR
       constexpr uint32_t kHi = desc_hi_sw128(1024);  // 8-row (K-major) / 8-row-of-K (MN-major) groups 1 KB apart
       // S^T = K Q_i^T and dP^T = V dO_i^T: A = K / V (K-major, 128-row
-      // panels), B = Q_i / dO_i (K-major, 64-row panels), D/16 steps.
+      // panels), B = Q_i / dO_i (K-major, SR-row panels), N = SR, D/16 steps.
       auto issue_sdp = [&](int slot) {
         const uint32_t st = sRing + static_cast<uint32_t>(slot * L::kStageBytes);
         const uint32_t k_lo = desc_lo_sw128(sK, 16), v_lo = desc_lo_sw128(sV, 16);
@@ -395,44 +405,45 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t a = static_cast<uint32_t>(((kk >> 2) * kPanelBytes + (kk & 3) * 32) >> 4);
-          const uint32_t b = static_cast<uint32_t>(((kk >> 2) * kBwdQPanelBytes + (kk & 3) * 32) >> 4);
+          const uint32_t b = static_cast<uint32_t>(((kk >> 2) * L::kQPanelBytes + (kk & 3) * 32) >> 4);
           mma_ss_w(tmem + L::kColS, k_lo + a, kHi, q_lo + b, kHi, idesc_s, kk > 0 ? 1u : 0u);
         }
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t a = static_cast<uint32_t>(((kk >> 2) * kPanelBytes + (kk & 3) * 32) >> 4);
-          const uint32_t b = static_cast<uint32_t>(((kk >> 2) * kBwdQPanelBytes + (kk & 3) * 32) >> 4);
+          const uint32_t b = static_cast<uint32_t>(((kk >> 2) * L::kQPanelBytes + (kk & 3) * 32) >> 4);
           mma_ss_w(tmem + L::kColDP, v_lo + a, kHi, do_lo + b, kHi, idesc_s, kk > 0 ? 1u : 0u);
         }
       };
-      // dV += P^T dO_i and dK += dS^T Q_i: A = P^T / dS^T (K-major, one
-      // panel of 64 query columns), B = dO_i / Q_i (MN-major: rows are the
-      // contraction index, 64-column panels 8 KB apart), 4 steps of 16 rows.
+      // dV += P^T dO_i and dK += dS^T Q_i: A = P^T / dS^T (K-major, panels
+      // of 64 query columns 16 KB apart), B = dO_i / Q_i (MN-major: rows are
+      // the contraction index, 64-column panels of SR rows), SR/16 steps of
+      // 16 rows.
       auto issue_grads = [&](int slot, bool acc) {
         const uint32_t st = sRing + static_cast<uint32_t>(slot * L::kStageBytes);
         const uint32_t p_lo = desc_lo_sw128(sP, 16), ds_lo = desc_lo_sw128(sDS, 16);
-        const uint32_t q_mn = desc_lo_sw128(st, kBwdQPanelBytes);
-        const uint32_t do_mn = desc_lo_sw128(st + L::kQBytes, kBwdQPanelBytes);
+        const uint32_t q_mn = desc_lo_sw128(st, L::kQPanelBytes);
+        const uint32_t do_mn = desc_lo_sw128(st + L::kQBytes, L::kQPanelBytes);
 #pragma unroll
-        for (int kk = 0; kk < kBwdRows / 16; ++kk) {
-          const uint32_t a = static_cast<uint32_t>((kk * 32) >> 4);
+        for (int kk = 0; kk < L::kSR / 16; ++kk) {
+          const uint32_t a = static_cast<uint32_t>(((kk >> 2) * kPanelBytes + (kk & 3) * 32) >> 4);
           const uint32_t b = static_cast<uint32_t>((kk * 16 * 128) >> 4);
           mma_ss_w(tmem + L::kColDV, p_lo + a, kHi, do_mn + b, kHi, idesc_acc, (acc || kk > 0) ? 1u : 0u);
         }
 #pragma unroll
-        for (int kk = 0; kk < kBwdRows / 16; ++kk) {
-          const uint32_t a = static_cast<uint32_t>((kk * 32) >> 4);
+        for (int kk = 0; kk < L::kSR / 16; ++kk) {
+          const uint32_t a = static_cast<uint32_t>(((kk >> 2) * kPanelBytes + (kk & 3) * 32) >> 4);
           const uint32_t b = static_cast<uint32_t>((kk * 16 * 128) >> 4);
           mma_ss_w(tmem + L::kColDK, ds_lo + a, kHi, q_mn + b, kHi, idesc_acc, (acc || kk > 0) ? 1u : 0u);
         }
       };
       // dQ_i^T = K^T dS^T: A = K read MN-major (M = head-dim index, two
       // 64-row M panels 16 KB apart; at D = 64 the second panel is the V
-      // tile and its rows are discarded), B = dS^T MN-major (N = 64 query
-      // columns, one panel), 8 steps of 16 keys.
+      // tile and its rows are discarded), B = dS^T MN-major (N = SR query
+      // columns, panels of 64 16 KB apart), 8 steps of 16 keys.
       auto issue_dq = [&]() {
         const uint32_t kt_lo = desc_lo_sw128(sK, kPanelBytes);
-        const uint32_t ds_mn = desc_lo_sw128(sDS, kBwdPTileBytes);
+        const uint32_t ds_mn = desc_lo_sw128(sDS, kPanelBytes);
 #pragma unroll
         for (int kk = 0; kk < kBwdKeys / 16; ++kk) {
           const uint32_t off = static_cast<uint32_t>((kk * 16 * 128) >> 4);
@@ -452,7 +463,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         bool ok = true;
         BwdCursor cur = bwd_first_cursor(p);
         BwdSegment sg;
-        while (ok && bwd_next_segment<kCausal>(cur, sg, p)) {
+        while (ok && bwd_next_segment<kCausal, L::kR>(cur, sg, p)) {
           const int n_steps = sg.i_end - sg.i_begin;
           if (!wait_bounded(bar_kv_full, units & 1u, wd, kSiteBwdKvFull, true, kNapNs)) {
             ok = false;
@@ -527,7 +538,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         };
         BwdCursor wcur = bwd_first_cursor(p);
         BwdSegment sg;
-        while (ok && bwd_next_segment<kCausal>(wcur, sg, p)) {
+        while (ok && bwd_next_segment<kCausal, L::kR>(wcur, sg, p)) {
           const int n_steps = sg.i_end - sg.i_begin;
           if (!wait_bounded(bar_kv_full, units & 1u, wd, kSiteBwdKvFull, true, kNapNs)) {
             ok = false;
@@ -590,9 +601,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const int quarter = warp & 3;             // TMEM lane quarter this warp may access
     const int rr = quarter * 32 + lane;       // key row within the tile = TMEM lane
     const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
-    const uint32_t tS = tmem + lane_off + L::kColS + 32u * wg;
-    const uint32_t tDP = tmem + lane_off + L::kColDP + 32u * wg;
-    const uint32_t tDQ = tmem + lane_off + L::kColDQ + 32u * wg;
+    // this warpgroup's query columns of a step: [kCW*wg, kCW*wg + kCW), in halves of 32
+    const uint32_t tS = tmem + lane_off + L::kColS + static_cast<uint32_t>(L::kCW * wg);
+    const uint32_t tDP = tmem + lane_off + L::kColDP + static_cast<uint32_t>(L::kCW * wg);
+    const uint32_t tDQ = tmem + lane_off + L::kColDQ + static_cast<uint32_t>(L::kCW * wg);
     const uint32_t p_row = sP + static_cast<uint32_t>(rr * 128);
     const uint32_t ds_row = sDS + static_cast<uint32_t>(rr * 128);
     const uint32_t xr = static_cast<uint32_t>(rr & 7);
@@ -603,27 +615,30 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     bool ok = true;
     int pend_bh = 0, pend_q0 = 0;  // head and first row of the step whose dQ^T is pending
 
-    // dQ^T of global step `step` (head pend_bh, rows pend_q0 + [32wg, 32wg+32))
-    // from TMEM into the fp32 accumulator: this thread holds head-dim index
-    // rr of 32 query rows. The warpgroup writes them into its 32 x D staging
-    // rows (row-major, the accumulator's layout) and its leader thread adds
-    // the block into global memory with one TMA reduce-add; the staging rows
-    // are rewritten once that TMA has read them.
+    // dQ^T of global step `step` (head pend_bh, rows pend_q0 + kCW*wg +
+    // [0, kCW)) from TMEM into the fp32 accumulator: this thread holds
+    // head-dim index rr of those query rows. The warpgroup writes them into
+    // its kCW x D staging rows (row-major, the accumulator's layout) and its
+    // leader thread adds each block of 32 rows into global memory with one
+    // TMA reduce-add; the staging rows are rewritten once those TMAs have
+    // read them.
     const bool leader = (threadIdx.x & 127) == 0;
-    const uint32_t stage_rows = sDQS + static_cast<uint32_t>(wg * 32 * D * 4);
+    const uint32_t stage_rows = sDQS + static_cast<uint32_t>(wg * L::kCW * D * 4);
     uint32_t drains = 0;
     auto drain_dq = [&](uint32_t step) -> bool {
       bool got = wait_bounded(bar_dq_full, step & 1u, wd, kSiteBwdDqFull);
       got = __all_sync(0xffffffffu, got);
       if (!got) return false;
       tc_fence_after_sync();
-      uint32_t v[32];
+      uint32_t v[L::kHalves][32];
       // every warp loads (lanes from D on hold the discarded rows; a load
       // guarded by dq_rows made the compiler spill at D = 32 and 96), only
       // the warps with real head-dim rows store below
-      tmem_ld32x32_wait(tDQ, v);
+#pragma unroll
+      for (int h = 0; h < L::kHalves; ++h) tmem_ld32x32_wait(tDQ + 32u * h, v[h]);
       tc_fence_before_sync();
       mbar_arrive(bar_dq_free);
+      // the staging rows must have been read by the previous step's TMAs
       if (drains > 0) {
         if (leader) {
           bulk_wait_read_all();
@@ -635,10 +650,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       }
       if (dq_rows) {
 #pragma unroll
-        for (int i = 0; i < 32; ++i)
-          asm volatile("st.shared.f32 [%0], %1;" ::"r"(stage_rows + static_cast<uint32_t>((i * D + rr) * 4)),
-                       "f"(__uint_as_float(v[i]))
-                       : "memory");
+        for (int h = 0; h < L::kHalves; ++h) {
+#pragma unroll
+          for (int i = 0; i < 32; ++i)
+            asm volatile("st.shared.f32 [%0], %1;" ::"r"(stage_rows + static_cast<uint32_t>(((32 * h + i) * D + rr) * 4)),
+                         "f"(__uint_as_float(v[h][i]))
+                         : "memory");
+        }
       }
       fence_proxy_async_shared();
       mbar_arrive(bar_dqs_ready(wg));
@@ -648,11 +666,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         if (!rd) return false;
       }
       if (leader) {
-        const int q0 = pend_q0 + 32 * wg;
-        if (q0 < p.N) {  // rows past N are outside the map and skipped
-          tma_reduce_add_3d(&tmDQ, stage_rows, 0, q0, pend_bh);
-          bulk_commit_group();
+#pragma unroll
+        for (int h = 0; h < L::kHalves; ++h) {
+          const int q0 = pend_q0 + L::kCW * wg + 32 * h;
+          if (q0 < p.N)  // rows past N are outside the map and skipped
+            tma_reduce_add_3d(&tmDQ, stage_rows + static_cast<uint32_t>(32 * h * D * 4), 0, q0, pend_bh);
         }
+        bulk_commit_group();
       }
       ++drains;
       return true;
@@ -660,7 +680,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 
     BwdCursor cur = bwd_first_cursor(p);
     BwdSegment sg;
-    while (ok && bwd_next_segment<kCausal>(cur, sg, p)) {
+    while (ok && bwd_next_segment<kCausal, L::kR>(cur, sg, p)) {
       const int bh = sg.bh, kv = sg.kv;
       const int key = kv * kBwdKeys + rr;
       const bool key_ok = key < p.N;
@@ -673,46 +693,58 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           break;
         }
         tc_fence_after_sync();
-        uint32_t sr[32], dpr[32];
-        tmem_ld32x32_wait(tS, sr);
-        tmem_ld32x32_wait(tDP, dpr);
-        // S^T and dP^T are in registers: the issuer may compute the next ones.
-        tc_fence_before_sync();
-        mbar_arrive(bar_s_free);
-        const float* lse2 = stats + slot * (kBwdStatBytes / 4) + 32 * wg;
-        const float* delta = lse2 + kBwdRows;
-        const int q0 = i * kBwdRows + 32 * wg;  // query row of this thread's first column
-        // masked: keys past N (ragged last tile) and, causal, keys after the query
-        const bool masked = !key_ok || (kCausal && key > q0);
-        uint32_t pk[16], dk[16];
+        const float* lse2_step = stats + slot * (L::kStatBytes / 4) + L::kCW * wg;
+        const float* delta_step = lse2_step + L::kSR;
+        bool fr = true;
 #pragma unroll
-        for (int j = 0; j < 32; j += 2) {
-          float p0 = ex2_approx(__uint_as_float(sr[j]) * c - lse2[j]);
-          float p1 = ex2_approx(__uint_as_float(sr[j + 1]) * c - lse2[j + 1]);
-          if (masked) {
-            if (!key_ok || key > q0 + j) p0 = 0.f;
-            if (!key_ok || key > q0 + j + 1) p1 = 0.f;
+        for (int h = 0; h < L::kHalves; ++h) {
+          uint32_t sr[32], dpr[32];
+          tmem_ld32x32_wait(tS + 32u * h, sr);
+          tmem_ld32x32_wait(tDP + 32u * h, dpr);
+          if (h == L::kHalves - 1) {
+            // S^T and dP^T are in registers: the issuer may compute the next ones.
+            tc_fence_before_sync();
+            mbar_arrive(bar_s_free);
           }
-          const float d0 = p0 * (__uint_as_float(dpr[j]) - delta[j]);
-          const float d1 = p1 * (__uint_as_float(dpr[j + 1]) - delta[j + 1]);
-          pk[j / 2] = pack2(p0, p1, kBf16);
-          dk[j / 2] = pack2(d0, d1, kBf16);
-        }
-        // the previous step's P^T / dS^T must have been read by the tensor core
-        if (g > 0) {
-          bool fr = wait_bounded(bar_p_free, (g - 1) & 1u, wd, kSiteBwdPFree);
-          fr = __all_sync(0xffffffffu, fr);
-          if (!fr) {
-            ok = false;
-            break;
-          }
-        }
-        // 4 chunks of 8 query columns into the 128-byte-swizzled key row
+          const float* lse2 = lse2_step + 32 * h;
+          const float* delta = delta_step + 32 * h;
+          const int q0 = i * L::kSR + L::kCW * wg + 32 * h;  // query row of this thread's first column
+          // masked: keys past N (ragged last tile) and, causal, keys after the query
+          const bool masked = !key_ok || (kCausal && key > q0);
+          uint32_t pk[16], dk[16];
 #pragma unroll
-        for (int ch = 0; ch < 4; ++ch) {
-          const uint32_t col = ((static_cast<uint32_t>(4 * wg + ch) ^ xr) << 4);
-          st_shared_v4(p_row + col, pk[4 * ch], pk[4 * ch + 1], pk[4 * ch + 2], pk[4 * ch + 3]);
-          st_shared_v4(ds_row + col, dk[4 * ch], dk[4 * ch + 1], dk[4 * ch + 2], dk[4 * ch + 3]);
+          for (int j = 0; j < 32; j += 2) {
+            float p0 = ex2_approx(__uint_as_float(sr[j]) * c - lse2[j]);
+            float p1 = ex2_approx(__uint_as_float(sr[j + 1]) * c - lse2[j + 1]);
+            if (masked) {
+              if (!key_ok || key > q0 + j) p0 = 0.f;
+              if (!key_ok || key > q0 + j + 1) p1 = 0.f;
+            }
+            const float d0 = p0 * (__uint_as_float(dpr[j]) - delta[j]);
+            const float d1 = p1 * (__uint_as_float(dpr[j + 1]) - delta[j + 1]);
+            pk[j / 2] = pack2(p0, p1, kBf16);
+            dk[j / 2] = pack2(d0, d1, kBf16);
+          }
+          // the previous step's P^T / dS^T must have been read by the tensor core
+          if (h == 0 && g > 0) {
+            fr = wait_bounded(bar_p_free, (g - 1) & 1u, wd, kSiteBwdPFree);
+            fr = __all_sync(0xffffffffu, fr);
+            if (!fr) break;
+          }
+          // 4 chunks of 8 query columns into the 128-byte-swizzled key row of
+          // the 64-column panel that holds them
+          const int qc = L::kCW * wg + 32 * h;  // first query column of this half in the step
+          const uint32_t panel = static_cast<uint32_t>((qc >> 6) * kPanelBytes);
+#pragma unroll
+          for (int ch = 0; ch < 4; ++ch) {
+            const uint32_t col = panel + ((static_cast<uint32_t>(((qc & 63) >> 3) + ch) ^ xr) << 4);
+            st_shared_v4(p_row + col, pk[4 * ch], pk[4 * ch + 1], pk[4 * ch + 2], pk[4 * ch + 3]);
+            st_shared_v4(ds_row + col, dk[4 * ch], dk[4 * ch + 1], dk[4 * ch + 2], dk[4 * ch + 3]);
+          }
+        }
+        if (!fr) {
+          ok = false;
+          break;
         }
         fence_proxy_async_shared();
         tc_fence_before_sync();
@@ -722,7 +754,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           break;
         }
         pend_bh = bh;
-        pend_q0 = i * kBwdRows;
+        pend_q0 = i * L::kSR;
         if (++slot == L::kStages) {
           slot = 0;
           ph ^= 1u;
@@ -757,7 +789,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                               pack2(y[4] * sc, y[5] * sc, kBf16), pack2(y[6] * sc, y[7] * sc, kBf16));
         }
       };
-      if (p.stream_k && sg.i_begin > bwd_first_step<kCausal>(kv)) {
+      if (p.stream_k && sg.i_begin > bwd_first_step<kCausal, L::kR>(kv)) {
         // Not the unit's first steps: hand this CTA's partial dV, dK to the
         // unit's owner through its workspace slot ([2][D][128], column-major
         // so that a warp's stores are contiguous), 32 columns at a time.

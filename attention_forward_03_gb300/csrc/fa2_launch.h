@@ -51,7 +51,9 @@ struct Params {
 constexpr int kBwdKeys = 128;       // keys per backward work unit (= TMEM lanes)
 // Head dimensions of the backward kernel (32 and 96 in the tiles of 64 and 128).
 constexpr bool bwd_head_dim_ok(int d) { return d == 32 || d == 64 || d == 96 || d == 128; }
-constexpr int kBwdRows = 64;        // query rows per backward step
+// Query rows per backward step: 128 at head dims up to 64 (the tensor
+// memory then holds 128-column S^T, dP^T and dQ^T beside dV and dK), else 64.
+constexpr int bwd_step_rows(int d) { return d <= 64 ? 128 : 64; }
 
 struct BwdParams {
   void* dk;                 // [B,H,N,D] 16-bit outputs
@@ -63,10 +65,10 @@ struct BwdParams {
   int* status;              // device watchdog word
   unsigned long long watchdog_ns;
   int N;
-  int Npad;                 // N rounded up to a multiple of kBwdRows
+  int Npad;                 // N rounded up to a multiple of the step rows
   int BH;
   int nkv;                  // K/V tiles (work units) per head = ceil(N / 128)
-  int nq;                   // query steps per head = ceil(N / 64)
+  int nq;                   // query steps per head = Npad / step rows
   int num_units;            // BH * nkv
   float scale_log2;         // scale * log2(e)
   float scale;

@@ -242,17 +242,20 @@ def test_backward_rejects_bad_arguments_before_any_gpu_work(lib, over, code):
 def test_backward_empty_problem_and_workspace_size(lib):
     assert call_bwd(lib, B=0) == lib.FA2_OK
     assert call_bwd(lib, N=0, Q=None, ws=None) == lib.FA2_OK
-    # fp32 dQ accumulator [B,H,N,D] + LSE*log2(e) and Delta rows padded to 64 + the balanced schedule's
-    # 160 partial slots of 2*128*D floats and their 160 flags, each rounded to 256 bytes
+    # fp32 dQ accumulator [B,H,N,D] + LSE*log2(e) and Delta rows padded to the step height (128 rows at
+    # head dims up to 64, else 64) + the balanced schedule's 160 partial slots of 2*128*D floats and their
+    # 160 flags, each rounded to 256 bytes
     r256 = lambda x: -(-x // 256) * 256  # noqa: E731
-    for (B, H, N, D) in ((1, 2, 64, 64), (2, 12, 1000, 64), (1, 8, 8192, 128), (1, 1, 1, 128)):
-        npad = -(-N // 64) * 64
+    for (B, H, N, D) in ((1, 2, 64, 64), (2, 12, 1000, 64), (1, 8, 8192, 128), (1, 1, 1, 128), (1, 3, 200, 96)):
+        sr = 128 if D <= 64 else 64
+        npad = -(-N // sr) * sr
         assert lib.fa2_bwd_workspace_bytes(B, H, N, D) == (r256(B * H * N * D * 4) + 2 * r256(B * H * npad * 4)
                                                            + r256(160 * 2 * 128 * D * 4) + r256(160 * 8))
     n = ctypes.c_size_t(0)
     assert lib.library().fa2_bwd_workspace_bytes(1, 1, 64, 256, ctypes.byref(n)) == lib.FA2_ERR_UNSUPPORTED
     for D in (32, 96):  # the padded head dims
-        assert lib.fa2_bwd_workspace_bytes(1, 1, 64, D) == (r256(64 * D * 4) + 2 * r256(64 * 4)
+        npad = 128 if D <= 64 else 64
+        assert lib.fa2_bwd_workspace_bytes(1, 1, 64, D) == (r256(64 * D * 4) + 2 * r256(npad * 4)
                                                             + r256(160 * 2 * 128 * D * 4) + r256(160 * 8))
     assert lib.library().fa2_bwd_workspace_bytes(1, 1, 64, 64, None) == lib.FA2_ERR_INVALID_ARG
 
