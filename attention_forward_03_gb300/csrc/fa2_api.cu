@@ -243,6 +243,8 @@ int record_cuda_error(cudaError_t e) { return record_cuda(e); }
 
 unsigned long long next_launch_epoch() { return next_epoch(); }
 
+int take_test_withhold() { return g_test_withhold.exchange(0, std::memory_order_relaxed); }
+
 int current_device_facts(int* sms, int** status) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);

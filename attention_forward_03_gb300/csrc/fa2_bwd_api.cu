@@ -307,6 +307,7 @@ extern "C" int fa2_bwd_sched(const void* Q, const void* K, const void* V, const 
     const long long split = (p.total_steps + sk_grid - 1) / sk_grid + kBwdSplitCostSteps;
     balanced = rounds > 0 && 100 * split < 95 * rounds;
   }
+  p.test_withhold = take_test_withhold();
   int grid = round_grid;
   if (balanced) {
     p.stream_k = 1;

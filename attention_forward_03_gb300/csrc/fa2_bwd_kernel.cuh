@@ -352,10 +352,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           ok = false;
           break;
         }
-        mbar_arrive_expect_tx(bar_kv_full, 2 * L::kKVBytes);
-        for (int pn = 0; pn < L::kPanels; ++pn) {
-          tma_load_3d_hint(sK + pn * kPanelBytes, &tmK, bar_kv_full, pn * 64, kv * kBwdKeys, bh, once);
-          tma_load_3d_hint(sV + pn * kPanelBytes, &tmV, bar_kv_full, pn * 64, kv * kBwdKeys, bh, once);
+        if (!(p.test_withhold && units == 0)) {  // test hook: the first K/V tile never arrives
+          mbar_arrive_expect_tx(bar_kv_full, 2 * L::kKVBytes);
+          for (int pn = 0; pn < L::kPanels; ++pn) {
+            tma_load_3d_hint(sK + pn * kPanelBytes, &tmK, bar_kv_full, pn * 64, kv * kBwdKeys, bh, once);
+            tma_load_3d_hint(sV + pn * kPanelBytes, &tmV, bar_kv_full, pn * 64, kv * kBwdKeys, bh, once);
+          }
         }
         ++units;
         for (int i = sg.i_begin; i < sg.i_end; ++i) {

@@ -83,6 +83,7 @@ struct BwdParams {
   float* ws_part;           // [G][2][D][128] fp32 partial dV, dK (unscaled) of a cut unit
   unsigned long long* ws_flags;  // [G] = epoch once that partial is written
   unsigned long long epoch; // unique tag of this launch
+  int test_withhold;        // test hook: the producer withholds its first K/V tile
 };
 
 // CTAs of the backward's stream-K schedule at most (its partial slots are
@@ -109,6 +110,10 @@ int record_cuda_error(cudaError_t e);
 // A tag no earlier launch of this process (or of another one) has used, for
 // the flags of cross-CTA partial results.
 unsigned long long next_launch_epoch();
+
+// The watchdog test hook's request (fa2_test_withhold_next_load), taken by
+// the launch that calls this (one launch only).
+int take_test_withhold();
 
 // Shared with the backward pass: the current device's SM count and watchdog
 // word (FA2_ERR_UNSUPPORTED unless it is a compute-capability 10.3 GPU), a

@@ -296,10 +296,11 @@ int fa2_set_watchdog_ns(unsigned long long ns);
 
 /*
  * fa2_test_withhold_next_load — test hook for the watchdog. When enable is
- * nonzero, the next launch of this library (process-wide, one launch only)
- * withholds its first K/V tile: the waits for that tile run out after the
- * watchdog time, the kernel records the wait site in the watchdog word,
- * winds down without leaving work in flight, and O/LSE are left unspecified.
+ * nonzero, the next launch of this library (process-wide, one launch only:
+ * a forward kernel, or the main kernel of fa2_bwd) withholds its first K/V
+ * tile: the waits for that tile run out after the watchdog time, the kernel
+ * records the wait site in the watchdog word, winds down without leaving
+ * work in flight, and its outputs (O/LSE, or dQ/dK/dV) are left unspecified.
  * No GPU fault, trap or hang is involved. Returns FA2_OK.
  */
 int fa2_test_withhold_next_load(int enable);

@@ -49,3 +49,36 @@ def test_withheld_tile_times_out_and_the_context_stays_usable(fa2, oracle_mod, D
     Oref, Lref = oracle_mod.attention_fwd(q.cpu(), k.cpu(), v.cpu(), w.scale, False)
     assert np.abs(O.float().cpu().numpy() - Oref).max() <= 1e-2
     assert np.abs(L.cpu().numpy() - Lref).max() <= 1e-3
+
+
+@pytest.mark.parametrize("D,schedule", [(128, "units"), (128, "balanced"), (64, "balanced")])
+def test_backward_withheld_tile_times_out_and_the_context_stays_usable(fa2, oracle_mod, D, schedule):
+    # The backward's main kernel takes the hook: its first K/V tile never
+    # arrives, every wait on it runs out, the balanced schedule's cross-CTA
+    # waits end too, and a normal call right after is right.
+    w = workloads.custom(1, 3, 640, D, "bf16", False, seed=78)
+    q, k, v = (t.cuda() for t in workloads.make_inputs(w))
+    do = workloads.make_grad_output(w).cuda()
+    O, L = fa2.attention_forward(q, k, v, scale=w.scale)
+    torch.cuda.synchronize()
+    assert fa2.fa2_device_status(clear=True) == 0
+    lib = fa2.library()
+    try:
+        fa2.fa2_set_watchdog_ns(20_000_000)  # 20 ms
+        assert lib.fa2_test_withhold_next_load(1) == fa2.FA2_OK
+        fa2.attention_backward(q, k, v, O, L, do, scale=w.scale, schedule=schedule)
+        torch.cuda.synchronize()  # returns: every wait in the kernel is bounded
+        assert fa2.fa2_device_status(clear=True) != 0, "the withheld tile should have made a wait run out"
+    finally:
+        lib.fa2_test_withhold_next_load(0)
+        fa2.fa2_set_watchdog_ns(0)
+    dq, dk, dv = fa2.attention_backward(q, k, v, O, L, do, scale=w.scale, schedule=schedule)
+    torch.cuda.synchronize()
+    assert fa2.fa2_device_status(clear=True) == 0
+    ref = oracle_mod.attention_bwd(q.cpu(), k.cpu(), v.cpu(), do.cpu(), w.scale, False, magnitudes=True)
+    u = 2.0 ** -8
+    for name, g in zip(("dq", "dk", "dv"), (dq, dk, dv)):
+        r, m = ref[name], ref[name + "_mag"]
+        bound = 3 * u * m + u * np.abs(r) + 2.0 ** -20 * m.max()
+        assert float((np.abs(g.float().cpu().numpy() - r) / bound).max()) <= 1.0, name
+
