@@ -554,8 +554,9 @@ def main(argv=None):
     ap.add_argument("--workload", default="target", choices=sorted(workloads.WORKLOADS))
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--schedule", default="auto", choices=["auto", "balanced", "units"],
-                    help="auto: the binding's choice; balanced: fa2_fwd_ws (equal K/V-tile steps per SM); "
-                         "units: fa2_fwd")
+                    help="forward: auto = the binding's choice, balanced = fa2_fwd_ws (equal K/V-tile steps per "
+                         "SM), units = fa2_fwd; backward (--pass bwd): the same choice passed to fa2_bwd_sched "
+                         "(auto = the library's)")
     ap.add_argument("--settle-seconds", type=float, default=1.0)
     ap.add_argument("--e2e-heads-per-chunk", type=int, default=0,
                     help="heads per chunk of the end-to-end host-memory pipeline (0 = the binding's default)")
