@@ -45,10 +45,12 @@ BwdWorkspace workspace_layout(int64_t bh, int N, int D) {
 
 // Cost of the busiest CTA in query steps under the round schedule (units
 // dealt in rounds, zig-zag when causal: the kernel's bwd_round_unit and
-// bwd_unit), or -1 when there are too many units to count here.
+// bwd_unit), or -1 when there are too many causal units to count on every
+// call (the count is one pass over the units; past 2^15 units the zig-zag
+// rounds are many and even, and the rounds are kept).
 long long round_schedule_cost(long long units, int bh, int nkv, int nq, int steps_per_tile, bool causal, int grid) {
   if (!causal) return (units + grid - 1) / grid * nq;
-  if (units > (1ll << 22)) return -1;
+  if (units > (1ll << 15)) return -1;
   long long worst = 0;
   for (int b = 0; b < grid; ++b) {
     long long sum = 0;

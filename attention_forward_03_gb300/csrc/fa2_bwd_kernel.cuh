@@ -139,6 +139,18 @@ struct BwdLayout {
   static constexpr uint32_t kColDP = 2 * kDp + kSR;
   static constexpr uint32_t kColDQ = 2 * kDp + 2 * kSR;
   static_assert(kColDQ + kSR <= kTmemCols, "TMEM budget");
+  // With 64-row steps (Dp = 128) the 64 columns past dQ^T can hold the
+  // step's P^T and dS^T as packed 16-bit pairs: the A operands of dV += P^T
+  // dO and dK += dS^T Q then come from tensor memory (the faster form of the
+  // MMA, and no shared-memory operand reads for them). dS^T also goes to
+  // shared memory, where dQ^T = K^T dS^T reads it as its B operand. Used by
+  // non-causal launches only (the kernel's kATmem): measured +1.8 % (target)
+  // and +2.5 % (B4 H16 N8192 D128) there, but -2.4 % on long causal rows,
+  // whose single issuer waits on the compute threads' extra TMEM stores.
+  static constexpr bool kGradATmem = (kSR == 64);
+  static constexpr uint32_t kColPT = kColDQ + kSR;
+  static constexpr uint32_t kColDST = kColPT + kSR / 2;
+  static_assert(!kGradATmem || kColDST + kSR / 2 <= kTmemCols, "TMEM budget");
   static_assert(kSmemBytes <= 232448, "shared memory budget");
   static_assert(kRing % 1024 == 0 && kP % 1024 == 0 && kDS % 1024 == 0, "swizzled tiles need 1 KB alignment");
 };
@@ -251,6 +263,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                    const __grid_constant__ CUtensorMap tmDQ, const BwdParams p) {
   using L = BwdLayout<D>;
   constexpr bool kTwoIssuers = !kCausal;
+  constexpr bool kATmem = L::kGradATmem && !kCausal;  // P^T, dS^T in TMEM for dV, dK
   constexpr uint32_t kReaders = kTwoIssuers ? 2 : 1;  // issuer threads reading a ring slot and K/V
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   const uint32_t raw = smem_addr(smem_raw);
@@ -430,13 +443,21 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         for (int kk = 0; kk < L::kSR / 16; ++kk) {
           const uint32_t a = static_cast<uint32_t>(((kk >> 2) * kPanelBytes + (kk & 3) * 32) >> 4);
           const uint32_t b = static_cast<uint32_t>((kk * 16 * 128) >> 4);
-          mma_ss_w(tmem + L::kColDV, p_lo + a, kHi, do_mn + b, kHi, idesc_acc, (acc || kk > 0) ? 1u : 0u);
+          const uint32_t acc_kk = (acc || kk > 0) ? 1u : 0u;
+          if constexpr (kATmem)  // A = P^T in TMEM: 16 query columns = 8 packed columns per K-step
+            mma_ts_w(tmem + L::kColDV, tmem + L::kColPT + 8u * kk, do_mn + b, kHi, idesc_acc, acc_kk);
+          else
+            mma_ss_w(tmem + L::kColDV, p_lo + a, kHi, do_mn + b, kHi, idesc_acc, acc_kk);
         }
 #pragma unroll
         for (int kk = 0; kk < L::kSR / 16; ++kk) {
           const uint32_t a = static_cast<uint32_t>(((kk >> 2) * kPanelBytes + (kk & 3) * 32) >> 4);
           const uint32_t b = static_cast<uint32_t>((kk * 16 * 128) >> 4);
-          mma_ss_w(tmem + L::kColDK, ds_lo + a, kHi, q_mn + b, kHi, idesc_acc, (acc || kk > 0) ? 1u : 0u);
+          const uint32_t acc_kk = (acc || kk > 0) ? 1u : 0u;
+          if constexpr (kATmem)
+            mma_ts_w(tmem + L::kColDK, tmem + L::kColDST + 8u * kk, q_mn + b, kHi, idesc_acc, acc_kk);
+          else
+            mma_ss_w(tmem + L::kColDK, ds_lo + a, kHi, q_mn + b, kHi, idesc_acc, acc_kk);
         }
       };
       // dQ_i^T = K^T dS^T: A = K read MN-major (M = head-dim index, two
@@ -737,10 +758,17 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           // the 64-column panel that holds them
           const int qc = L::kCW * wg + 32 * h;  // first query column of this half in the step
           const uint32_t panel = static_cast<uint32_t>((qc >> 6) * kPanelBytes);
+          if constexpr (kATmem) {
+            // P^T and dS^T of these 32 query columns into this thread's TMEM
+            // lane (16 packed columns per warpgroup)
+            tmem_st32x16(tmem + lane_off + L::kColPT + static_cast<uint32_t>(qc / 2), pk);
+            tmem_st32x16(tmem + lane_off + L::kColDST + static_cast<uint32_t>(qc / 2), dk);
+          }
 #pragma unroll
           for (int ch = 0; ch < 4; ++ch) {
             const uint32_t col = panel + ((static_cast<uint32_t>(((qc & 63) >> 3) + ch) ^ xr) << 4);
-            st_shared_v4(p_row + col, pk[4 * ch], pk[4 * ch + 1], pk[4 * ch + 2], pk[4 * ch + 3]);
+            if constexpr (!kATmem)
+              st_shared_v4(p_row + col, pk[4 * ch], pk[4 * ch + 1], pk[4 * ch + 2], pk[4 * ch + 3]);
             st_shared_v4(ds_row + col, dk[4 * ch], dk[4 * ch + 1], dk[4 * ch + 2], dk[4 * ch + 3]);
           }
         }
@@ -748,6 +776,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           ok = false;
           break;
         }
+        if constexpr (kATmem) tmem_wait_st();
         fence_proxy_async_shared();
         tc_fence_before_sync();
         mbar_arrive(bar_p_full);

@@ -21,9 +21,11 @@ namespace fa2 {
 constexpr int kThreads = 384;     // 3 warpgroups
 constexpr int kMmaWarp = 8;       // first MMA issuer warp
 constexpr int kLoadWarp = 10;
-// Two MMA issuers, one per sub-tile: a thread issuing tcgen05.mma is held
-// until the tensor core takes each instruction (~90-110 cycles for these
-// M=128 x N=128 x K=16 steps), so one thread cannot keep the tensor core busy.
+// Two MMA issuers (one per sub-tile, or one per instruction type: every S
+// and every P.V; each kernel says which): a thread issuing tcgen05.mma is
+// held until the tensor core takes each instruction (~90-110 cycles for
+// these M=128 x N=128 x K=16 steps), so one thread cannot keep the tensor
+// core busy.
 constexpr int kIssuers = 2;
 // Registers: the launch gives every thread kLaunchRegs (= 65536 / 384 rounded
 // down to 8); the softmax warpgroups then take kSoftmaxRegs and the third

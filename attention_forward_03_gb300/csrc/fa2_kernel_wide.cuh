@@ -15,8 +15,9 @@
 //   warps 0-3  softmax warpgroup (thread = query row = TMEM lane)
 //   warps 4-7  idle (they keep the launch's register split of the other
 //              forward kernel; the softmax of one sub-tile is one warpgroup)
-//   warp  8    S issuer: S(j) = Q K_j^T into S buffer j mod 2 (16 K-steps);
-//              owns the TMEM allocation
+//   warp  8    S issuer: S(j) = Q K_j^T into S buffer n mod 2, n the number
+//              of tiles the CTA has taken so far (16 K-steps); owns the TMEM
+//              allocation
 //   warp  9    P.V issuer: O (+)= P(j) V_j (8 K-steps of N = 256)
 //   warp 10    TMA producer; warp 11 idle
 // Tensor memory: [0,128) S buffer 0, [128,256) S buffer 1, [256,512) O.
