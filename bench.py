@@ -237,6 +237,28 @@ def oracle_rows(w: workloads.Workload, target_seconds: float, inputs):
     return np.sort(rng.choice(total, size=want, replace=False)) if want < total else None
 
 
+def host_cpu_model() -> str:
+    """The host CPU's model (best effort from /proc/cpuinfo: the model name where
+    there is one, else the Arm implementer and part codes)."""
+    import platform
+    fields = {}
+    try:
+        with open("/proc/cpuinfo") as fh:
+            for line in fh:
+                key, _, val = line.partition(":")
+                key, val = key.strip().lower(), val.strip()
+                if val and key not in fields:
+                    fields[key] = val
+    except OSError:
+        pass
+    for key in ("model name", "cpu model", "hardware"):
+        if key in fields:
+            return fields[key]
+    if "cpu part" in fields:
+        return f"{platform.machine()} (CPU implementer {fields.get('cpu implementer', '?')}, part {fields['cpu part']})"
+    return platform.processor() or platform.machine()
+
+
 def time_oracle(w: workloads.Workload, rows, inputs):
     """One timed oracle call on `rows` (None = every row).
     Returns (tflops, seconds, rows, threads, description)."""
@@ -286,7 +308,7 @@ def run_reference(args, w, rank, world):
         "data": "synthetic (seeded N(0, sigma^2) inputs, cast to the workload's 16-bit dtype)",
         "config": {"workload": w.describe(), "B": w.B, "H": w.H, "N": w.N, "D": w.D, "causal": w.causal,
                    "input_dtype": w.dtype, "l2": "host CPU run; no GPU L2 involved"},
-        "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle", "sample": desc},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "cpu_model": host_cpu_model(), "kind": "oracle", "sample": desc},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     return line
@@ -424,7 +446,7 @@ def run_gb300(args, w, rank, world, local):
     }
     if not args.no_cpu_baseline:
         tf, secs, rows, threads, desc = oracle_sample(w, args.cpu_seconds)
-        line["cpu_baseline"] = {"value": tf, "unit": UNIT, "cores": threads, "kind": "oracle", "sample": desc,
+        line["cpu_baseline"] = {"value": tf, "unit": UNIT, "cores": threads, "cpu_model": host_cpu_model(), "kind": "oracle", "sample": desc,
                                 "seconds": secs}
     return line
 
@@ -541,7 +563,7 @@ def run_gb300_bwd(args, w, rank, world, local):
     }
     if not args.no_cpu_baseline:
         tf, secs, threads, desc = time_grad_oracle(w, [0], (q, k, v, do))
-        line["cpu_baseline"] = {"value": tf, "unit": UNIT, "cores": threads, "kind": "oracle", "sample": desc,
+        line["cpu_baseline"] = {"value": tf, "unit": UNIT, "cores": threads, "cpu_model": host_cpu_model(), "kind": "oracle", "sample": desc,
                                 "seconds": secs}
     return line
 
