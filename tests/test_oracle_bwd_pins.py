@@ -67,7 +67,7 @@ def pin_autograd(grad, oracle_mod):
     """torch autograd through softmax(scale Q K^T [+ mask]) V in float64 on the CPU."""
     worst = 0.0
     for (B, H, N, D, causal, seed) in [(1, 2, 37, 16, False, 43), (2, 1, 29, 8, True, 44),
-                                       (1, 1, 64, 32, True, 45)]:
+                                       (1, 1, 64, 32, True, 45), (1, 1, 30, 96, False, 46)]:
         q, k, v, do = _rand(B, H, N, D, seed)
         scale = 1 / math.sqrt(D)
         r = grad(q, k, v, do, scale, causal)

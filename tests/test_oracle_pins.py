@@ -169,7 +169,8 @@ def pin_library_softmax(attn):
     """torch.softmax / logsumexp in float64 on the CPU (a textbook routine) on small shapes."""
     worst = 0.0
     for (B, H, N, D, causal, seed) in [(1, 2, 45, 16, False, 18), (2, 1, 33, 8, True, 19),
-                                       (1, 1, 128, 64, False, 20), (1, 1, 70, 32, True, 21)]:
+                                       (1, 1, 128, 64, False, 20), (1, 1, 70, 32, True, 21),
+                                       (1, 1, 40, 96, True, 23), (1, 2, 36, 256, False, 24)]:
         q, k, v = _rand(B, H, N, D, seed)
         scale = 1 / math.sqrt(D)
         O, L = attn(q, k, v, scale, causal)
