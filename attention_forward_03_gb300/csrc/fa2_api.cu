@@ -104,8 +104,8 @@ bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
   return x < y + nb && y < x + na;
 }
 
-using LaunchFn = cudaError_t (*)(const CUtensorMap&, const CUtensorMap&, const CUtensorMap&, const Params&, int,
-                                 cudaStream_t);
+using LaunchFn = cudaError_t (*)(const CUtensorMap&, const CUtensorMap&, const CUtensorMap&, const CUtensorMap&,
+                                 const Params&, int, cudaStream_t);
 
 template <int D>
 LaunchFn pick_d(bool bf, bool c) {
@@ -185,11 +185,11 @@ int launch(const void* Q, const void* K, const void* V, void* O, float* LSE, int
   if (info->cc_major != 10 || info->cc_minor != 3) return FA2_ERR_UNSUPPORTED;
   if (workspace && workspace_bytes < stream_k_workspace_bytes(info->sms, D)) return FA2_ERR_INVALID_ARG;
 
-  CUtensorMap mq, mk, mv;
+  CUtensorMap mq, mk, mv, mo;
   // V boxes: 128 rows, or at head dim 256 64 rows (the kernel streams V in
-  // halves of 64 keys there)
+  // halves of 64 keys there); O: the kernel stores it through a map at D >= 96
   if (!make_map(&mq, Q, (int)bh, N, D, dtype) || !make_map(&mk, K, (int)bh, N, D, dtype) ||
-      !make_rows_map(&mv, V, (int)bh, N, D, dtype, D == 256 ? 64u : 128u)) {
+      !make_rows_map(&mv, V, (int)bh, N, D, dtype, D == 256 ? 64u : 128u) || !make_map(&mo, O, (int)bh, N, D, dtype)) {
     std::snprintf(t_last_cuda_error, sizeof(t_last_cuda_error), "cuTensorMapEncodeTiled failed");
     return FA2_ERR_CUDA;
   }
@@ -231,7 +231,7 @@ int launch(const void* Q, const void* K, const void* V, void* O, float* LSE, int
     p.stream_k = 0;
     grid = p.num_units < info->sms ? p.num_units : info->sms;
   }
-  e = pick(D, dtype, is_causal)(mq, mk, mv, p, grid, stream);
+  e = pick(D, dtype, is_causal)(mq, mk, mv, mo, p, grid, stream);
   if (e != cudaSuccess) return record_cuda(e);
   return FA2_OK;
 }

@@ -58,6 +58,8 @@ enum : int {
   kSitePartialFlag = 10,
   kSiteMmaSFree = 11,
   kSiteSoftmaxPFree = 12,
+  kSiteOStaged = 13,
+  kSiteOBufFree = 14,
 };
 
 // A work unit is kR 128-row query sub-tiles: kR = 2 (256 rows, head dims up

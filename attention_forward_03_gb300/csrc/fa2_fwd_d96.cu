@@ -2,12 +2,12 @@
 #include "fa2_kernel.cuh"
 
 namespace fa2 {
-template cudaError_t launch_fwd<96, false, false>(const CUtensorMap&, const CUtensorMap&, const CUtensorMap&,
+template cudaError_t launch_fwd<96, false, false>(const CUtensorMap&, const CUtensorMap&, const CUtensorMap&, const CUtensorMap&,
                                                   const Params&, int, cudaStream_t);
-template cudaError_t launch_fwd<96, false, true>(const CUtensorMap&, const CUtensorMap&, const CUtensorMap&,
+template cudaError_t launch_fwd<96, false, true>(const CUtensorMap&, const CUtensorMap&, const CUtensorMap&, const CUtensorMap&,
                                                  const Params&, int, cudaStream_t);
-template cudaError_t launch_fwd<96, true, false>(const CUtensorMap&, const CUtensorMap&, const CUtensorMap&,
+template cudaError_t launch_fwd<96, true, false>(const CUtensorMap&, const CUtensorMap&, const CUtensorMap&, const CUtensorMap&,
                                                  const Params&, int, cudaStream_t);
-template cudaError_t launch_fwd<96, true, true>(const CUtensorMap&, const CUtensorMap&, const CUtensorMap&,
+template cudaError_t launch_fwd<96, true, true>(const CUtensorMap&, const CUtensorMap&, const CUtensorMap&, const CUtensorMap&,
                                                 const Params&, int, cudaStream_t);
 }  // namespace fa2

@@ -84,8 +84,8 @@ struct Layout {
   static constexpr int kRingOffset = kPOffset + (kPInTmem ? 0 : kSubTiles * kPTileBytes);
   static constexpr int kBarOffset = kRingOffset + kStages * kTileBytes;
   // barriers: q_full, q_empty, ring full (K tile)[S], ring full (V tile)[S], ring empty[S], s_full[2],
-  // s_free[2], p_full[2], p_free[2], o_full[2], drain[2], part_done[2]
-  static constexpr int kNumBars = 2 + 3 * kStages + 2 * 7;
+  // s_free[2], p_full[2], p_free[2], o_full[2], drain[2], part_done[2], o_staged[2], o_buf_free[2]
+  static constexpr int kNumBars = 2 + 3 * kStages + 2 * 9;
   static constexpr int kMiscOffset = kBarOffset + kNumBars * 8;
   static constexpr int kSmemBytes = kMiscOffset + 16 + 1024;  // + slack for 1 KB alignment
   static constexpr uint32_t kColO = 2 * kKeys;                 // O0 at 256, O1 at 256 + kDp
@@ -97,7 +97,8 @@ struct Layout {
 template <int D, bool kBf16, bool kCausal>
 __global__ void __launch_bounds__(kThreads, 1)
     fa2_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
-                   const __grid_constant__ CUtensorMap tmV, const Params p) {
+                   const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmO,
+                   const Params p) {
   using L = Layout<D>;
   // MMA issuers split by instruction type (one thread for every S, one for
   // every P.V) or by sub-tile (each thread S and P.V of one sub-tile). Both
@@ -129,6 +130,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t bar_o_full0 = bar_p_free0 + 16;              // [sub-tile]
   const uint32_t bar_drain = bar_o_full0 + 16;                // [issuer]
   const uint32_t bar_part0 = bar_drain + 16;                  // [sub-tile]
+  // Epilogue at D >= 96: O of sub-tile t is staged in its (then idle) P
+  // buffer and stored by TMA; o_staged counts the warpgroup's rows written,
+  // o_buf_free tells it the store engine has read the buffer.
+  const uint32_t bar_ostage0 = bar_part0 + 16;                // [sub-tile]
+  const uint32_t bar_obuf0 = bar_ostage0 + 16;                // [sub-tile]
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kMiscOffset);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kMiscOffset + 4);
 
@@ -153,6 +159,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(bar_o_full0 + 8 * t, 1);
       mbar_init(bar_drain + 8 * t, 1);
       mbar_init(bar_part0 + 8 * t, 4 * 32);
+      mbar_init(bar_ostage0 + 8 * t, 4 * 32);
+      mbar_init(bar_obuf0 + 8 * t, 1);
     }
     *abort_flag = 0;
     mbar_init_fence();
@@ -427,11 +435,25 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t p_xor = static_cast<uint32_t>(rr & 7);
     const float c = p.scale_log2;
     uint32_t s_phase = 0, o_phase = 0, part_phase = 0;
+    // D >= 96, O staged in the P buffer (see the epilogue): bit 0 the parity
+    // of the next o_staged phase, bit 1 that of o_buf_free, bit 2 set while
+    // the buffer holds an O whose store may still be reading it
+    uint32_t ost_state = 0;
     uint32_t p_count = 0;  // P tiles published so far (= P.V products issued or pending)
     bool ok = true;
     SegCursor cur = first_cursor(p);
     Segment w;
     while (ok && next_segment<kCausal>(cur, w, p)) {
+      if constexpr (!L::kPInTmem) {
+        // the previous segment's O was staged in this P buffer: the store
+        // engine must have read it before this segment's first P overwrites it
+        if (ost_state & 4u) {
+          bool fb = wait_bounded(bar_obuf0 + 8 * t, (ost_state >> 1) & 1u, wd, kSiteOBufFree);
+          fb = __all_sync(0xffffffffu, fb);
+          if (!fb) break;
+          ost_state = (ost_state ^ 2u) & ~4u;
+        }
+      }
       const int row = w.q0 + t * kRows + rr;
       const int limit = kCausal ? min(p.N, row + 1) : p.N;  // allowed keys: [0, limit)
       float m_raw = -CUDART_INF_F;  // running max of the raw scores seen so far
@@ -628,11 +650,45 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t pk[16];
 #pragma unroll
         for (int i = 0; i < 16; ++i) pk[i] = pack2(of[2 * i] * inv, of[2 * i + 1] * inv, kBf16);
-        if (live) {
-          uint4* dst = reinterpret_cast<uint4*>(orow + cc * 2);
+        if constexpr (L::kPInTmem) {
+          if (live) {
+            uint4* dst = reinterpret_cast<uint4*>(orow + cc * 2);
 #pragma unroll
-          for (int q = 0; q < 4; ++q) dst[q] = make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+            for (int q = 0; q < 4; ++q)
+              dst[q] = make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+          }
+        } else {
+          // into this row of the P buffer, in the 128-byte-swizzled layout
+          // of the O map's boxes (8-element chunk c of the row at panel c/8,
+          // chunk (c mod 8) xor (row mod 8))
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const int c8 = cc / 8 + q;
+            const uint32_t addr = p_row + static_cast<uint32_t>((c8 >> 3) * kPanelBytes) +
+                                  ((static_cast<uint32_t>(c8 & 7) ^ p_xor) << 4);
+            st_shared_v4(addr, pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+          }
         }
+      }
+      if constexpr (!L::kPInTmem) {
+        // One thread stores the staged tile with TMA once every row is in
+        // (rows past N are clipped by the map; a sub-tile wholly past N has
+        // nothing to store). Coalesced, asynchronous writes instead of each
+        // thread's 16-byte pieces of its own row, which serialised in the
+        // load/store unit (about 6,000 cycles per epilogue).
+        fence_proxy_async_shared();
+        mbar_arrive(bar_ostage0 + 8 * t);
+        if (rr == 0 && wait_bounded(bar_ostage0 + 8 * t, ost_state & 1u, wd, kSiteOStaged)) {
+          if (w.q0 + t * kRows < p.N) {
+            const uint32_t p_tile = sP + static_cast<uint32_t>(t * kPTileBytes);
+            for (int pn = 0; pn < L::kPanels; ++pn)
+              tma_store_3d(&tmO, p_tile + static_cast<uint32_t>(pn * kPanelBytes), pn * 64, w.q0 + t * kRows, w.bh);
+            bulk_commit_group();
+            bulk_wait_read_all();
+          }
+          mbar_arrive(bar_obuf0 + 8 * t);
+        }
+        ost_state = (ost_state ^ 1u) | 4u;
       }
       if (live) {
         p.lse[static_cast<size_t>(w.bh) * p.N + row] =
@@ -641,6 +697,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       // O_t is read out; the next segment's first P.V may overwrite it once
       // this warpgroup publishes that segment's first P (ordered by bar_p).
       tc_fence_before_sync();
+    }
+    // the O stores this thread issued complete before the CTA exits
+    if constexpr (!L::kPInTmem) {
+      if (rr == 0) bulk_wait_all();
     }
   }
 
@@ -655,8 +715,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 // The stream-K schedule waits across CTAs, so it is launched cooperatively
 // (the whole grid resident at once, or the launch fails).
 template <int D, bool kBf16, bool kCausal>
-cudaError_t launch_fwd(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v, const Params& p,
-                       int grid, cudaStream_t stream) {
+cudaError_t launch_fwd(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v, const CUtensorMap& o,
+                       const Params& p, int grid, cudaStream_t stream) {
   auto kern = fa2_fwd_kernel<D, kBf16, kCausal>;
   const int smem = Layout<D>::kSmemBytes;
   cudaFuncAttributes fa;
@@ -677,7 +737,7 @@ cudaError_t launch_fwd(const CUtensorMap& q, const CUtensorMap& k, const CUtenso
   attr[0].val.cooperative = p.stream_k ? 1 : 0;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kern, q, k, v, p);
+  return cudaLaunchKernelEx(&cfg, kern, q, k, v, o, p);
 }
 
 }  // namespace fa2

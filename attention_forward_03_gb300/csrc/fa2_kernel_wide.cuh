@@ -541,8 +541,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 // The stream-K schedule waits across CTAs, so it is launched cooperatively
 // (the whole grid resident at once, or the launch fails).
 template <int D, bool kBf16, bool kCausal>
-cudaError_t launch_fwd_wide(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v, const Params& p,
-                            int grid, cudaStream_t stream) {
+cudaError_t launch_fwd_wide(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v,
+                            const CUtensorMap& /*o: stored directly at this head dim*/, const Params& p, int grid,
+                            cudaStream_t stream) {
   auto kern = fa2_fwd_wide_kernel<D, kBf16, kCausal>;
   const int smem = WideLayout<D>::kSmemBytes;
   cudaFuncAttributes fa;

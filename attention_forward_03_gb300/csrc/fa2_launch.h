@@ -130,13 +130,15 @@ template <int D, bool kBf16, bool kCausal>
 cudaError_t launch_bwd(const CUtensorMap& k, const CUtensorMap& v, const CUtensorMap& q, const CUtensorMap& dout,
                        const CUtensorMap& dq_acc, const BwdParams& p, int grid, cudaStream_t stream);
 
+// q, k, v: the input maps; o: the output's map (boxes of 128 rows x 64
+// elements, 128-byte swizzle), through which the kernel stores O at D >= 96.
 template <int D, bool kBf16, bool kCausal>
-cudaError_t launch_fwd(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v, const Params& p,
-                       int grid, cudaStream_t stream);
+cudaError_t launch_fwd(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v, const CUtensorMap& o,
+                       const Params& p, int grid, cudaStream_t stream);
 
 // Head dim 256 (fa2_kernel_wide.cuh, instantiated in fa2_fwd_d256.cu).
 template <int D, bool kBf16, bool kCausal>
-cudaError_t launch_fwd_wide(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v, const Params& p,
-                            int grid, cudaStream_t stream);
+cudaError_t launch_fwd_wide(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v, const CUtensorMap& o,
+                            const Params& p, int grid, cudaStream_t stream);
 
 }  // namespace fa2
