@@ -1,6 +1,6 @@
 """Thin ctypes binding over the C ABI in include/fa2.h (argument marshalling only).
 
-Every step of the forward pass runs in the sm_103a kernels of
+Every step of the forward and backward passes runs in the sm_103a kernels of
 libfa2_gb300.so. This module only turns tensors into pointers, sizes and a
 stream handle, and turns status codes into exceptions. There is no fallback:
 if the library is missing, importing the functions below raises.
