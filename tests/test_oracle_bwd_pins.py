@@ -18,6 +18,14 @@ import numpy as np
 import pytest
 import torch
 
+
+def _worst(*errors) -> float:
+    """The largest of the given errors, with NaN counted as the worst possible
+    (the built-in max keeps its first argument when a later one is NaN)."""
+    vals = [float(e) for e in errors]
+    return math.inf if any(math.isnan(x) for x in vals) else max(vals)
+
+
 TOL = 1e-11       # pins that hold up to fp64 rounding
 FD_TOL = 1e-7     # central differences, step 1e-5 (truncation ~h^2, rounding ~eps/h)
 
@@ -59,7 +67,7 @@ def pin_finite_differences(grad, oracle_mod):
                     plus[idx][0, 0, i, d] += h
                     minus[idx][0, 0, i, d] -= h
                     num[i, d] = (loss(*plus) - loss(*minus)) / (2 * h)
-            worst = max(worst, np.abs(r[name][0, 0] - num).max() / FD_TOL)
+            worst = _worst(worst, np.abs(r[name][0, 0] - num).max() / FD_TOL)
     return worst
 
 
@@ -78,7 +86,7 @@ def pin_autograd(grad, oracle_mod):
         O = torch.softmax(S, dim=-1) @ tv
         O.backward(torch.from_numpy(do))
         for name, t in (("dq", tq), ("dk", tk), ("dv", tv)):
-            worst = max(worst, np.abs(r[name] - t.grad.numpy()).max() / TOL)
+            worst = _worst(worst, np.abs(r[name] - t.grad.numpy()).max() / TOL)
     return worst
 
 
@@ -104,9 +112,9 @@ def pin_uniform_weights(grad, oracle_mod):
             for j in range(N):
                 for i in range(j if causal else 0, N):
                     expect[j] += do[0, 0, i] / cnt[i]
-            worst = max(worst, np.abs(r["dv"][0, 0] - expect).max() / TOL)
+            worst = _worst(worst, np.abs(r["dv"][0, 0] - expect).max() / TOL)
             if mode == "same_k":
-                worst = max(worst, np.abs(r["dq"]).max() / TOL)
+                worst = _worst(worst, np.abs(r["dq"]).max() / TOL)
     return worst
 
 
@@ -117,7 +125,7 @@ def pin_dk_sums_to_zero(grad, oracle_mod):
         q, k, v, do = _rand(1, 2, 33, 8, seed)
         r = grad(q, k, v, do, 0.4, causal)
         scale_ref = np.abs(r["dk"]).max()
-        worst = max(worst, np.abs(r["dk"].sum(axis=2)).max() / (TOL * max(1.0, 33 * scale_ref)))
+        worst = _worst(worst, np.abs(r["dk"].sum(axis=2)).max() / (TOL * max(1.0, 33 * scale_ref)))
     return worst
 
 
@@ -127,7 +135,7 @@ def pin_single_key(grad, oracle_mod):
     worst = 0.0
     for causal in (False, True):
         r = grad(q, k, v, do, 0.3, causal)
-        worst = max(worst, np.abs(r["dq"]).max() / TOL, np.abs(r["dk"]).max() / TOL,
+        worst = _worst(worst, np.abs(r["dq"]).max() / TOL, np.abs(r["dk"]).max() / TOL,
                     np.abs(r["dv"] - do).max() / TOL)
     return worst
 
@@ -138,7 +146,7 @@ def pin_permutation(grad, oracle_mod):
     perm = np.random.default_rng(51).permutation(27)
     r1 = grad(q, k, v, do, 0.5, False)
     r2 = grad(q, k[:, :, perm], v[:, :, perm], do, 0.5, False)
-    return max(np.abs(r1["dq"] - r2["dq"]).max(), np.abs(r1["dk"][:, :, perm] - r2["dk"]).max(),
+    return _worst(np.abs(r1["dq"] - r2["dq"]).max(), np.abs(r1["dk"][:, :, perm] - r2["dk"]).max(),
                np.abs(r1["dv"][:, :, perm] - r2["dv"]).max()) / TOL
 
 
@@ -153,17 +161,17 @@ def pin_causal_structure(grad, oracle_mod):
         k2[0, 0, i + 1:] += 2.0
         v2[0, 0, i + 1:] -= 1.5
         r2 = grad(q, k2, v2, do, 0.4, True)
-        worst = max(worst, np.abs(r1["dq"][0, 0, :i + 1] - r2["dq"][0, 0, :i + 1]).max() / TOL)
+        worst = _worst(worst, np.abs(r1["dq"][0, 0, :i + 1] - r2["dq"][0, 0, :i + 1]).max() / TOL)
         if np.abs(r1["dq"][0, 0, i + 1:] - r2["dq"][0, 0, i + 1:]).max() < 1e-6:
-            worst = max(worst, 1e3)
+            worst = _worst(worst, 1e3)
         q3, do3 = q.copy(), do.copy()
         q3[0, 0, :i] += 1.0
         do3[0, 0, :i] *= -2.0
         r3 = grad(q3, k, v, do3, 0.4, True)
-        worst = max(worst, np.abs(r1["dk"][0, 0, i:] - r3["dk"][0, 0, i:]).max() / TOL,
+        worst = _worst(worst, np.abs(r1["dk"][0, 0, i:] - r3["dk"][0, 0, i:]).max() / TOL,
                     np.abs(r1["dv"][0, 0, i:] - r3["dv"][0, 0, i:]).max() / TOL)
         if i > 0 and np.abs(r1["dv"][0, 0, :i] - r3["dv"][0, 0, :i]).max() < 1e-6:
-            worst = max(worst, 1e3)
+            worst = _worst(worst, 1e3)
     return worst
 
 
@@ -174,7 +182,7 @@ def pin_delta_is_dout_dot_output(grad, oracle_mod):
         q, k, v, do = _rand(2, 1, 25, 16, seed)
         r = grad(q, k, v, do, 0.25, causal)
         O, _ = oracle_mod.attention_fwd(q, k, v, 0.25, causal)
-        worst = max(worst, np.abs(r["delta"] - np.einsum("bhnd,bhnd->bhn", do, O)).max() / TOL)
+        worst = _worst(worst, np.abs(r["delta"] - np.einsum("bhnd,bhnd->bhn", do, O)).max() / TOL)
     return worst
 
 
@@ -187,8 +195,8 @@ def pin_magnitudes(grad, oracle_mod):
     for causal in (False, True):
         r = grad(q, k, v, do, 0.5, causal, magnitudes=True)
         for name in ("dq", "dk", "dv"):
-            worst = max(worst, np.max(np.abs(r[name]) - r[name + "_mag"]) / TOL)
-        worst = max(worst, np.abs(r["dv_mag"] - r["dv"]).max() / TOL)
+            worst = _worst(worst, np.max(np.abs(r[name]) - r[name + "_mag"]) / TOL)
+        worst = _worst(worst, np.abs(r["dv_mag"] - r["dv"]).max() / TOL)
     return worst
 
 
@@ -201,7 +209,7 @@ def pin_head_selection(grad, oracle_mod):
     for r, bh in enumerate((5, 1)):
         b, h = divmod(bh, 3)
         for name in ("dq", "dk", "dv"):
-            worst = max(worst, np.abs(part[name][r] - full[name][b, h]).max() / TOL)
+            worst = _worst(worst, np.abs(part[name][r] - full[name][b, h]).max() / TOL)
     return worst
 
 

@@ -20,6 +20,14 @@ import torch
 
 import workloads
 
+
+def _worst(*errors) -> float:
+    """The largest of the given errors, with NaN counted as the worst possible
+    (the built-in max keeps its first argument when a later one is NaN)."""
+    vals = [float(e) for e in errors]
+    return math.inf if any(math.isnan(x) for x in vals) else max(vals)
+
+
 GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
 TOL = 1e-11
 
@@ -55,7 +63,7 @@ def pin_closed_forms(attn):
         O, L = attn(Q[None, None], K[None, None], V[None, None], c["scale"], c["causal"])
         Oexp = np.array([[ev(x) for x in r] for r in c["O"]])
         Lexp = np.array([ev(x) for x in c["LSE"]])
-        worst = max(worst, np.abs(O[0, 0, :m] - Oexp).max(), np.abs(L[0, 0, :m] - Lexp).max())
+        worst = _worst(worst, np.abs(O[0, 0, :m] - Oexp).max(), np.abs(L[0, 0, :m] - Lexp).max())
     return worst
 
 
@@ -68,7 +76,7 @@ def pin_online_merge(attn, oracle_mod):
         scale = 1 / math.sqrt(D)
         O, L = attn(q, k, v, scale, causal)
         o2, l2 = oracle_mod.online_merge(q[0, 0], k[0, 0], v[0, 0], scale, causal, block)
-        worst = max(worst, np.abs(O[0, 0] - o2).max(), np.abs(L[0, 0] - l2).max())
+        worst = _worst(worst, np.abs(O[0, 0] - o2).max(), np.abs(L[0, 0] - l2).max())
     # every score far below zero (the running-max initialisation case); LSE is ~ -1e3
     # there, so its agreement is checked relative to its size
     q, k, v = _rand(1, 1, 40, 8, 7)
@@ -76,7 +84,7 @@ def pin_online_merge(attn, oracle_mod):
     O, L = attn(q, k, v, 1.0, False)
     o2, l2 = oracle_mod.online_merge(q[0, 0], k[0, 0], v[0, 0], 1.0, False, 8)
     rel = np.abs(L[0, 0] - l2).max() / max(1.0, np.abs(l2).max())
-    worst = max(worst, np.abs(O[0, 0] - o2).max(), rel)
+    worst = _worst(worst, np.abs(O[0, 0] - o2).max(), rel)
     return worst
 
 
@@ -94,7 +102,7 @@ def pin_identical_keys(attn):
         for i in range(N):
             cnt = i + 1 if causal else N
             s = scale * float(q[0, 0, i] @ k[0, 0, 0])
-            worst = max(worst, np.abs(O[0, 0, i] - v[0, 0, :cnt].mean(axis=0)).max(),
+            worst = _worst(worst, np.abs(O[0, 0, i] - v[0, 0, :cnt].mean(axis=0)).max(),
                         abs(L[0, 0, i] - (s + math.log(cnt))))
     return worst
 
@@ -107,7 +115,7 @@ def pin_zero_query(attn):
     k = g.standard_normal((1, 2, N, D))
     v = g.standard_normal((1, 2, N, D))
     O, L = attn(q, k, v, 0.25, False)
-    return max(np.abs(O - v.mean(axis=2, keepdims=True)).max(), np.abs(L - math.log(N)).max())
+    return _worst(np.abs(O - v.mean(axis=2, keepdims=True)).max(), np.abs(L - math.log(N)).max())
 
 
 def pin_permutation(attn):
@@ -116,7 +124,7 @@ def pin_permutation(attn):
     perm = np.random.default_rng(14).permutation(31)
     O1, L1 = attn(q, k, v, 0.5, False)
     O2, L2 = attn(q, k[:, :, perm], v[:, :, perm], 0.5, False)
-    return max(np.abs(O1 - O2).max(), np.abs(L1 - L2).max())
+    return _worst(np.abs(O1 - O2).max(), np.abs(L1 - L2).max())
 
 
 def pin_causal_prefix(attn):
@@ -130,11 +138,11 @@ def pin_causal_prefix(attn):
         k2[0, 0, i + 1:] += 3.0
         v2[0, 0, i + 1:] -= 2.0
         O2, L2 = attn(q, k2, v2, 0.4, True)
-        worst = max(worst, np.abs(O1[0, 0, :i + 1] - O2[0, 0, :i + 1]).max(),
+        worst = _worst(worst, np.abs(O1[0, 0, :i + 1] - O2[0, 0, :i + 1]).max(),
                     np.abs(L1[0, 0, :i + 1] - L2[0, 0, :i + 1]).max())
         # the changed rows must move (a mask that hid everything would pass the line above)
         if np.abs(O1[0, 0, i + 1:] - O2[0, 0, i + 1:]).max() < 1e-6:
-            worst = max(worst, 1.0)
+            worst = _worst(worst, 1.0)
     return worst
 
 
@@ -153,7 +161,7 @@ def pin_dominant_logit(attn):
     bound = math.exp(-gap) * (N - 1) * 2 * np.abs(v).max()
     err = np.abs(O[0, 0, i] - v[0, 0, j]).max()
     lse_err = abs(L[0, 0, i] - s[j])  # LSE -> max logit, error <= ln(1 + (N-1) e^-gap)
-    return max(0.0, err - bound, lse_err - math.log1p((N - 1) * math.exp(-gap)))
+    return _worst(0.0, err - bound, lse_err - math.log1p((N - 1) * math.exp(-gap)))
 
 
 def pin_single_key(attn):
@@ -162,7 +170,7 @@ def pin_single_key(attn):
     O, L = attn(q, k, v, 0.7, False)
     s = 0.7 * np.einsum("bhnd,bhnd->bhn", q, k)
     Oc, Lc = attn(q, k, v, 0.7, True)
-    return max(np.abs(O - v).max(), np.abs(L - s).max(), np.abs(Oc - v).max(), np.abs(Lc - s).max())
+    return _worst(np.abs(O - v).max(), np.abs(L - s).max(), np.abs(Oc - v).max(), np.abs(Lc - s).max())
 
 
 def pin_library_softmax(attn):
@@ -180,7 +188,7 @@ def pin_library_softmax(attn):
         P = torch.softmax(S, dim=-1)
         Oref = (P @ torch.from_numpy(v)).numpy()
         Lref = torch.logsumexp(S, dim=-1).numpy()
-        worst = max(worst, np.abs(O - Oref).max(), np.abs(L - Lref).max())
+        worst = _worst(worst, np.abs(O - Oref).max(), np.abs(L - Lref).max())
     return worst
 
 
@@ -192,7 +200,7 @@ def pin_row_sampling(attn):
     Os, Ls = attn(q, k, v, 0.5, True, rows=rows)
     Of = O.reshape(-1, 8)[rows]
     Lf = L.reshape(-1)[rows]
-    return max(np.abs(Os - Of).max(), np.abs(Ls - Lf).max())
+    return _worst(np.abs(Os - Of).max(), np.abs(Ls - Lf).max())
 
 
 PINS = [pin_closed_forms, pin_identical_keys, pin_zero_query, pin_permutation, pin_causal_prefix,
@@ -248,7 +256,7 @@ def test_online_merge_mutations_are_caught(oracle_mod, mutation, case):
     O, L = oracle_mod.attention_fwd(q, k, v, scale, False)
     good = oracle_mod.online_merge(q[0, 0], k[0, 0], v[0, 0], scale, False, block)
     bad = oracle_mod.online_merge(q[0, 0], k[0, 0], v[0, 0], scale, False, block, mutation=mutation)
-    assert max(np.abs(good[0] - O[0, 0]).max(), np.abs(good[1] - L[0, 0]).max()) < TOL
+    assert _worst(np.abs(good[0] - O[0, 0]).max(), np.abs(good[1] - L[0, 0]).max()) < TOL
     diff = np.abs(np.nan_to_num(bad[0], nan=1e9) - O[0, 0]).max()
     diff = max(diff, np.abs(np.nan_to_num(bad[1], nan=1e9, posinf=1e9) - L[0, 0]).max())
     assert diff > 1e-3
