@@ -36,6 +36,11 @@ SIGNATURES = {
     "fa2_fwd_ws": (ctypes.c_int, [_VP, _VP, _VP, _VP, _VP, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                   ctypes.c_int, ctypes.c_float, ctypes.c_int, ctypes.c_int, _VP, ctypes.c_size_t,
                                   _VP]),
+    "fa2_fwd_sched": (ctypes.c_int, [_VP, _VP, _VP, _VP, _VP, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                     ctypes.c_int, ctypes.c_float, ctypes.c_int, ctypes.c_int, _VP, ctypes.c_size_t,
+                                     ctypes.c_int, _VP]),
+    "fa2_fwd_schedule_for": (ctypes.c_int, [ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                            ctypes.c_int, ctypes.POINTER(ctypes.c_int)]),
     "fa2_fwd_noalloc": (ctypes.c_int, [_VP, _VP, _VP, _VP, _VP, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                        ctypes.c_int, ctypes.c_float, ctypes.c_int, ctypes.c_int, _VP]),
     "fa2_fwd_host_buffer_bytes": (ctypes.c_int, [ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
@@ -110,6 +115,22 @@ def fa2_fwd_ws(Q: int, K: int, V: int, O: int, LSE: int, B: int, H: int, N: int,
                                 int(workspace_bytes), stream)
 
 
+def fa2_fwd_sched(Q: int, K: int, V: int, O: int, LSE: int, B: int, H: int, N: int, D: int, scale: float,
+                  is_causal: int, dtype: int, workspace: int | None, workspace_bytes: int, schedule: int,
+                  stream: int | None) -> int:
+    """Pointer-level call with an explicit schedule code (FA2_SCHED_*); returns the raw status code."""
+    return library().fa2_fwd_sched(Q, K, V, O, LSE, B, H, N, D, float(scale), int(is_causal), int(dtype), workspace,
+                                   int(workspace_bytes), int(schedule), stream)
+
+
+def fa2_fwd_schedule_for(B: int, H: int, N: int, D: int, is_causal: bool, sms: int) -> int:
+    """The schedule code FA2_SCHED_AUTO takes for this problem on a device with `sms` SMs (host arithmetic)."""
+    out = ctypes.c_int(0)
+    _check(library().fa2_fwd_schedule_for(int(B), int(H), int(N), int(D), int(bool(is_causal)), int(sms),
+                                          ctypes.byref(out)), "fa2_fwd_schedule_for")
+    return out.value
+
+
 def fa2_fwd_workspace_bytes(D: int) -> int:
     n = ctypes.c_size_t(0)
     _check(library().fa2_fwd_workspace_bytes(int(D), ctypes.byref(n)), "fa2_fwd_workspace_bytes")
@@ -147,8 +168,12 @@ def fa2_bwd_sched(Q: int, K: int, V: int, O: int, dO: int, LSE: int, dQ: int, dK
 
 
 def fa2_device_status(stream: int | None = None, clear: bool = False) -> int:
+    """The device watchdog word: 0, or the site id of the wait that timed out (the C call then
+    returns FA2_ERR_TIMEOUT, which is reported here through the value, not raised)."""
     v = ctypes.c_int(0)
-    _check(library().fa2_device_status(stream, ctypes.byref(v), int(bool(clear))), "fa2_device_status")
+    code = library().fa2_device_status(stream, ctypes.byref(v), int(bool(clear)))
+    if code != FA2_ERR_TIMEOUT:
+        _check(code, "fa2_device_status")
     return v.value
 
 
@@ -171,13 +196,22 @@ def _dtype_code(t) -> int:
 
 
 _workspaces = {}
+_sm_counts = {}
 
 
-def workspace_for(device, D: int):
-    """A cached caller-side workspace (torch uint8 tensor) for fa2_fwd_ws on `device`."""
+def workspace_for(device, D: int, stream=None):
+    """A cached caller-side workspace (torch uint8 tensor) for the balanced schedule on `device`.
+
+    One per (device, head dim, stream): calls on one stream are ordered, so they
+    may share it; calls on different streams get different workspaces, since
+    two balanced launches that overlap on the GPU must not share one. The
+    cache keeps one workspace (about 21 MB on a 152-SM GPU) per stream used.
+    """
     import torch
     dev = torch.device(device)
-    key = (dev.index, D)
+    if stream is None:
+        stream = torch.cuda.current_stream(dev)
+    key = (dev.index, D, int(stream.cuda_stream))
     ws = _workspaces.get(key)
     if ws is None:
         with torch.cuda.device(dev):
@@ -187,9 +221,18 @@ def workspace_for(device, D: int):
     return ws
 
 
+def sm_count(device) -> int:
+    import torch
+    dev = torch.device(device)
+    n = _sm_counts.get(dev.index)
+    if n is None:
+        n = torch.cuda.get_device_properties(dev).multi_processor_count
+        _sm_counts[dev.index] = n
+    return n
+
+
 UNIT_ROWS = 256  # query rows per work unit of the kernel (head dims up to 128)
 KV_TILE = 128    # keys per K/V tile
-SPLIT_COST_STEPS = 4  # measured cost of a split unit (partial write, merge), in K/V-tile steps
 
 
 def unit_rows(D: int = 128) -> int:
@@ -208,22 +251,13 @@ def steps_per_head(N: int, is_causal: bool, D: int = 128) -> int:
 
 
 def choose_schedule(B: int, H: int, N: int, is_causal: bool, sms: int, D: int = 128) -> str:
-    """Pick the kernel schedule for a problem (a choice between two C entry points).
+    """The schedule the library's FA2_SCHED_AUTO takes for a problem ("units" or "balanced").
 
-    Cost in K/V-tile steps of the busiest SM: the round schedule (fa2_fwd)
-    takes ceil(units / SMs) rounds of whole units; the balanced schedule
-    (fa2_fwd_ws) takes total steps / SMs plus the cost of the partial-result
-    merge of the units it splits. Balanced is chosen when it is at least 5%
-    cheaper. Causal work stays on the round schedule, whose heaviest-first
-    zig-zag measured faster than the split on every causal workload.
+    The choice is made in C (fa2_fwd_schedule_for, the cost model of
+    fa2_fwd_sched); this only names it.
     """
-    units = B * H * -(-N // unit_rows(D))
-    if is_causal or units == 0:
-        return "units"
-    nkv = -(-N // KV_TILE)
-    rounds_cost = -(-units // sms) * nkv
-    balanced_cost = units * nkv / sms + SPLIT_COST_STEPS
-    return "balanced" if balanced_cost < 0.95 * rounds_cost else "units"
+    code = fa2_fwd_schedule_for(B, H, N, D, is_causal, sms)
+    return "balanced" if code == FA2_SCHED_BALANCED else "units"
 
 
 def attention_forward(q, k, v, scale: float | None = None, is_causal: bool = False, out=None, lse=None,
@@ -233,11 +267,12 @@ def attention_forward(q, k, v, scale: float | None = None, is_causal: bool = Fal
     Returns (O, LSE): O like q, LSE float32 [B, H, N]. `out` / `lse` may be
     passed to write into caller-owned buffers. Runs on `stream` (a
     torch.cuda.Stream) or the current stream.
-    schedule: "auto" (choose_schedule), "balanced" (fa2_fwd_ws with a
-    workspace: equal work per SM) or "units" (fa2_fwd: whole query tiles per
-    CTA, no workspace).
+    schedule: "auto" (the library's choice, fa2_fwd_sched with FA2_SCHED_AUTO),
+    "balanced" (equal work per SM, with a workspace) or "units" (whole query
+    tiles per CTA in rounds, no workspace).
     workspace: optional uint8 CUDA tensor for the balanced schedule; by default
-    a cached one per device is used.
+    a cached one per (device, head dim, stream) is used, so calls on different
+    streams never share one.
     """
     import torch
     if not (q.is_cuda and k.is_cuda and v.is_cuda):
@@ -251,9 +286,6 @@ def attention_forward(q, k, v, scale: float | None = None, is_causal: bool = Fal
     if schedule not in ("auto", "balanced", "units"):
         raise ValueError("schedule must be 'auto', 'balanced' or 'units'")
     B, H, N, D = q.shape
-    if schedule == "auto":
-        sms = torch.cuda.get_device_properties(q.device).multi_processor_count
-        schedule = choose_schedule(B, H, N, is_causal, sms, D)
     if scale is None:
         scale = 1.0 / math.sqrt(D)
     if out is None:
@@ -267,15 +299,14 @@ def attention_forward(q, k, v, scale: float | None = None, is_causal: bool = Fal
     s = stream if stream is not None else torch.cuda.current_stream(q.device)
     with torch.cuda.device(q.device):
         if schedule == "units":
-            code = fa2_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(),
-                           B, H, N, D, scale, int(bool(is_causal)), _dtype_code(q), s.cuda_stream)
-            _check(code, "fa2_fwd")
+            ws_ptr, ws_bytes = None, 0
         else:
-            ws = workspace if workspace is not None else workspace_for(q.device, D)
-            code = fa2_fwd_ws(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(),
-                              B, H, N, D, scale, int(bool(is_causal)), _dtype_code(q), ws.data_ptr(),
-                              ws.numel() * ws.element_size(), s.cuda_stream)
-            _check(code, "fa2_fwd_ws")
+            ws = workspace if workspace is not None else workspace_for(q.device, D, s)
+            ws_ptr, ws_bytes = ws.data_ptr(), ws.numel() * ws.element_size()
+        code = fa2_fwd_sched(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(),
+                             B, H, N, D, scale, int(bool(is_causal)), _dtype_code(q), ws_ptr, ws_bytes,
+                             _SCHEDULES[schedule], s.cuda_stream)
+        _check(code, "fa2_fwd_sched")
     return out, lse
 
 
@@ -331,7 +362,7 @@ def attention_forward_host(q, k, v, scale: float | None = None, is_causal: bool 
         raise ValueError("schedule must be 'auto', 'balanced' or 'units'")
     B, H, N, D = q.shape
     dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
-    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    sms = sm_count(dev)
     hpc = host_chunk_heads(B, H, N, is_causal, sms, D) if heads_per_chunk is None else int(heads_per_chunk)
     if hpc < 1:
         raise ValueError("heads_per_chunk must be >= 1")

@@ -21,7 +21,6 @@
 namespace fa2 {
 namespace {
 
-constexpr int kMaxDevices = 64;
 constexpr unsigned long long kDefaultWatchdogNs = 1000000000ull;
 
 __device__ int g_watchdog_word;  // 0 = no timeout since last clear
@@ -33,6 +32,7 @@ thread_local char t_last_cuda_error[256] = "";
 struct DeviceInfo {
   std::once_flag once;
   cudaError_t err = cudaSuccess;
+  bool supported = false;  // compute capability 10.3, and this library's device code loaded there
   int sms = 0;
   int cc_major = 0, cc_minor = 0;
   int* status = nullptr;
@@ -46,7 +46,9 @@ int record_cuda(cudaError_t e) {
 }
 
 // Device properties and the watchdog word's device address, once per device,
-// queried with that device current.
+// queried with that device current. The compute capability comes first: on
+// any other GPU this library's device code (sm_103a only) cannot load, so
+// the symbol lookup is not attempted there and the device is "unsupported".
 DeviceInfo* device_info(int dev) {
   if (dev < 0 || dev >= kMaxDevices) return nullptr;
   DeviceInfo& d = g_devices[dev];
@@ -54,10 +56,27 @@ DeviceInfo* device_info(int dev) {
     cudaError_t e = cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev);
     if (e == cudaSuccess) e = cudaDeviceGetAttribute(&d.cc_major, cudaDevAttrComputeCapabilityMajor, dev);
     if (e == cudaSuccess) e = cudaDeviceGetAttribute(&d.cc_minor, cudaDevAttrComputeCapabilityMinor, dev);
-    if (e == cudaSuccess) e = cudaGetSymbolAddress(reinterpret_cast<void**>(&d.status), g_watchdog_word);
+    if (e == cudaSuccess && d.cc_major == 10 && d.cc_minor == 3) {
+      e = cudaGetSymbolAddress(reinterpret_cast<void**>(&d.status), g_watchdog_word);
+      d.supported = e == cudaSuccess;
+    }
     d.err = e;
   });
   return &d;
+}
+
+// The current device's facts: FA2_OK, FA2_ERR_CUDA (recorded) or
+// FA2_ERR_UNSUPPORTED (not an sm_103 GPU).
+int current_device(DeviceInfo** out) {
+  int dev = 0;
+  const cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return record_cuda(e);
+  DeviceInfo* info = device_info(dev);
+  if (!info) return FA2_ERR_UNSUPPORTED;
+  if (info->err != cudaSuccess) return record_cuda(info->err);
+  if (!info->supported) return FA2_ERR_UNSUPPORTED;
+  *out = info;
+  return FA2_OK;
 }
 
 using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
@@ -78,21 +97,74 @@ EncodeTiledFn encode_fn() {
   return fn;
 }
 
+// Encoded tensor maps, cached by everything that goes into them (address,
+// shape, element type, box height), so that repeated calls on the same
+// buffers skip the encoding. A descriptor depends only on these values, so
+// an entry stays valid after its buffer is freed (a later buffer at the same
+// address with the same shape gets the same descriptor). Direct-mapped,
+// guarded by one lock.
+struct MapKey {
+  const void* ptr;
+  int bh, n, d, kind;  // kind: the 16-bit dtype code, or 16 for fp32 rows
+  unsigned rows;
+  bool operator==(const MapKey& o) const {
+    return ptr == o.ptr && bh == o.bh && n == o.n && d == o.d && kind == o.kind && rows == o.rows;
+  }
+};
+
+constexpr int kMapCacheSlots = 512;
+struct MapCache {
+  std::mutex mu;
+  bool used[kMapCacheSlots] = {};
+  MapKey key[kMapCacheSlots];
+  CUtensorMap map[kMapCacheSlots];
+};
+MapCache g_maps;
+
+uint32_t map_slot(const MapKey& k) {
+  uint64_t h = reinterpret_cast<uintptr_t>(k.ptr);
+  for (uint64_t v : {(uint64_t)k.bh, (uint64_t)k.n, (uint64_t)k.d, (uint64_t)k.kind, (uint64_t)k.rows})
+    h = (h ^ v) * 0x9e3779b97f4a7c15ull;
+  h ^= h >> 29;
+  return static_cast<uint32_t>(h % kMapCacheSlots);
+}
+
+// Looks `key` up; on a miss encodes it with `enc_fn` and stores it.
+template <typename F>
+bool cached_map(CUtensorMap* out, const MapKey& key, F&& enc_fn) {
+  const uint32_t slot = map_slot(key);
+  {
+    std::lock_guard<std::mutex> lock(g_maps.mu);
+    if (g_maps.used[slot] && g_maps.key[slot] == key) {
+      *out = g_maps.map[slot];
+      return true;
+    }
+  }
+  if (!enc_fn(out)) return false;
+  std::lock_guard<std::mutex> lock(g_maps.mu);
+  g_maps.used[slot] = true;
+  g_maps.key[slot] = key;
+  g_maps.map[slot] = *out;
+  return true;
+}
+
 // [B*H, N, D] view of a [B,H,N,D] tensor; `rows` rows x 64 elements per box,
 // 128-byte swizzle; rows past N, and columns past D (D = 32, or the second
 // panel at D = 96), read as zeros.
 bool make_rows_map(CUtensorMap* map, const void* ptr, int bh, int n, int d, int dtype, unsigned rows) {
-  EncodeTiledFn enc = encode_fn();
-  if (!enc) return false;
-  cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)n, (cuuint64_t)bh};
-  cuuint64_t strides[2] = {(cuuint64_t)d * 2, (cuuint64_t)n * d * 2};
-  cuuint32_t box[3] = {64, rows, 1};
-  cuuint32_t estride[3] = {1, 1, 1};
-  CUresult r = enc(map, dtype == FA2_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3,
-                   const_cast<void*>(ptr), dims, strides, box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                   CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS;
+  return cached_map(map, MapKey{ptr, bh, n, d, dtype, rows}, [&](CUtensorMap* m) {
+    EncodeTiledFn enc = encode_fn();
+    if (!enc) return false;
+    cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)n, (cuuint64_t)bh};
+    cuuint64_t strides[2] = {(cuuint64_t)d * 2, (cuuint64_t)n * d * 2};
+    cuuint32_t box[3] = {64, rows, 1};
+    cuuint32_t estride[3] = {1, 1, 1};
+    CUresult r = enc(m, dtype == FA2_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3,
+                     const_cast<void*>(ptr), dims, strides, box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                     CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+  });
 }
 
 bool make_map(CUtensorMap* map, const void* ptr, int bh, int n, int d, int dtype) {
@@ -149,8 +221,16 @@ unsigned long long next_epoch() {
   return salt | ((g_epoch.fetch_add(1, std::memory_order_relaxed) + 1) & 0xffffffffull);
 }
 
+// `schedule`: FA2_SCHED_UNITS (the workspace is ignored), FA2_SCHED_BALANCED
+// (needs the workspace) or FA2_SCHED_AUTO (the cost model's choice, the
+// rounds when there is no workspace).
 int launch(const void* Q, const void* K, const void* V, void* O, float* LSE, int B, int H, int N, int D,
-           float scale, int is_causal, int dtype, void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+           float scale, int is_causal, int dtype, void* workspace, size_t workspace_bytes, int schedule,
+           cudaStream_t stream) {
+  if (schedule == FA2_SCHED_UNITS) {
+    workspace = nullptr;
+    workspace_bytes = 0;
+  }
   if (B < 0 || H < 0 || N < 0) return FA2_ERR_INVALID_ARG;
   if (!fwd_head_dim_ok(D)) return FA2_ERR_UNSUPPORTED;
   if (dtype != FA2_F16 && dtype != FA2_BF16) return FA2_ERR_UNSUPPORTED;
@@ -176,14 +256,13 @@ int launch(const void* Q, const void* K, const void* V, void* O, float* LSE, int
                     overlaps(workspace, workspace_bytes, LSE, lbytes)))
     return FA2_ERR_INVALID_ARG;
 
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return record_cuda(e);
-  DeviceInfo* info = device_info(dev);
-  if (!info) return FA2_ERR_UNSUPPORTED;
-  if (info->err != cudaSuccess) return record_cuda(info->err);
-  if (info->cc_major != 10 || info->cc_minor != 3) return FA2_ERR_UNSUPPORTED;
+  DeviceInfo* info = nullptr;
+  const int rc = current_device(&info);
+  if (rc != FA2_OK) return rc;
   if (workspace && workspace_bytes < stream_k_workspace_bytes(info->sms, D)) return FA2_ERR_INVALID_ARG;
+  if (schedule == FA2_SCHED_AUTO && workspace &&
+      fwd_auto_schedule(B, H, N, D, is_causal, info->sms) != FA2_SCHED_BALANCED)
+    workspace = nullptr;  // the rounds win: run them, the workspace unused
 
   CUtensorMap mq, mk, mv, mo;
   // V boxes: 128 rows, or at head dim 256 64 rows (the kernel streams V in
@@ -231,7 +310,7 @@ int launch(const void* Q, const void* K, const void* V, void* O, float* LSE, int
     p.stream_k = 0;
     grid = p.num_units < info->sms ? p.num_units : info->sms;
   }
-  e = pick(D, dtype, is_causal)(mq, mk, mv, mo, p, grid, stream);
+  const cudaError_t e = pick(D, dtype, is_causal)(mq, mk, mv, mo, p, grid, stream);
   if (e != cudaSuccess) return record_cuda(e);
   return FA2_OK;
 }
@@ -246,13 +325,9 @@ unsigned long long next_launch_epoch() { return next_epoch(); }
 int take_test_withhold() { return g_test_withhold.exchange(0, std::memory_order_relaxed); }
 
 int current_device_facts(int* sms, int** status) {
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return record_cuda(e);
-  DeviceInfo* info = device_info(dev);
-  if (!info) return FA2_ERR_UNSUPPORTED;
-  if (info->err != cudaSuccess) return record_cuda(info->err);
-  if (info->cc_major != 10 || info->cc_minor != 3) return FA2_ERR_UNSUPPORTED;
+  DeviceInfo* info = nullptr;
+  const int rc = current_device(&info);
+  if (rc != FA2_OK) return rc;
   *sms = info->sms;
   *status = info->status;
   return FA2_OK;
@@ -263,16 +338,18 @@ bool encode_tile_map(CUtensorMap* map, const void* ptr, int bh, int n, int d, in
 }
 
 bool encode_f32_rows_map(CUtensorMap* map, float* ptr, int bh, int n, int d, unsigned rows) {
-  EncodeTiledFn enc = encode_fn();
-  if (!enc) return false;
-  cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)n, (cuuint64_t)bh};
-  cuuint64_t strides[2] = {(cuuint64_t)d * 4, (cuuint64_t)n * d * 4};
-  cuuint32_t box[3] = {(cuuint32_t)d, rows, 1};
-  cuuint32_t estride[3] = {1, 1, 1};
-  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, ptr, dims, strides, box, estride,
-                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS;
+  return cached_map(map, MapKey{ptr, bh, n, d, 16, rows}, [&](CUtensorMap* m) {
+    EncodeTiledFn enc = encode_fn();
+    if (!enc) return false;
+    cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)n, (cuuint64_t)bh};
+    cuuint64_t strides[2] = {(cuuint64_t)d * 4, (cuuint64_t)n * d * 4};
+    cuuint32_t box[3] = {(cuuint32_t)d, rows, 1};
+    cuuint32_t estride[3] = {1, 1, 1};
+    CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, ptr, dims, strides, box, estride,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+  });
 }
 
 unsigned long long watchdog_limit_ns() { return g_watchdog_ns.load(std::memory_order_relaxed); }
@@ -280,15 +357,50 @@ unsigned long long watchdog_limit_ns() { return g_watchdog_ns.load(std::memory_o
 bool ranges_overlap(const void* a, size_t na, const void* b, size_t nb) { return overlaps(a, na, b, nb); }
 
 int launch_forward(const void* Q, const void* K, const void* V, void* O, float* LSE, int B, int H, int N, int D,
-                   float scale, int is_causal, int dtype, void* workspace, size_t workspace_bytes,
+                   float scale, int is_causal, int dtype, void* workspace, size_t workspace_bytes, bool balanced,
                    cudaStream_t stream) {
-  return ::launch(Q, K, V, O, LSE, B, H, N, D, scale, is_causal, dtype, workspace, workspace_bytes, stream);
+  return ::launch(Q, K, V, O, LSE, B, H, N, D, scale, is_causal, dtype, workspace, workspace_bytes,
+                  balanced ? FA2_SCHED_BALANCED : FA2_SCHED_UNITS, stream);
+}
+
+// Cost of each schedule in K/V-tile steps of the busiest SM (a step: one
+// work unit against one 128-key tile). Rounds: ceil(units / SMs) rounds of
+// whole units. Balanced: total steps / SMs plus kSplitCostSteps for the
+// partial-result write and merge of the units it cuts. Balanced is taken
+// when at least 5 % cheaper, for non-causal work only: the heaviest-first
+// zig-zag rounds measured faster than the split on every causal workload.
+int fwd_auto_schedule(long long B, long long H, long long N, int D, int is_causal, int sms) {
+  constexpr double kSplitCostSteps = 4.0;
+  const long long rows = fwd_unit_rows(D);
+  const long long units = B * H * ((N + rows - 1) / rows);
+  if (is_causal || units <= 0 || sms <= 0) return FA2_SCHED_UNITS;
+  const long long nkv = (N + kKeys - 1) / kKeys;
+  const double rounds_cost = static_cast<double>((units + sms - 1) / sms) * static_cast<double>(nkv);
+  const double balanced_cost = static_cast<double>(units) * static_cast<double>(nkv) / sms + kSplitCostSteps;
+  return balanced_cost < 0.95 * rounds_cost ? FA2_SCHED_BALANCED : FA2_SCHED_UNITS;
 }
 }  // namespace fa2
 
 extern "C" int fa2_fwd(const void* Q, const void* K, const void* V, void* O, float* LSE, int B, int H, int N,
                        int D, float scale, int is_causal, int dtype, struct CUstream_st* stream) {
-  return launch(Q, K, V, O, LSE, B, H, N, D, scale, is_causal, dtype, nullptr, 0,
+  return launch(Q, K, V, O, LSE, B, H, N, D, scale, is_causal, dtype, nullptr, 0, FA2_SCHED_UNITS,
+                reinterpret_cast<cudaStream_t>(stream));
+}
+
+extern "C" int fa2_fwd_schedule_for(int B, int H, int N, int D, int is_causal, int sms, int* schedule) {
+  if (!schedule || B < 0 || H < 0 || N < 0 || sms < 1) return FA2_ERR_INVALID_ARG;
+  if (!fwd_head_dim_ok(D)) return FA2_ERR_UNSUPPORTED;
+  *schedule = fwd_auto_schedule(B, H, N, D, is_causal, sms);
+  return FA2_OK;
+}
+
+extern "C" int fa2_fwd_sched(const void* Q, const void* K, const void* V, void* O, float* LSE, int B, int H, int N,
+                             int D, float scale, int is_causal, int dtype, void* workspace, size_t workspace_bytes,
+                             int schedule, struct CUstream_st* stream) {
+  if (schedule != FA2_SCHED_AUTO && schedule != FA2_SCHED_UNITS && schedule != FA2_SCHED_BALANCED)
+    return FA2_ERR_INVALID_ARG;
+  if (schedule == FA2_SCHED_BALANCED && !workspace && B > 0 && H > 0 && N > 0) return FA2_ERR_INVALID_ARG;
+  return launch(Q, K, V, O, LSE, B, H, N, D, scale, is_causal, dtype, workspace, workspace_bytes, schedule,
                 reinterpret_cast<cudaStream_t>(stream));
 }
 
@@ -309,20 +421,17 @@ extern "C" int fa2_fwd_ws(const void* Q, const void* K, const void* V, void* O, 
                           int D, float scale, int is_causal, int dtype, void* workspace, size_t workspace_bytes,
                           struct CUstream_st* stream) {
   return launch(Q, K, V, O, LSE, B, H, N, D, scale, is_causal, dtype, workspace, workspace_bytes,
-                reinterpret_cast<cudaStream_t>(stream));
+                workspace ? FA2_SCHED_BALANCED : FA2_SCHED_UNITS, reinterpret_cast<cudaStream_t>(stream));
 }
 
 extern "C" int fa2_device_status(struct CUstream_st* stream, int* status, int clear) {
   if (!status) return FA2_ERR_INVALID_ARG;
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return record_cuda(e);
-  DeviceInfo* info = device_info(dev);
-  if (!info) return FA2_ERR_UNSUPPORTED;
-  if (info->err != cudaSuccess) return record_cuda(info->err);
+  DeviceInfo* info = nullptr;
+  const int rc = current_device(&info);
+  if (rc != FA2_OK) return rc;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   int v = 0;
-  e = cudaMemcpyAsync(&v, info->status, sizeof(int), cudaMemcpyDeviceToHost, s);
+  cudaError_t e = cudaMemcpyAsync(&v, info->status, sizeof(int), cudaMemcpyDeviceToHost, s);
   if (e == cudaSuccess) e = cudaStreamSynchronize(s);
   if (e == cudaSuccess && clear) {
     e = cudaMemsetAsync(info->status, 0, sizeof(int), s);
@@ -330,7 +439,7 @@ extern "C" int fa2_device_status(struct CUstream_st* stream, int* status, int cl
   }
   if (e != cudaSuccess) return record_cuda(e);
   *status = v;
-  return FA2_OK;
+  return v != 0 ? FA2_ERR_TIMEOUT : FA2_OK;
 }
 
 extern "C" int fa2_set_watchdog_ns(unsigned long long ns) {
@@ -357,4 +466,4 @@ extern "C" const char* fa2_error_string(int code) {
 
 extern "C" const char* fa2_last_cuda_error(void) { return t_last_cuda_error; }
 
-extern "C" int fa2_version(void) { return (1 << 16) | 0; }
+extern "C" int fa2_version(void) { return (1 << 16) | 1; }

@@ -937,7 +937,10 @@ cudaError_t launch_bwd(const CUtensorMap& k, const CUtensorMap& v, const CUtenso
                        const CUtensorMap& dq_acc, const BwdParams& p, int grid, cudaStream_t stream) {
   auto kern = fa2_bwd_kernel<D, kBf16, kCausal>;
   const int smem = BwdLayout<D>::kSmemBytes;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  // Once per device: the shared-memory opt-in.
+  static PerDeviceOnce prepared;
+  const cudaError_t e = once_per_device(
+      prepared, [&]() { return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem); });
   if (e != cudaSuccess) return e;
   // The stream-K schedule waits across CTAs, so it is launched cooperatively
   // (the whole grid resident at once, or the launch fails).

@@ -21,7 +21,7 @@
 
 namespace {
 
-constexpr int kMaxDevices = 64;
+using fa2::kMaxDevices;
 
 // Two non-blocking copy streams and four events per device, created on first
 // use and kept for the life of the process. A stream wait binds to the event's
@@ -170,7 +170,7 @@ extern "C" int fa2_fwd_host(const void* Q, const void* K, const void* V, void* O
       break;
     }
     rc = fa2::launch_forward(dq + off, dk + off, dv + off, dout + off, dl, 1, nh, N, D, scale, is_causal, dtype, ws,
-                             ws ? L.ws_bytes : 0, s);
+                             ws ? L.ws_bytes : 0, ws != nullptr, s);
     if (rc != FA2_OK) break;
     e = cudaEventRecord(pp.computed, s);
     if (e == cudaSuccess) e = cudaStreamWaitEvent(pp.out, pp.computed, 0);

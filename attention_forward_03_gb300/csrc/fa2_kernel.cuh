@@ -719,13 +719,17 @@ cudaError_t launch_fwd(const CUtensorMap& q, const CUtensorMap& k, const CUtenso
                        const Params& p, int grid, cudaStream_t stream) {
   auto kern = fa2_fwd_kernel<D, kBf16, kCausal>;
   const int smem = Layout<D>::kSmemBytes;
-  cudaFuncAttributes fa;
-  cudaError_t e = cudaFuncGetAttributes(&fa, kern);
-  if (e != cudaSuccess) return e;
-  // The in-kernel register split assumes exactly kLaunchRegs per thread at
-  // launch; any other count could leave a warpgroup waiting for registers.
-  if (fa.numRegs != kLaunchRegs) return cudaErrorInvalidConfiguration;
-  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  // Once per device: the register check and the shared-memory opt-in.
+  static PerDeviceOnce prepared;
+  const cudaError_t e = once_per_device(prepared, [&]() -> cudaError_t {
+    cudaFuncAttributes fa;
+    cudaError_t r = cudaFuncGetAttributes(&fa, kern);
+    if (r != cudaSuccess) return r;
+    // The in-kernel register split assumes exactly kLaunchRegs per thread at
+    // launch; any other count could leave a warpgroup waiting for registers.
+    if (fa.numRegs != kLaunchRegs) return cudaErrorInvalidConfiguration;
+    return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  });
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);

@@ -7,7 +7,31 @@
 #include <cuda_runtime.h>
 #include <stddef.h>
 
+#include <mutex>
+
 namespace fa2 {
+
+// Devices the library keeps per-device state for (set-up done once per device).
+constexpr int kMaxDevices = 64;
+
+// One-time, per-device preparation of a kernel (its function attributes):
+// `prep` runs once for each device, with that device current, and its result
+// is returned to every later call on the device. Devices past the table run
+// `prep` on every call.
+struct PerDeviceOnce {
+  std::once_flag flag[kMaxDevices];
+  cudaError_t err[kMaxDevices] = {};
+};
+
+template <typename F>
+cudaError_t once_per_device(PerDeviceOnce& o, F&& prep) {
+  int dev = 0;
+  const cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return prep();
+  std::call_once(o.flag[dev], [&] { o.err[dev] = prep(); });
+  return o.err[dev];
+}
 
 constexpr int kRows = 128;          // query rows per sub-tile (= TMEM lanes)
 constexpr int kSubTiles = 2;        // sub-tiles per work unit
@@ -98,10 +122,16 @@ constexpr size_t stream_k_workspace_bytes(int grid, int d) {
 }
 
 // The full forward call (validation, tensor maps, launch) with an optional
-// stream-K workspace; the C entry points are thin wrappers around it.
+// stream-K workspace; the C entry points are thin wrappers around it. With
+// `balanced` false the round schedule runs whatever the workspace.
 int launch_forward(const void* Q, const void* K, const void* V, void* O, float* LSE, int B, int H, int N, int D,
-                   float scale, int is_causal, int dtype, void* workspace, size_t workspace_bytes,
+                   float scale, int is_causal, int dtype, void* workspace, size_t workspace_bytes, bool balanced,
                    cudaStream_t stream);
+
+// The forward schedule with less work on the busiest SM (FA2_SCHED_UNITS or
+// FA2_SCHED_BALANCED) for a problem on a device with `sms` SMs; see
+// fa2_fwd_schedule_for in include/fa2.h.
+int fwd_auto_schedule(long long B, long long H, long long N, int D, int is_causal, int sms);
 
 // Records `e` as the calling thread's last CUDA error (fa2_last_cuda_error)
 // and returns FA2_ERR_CUDA.
@@ -116,7 +146,9 @@ unsigned long long next_launch_epoch();
 int take_test_withhold();
 
 // Shared with the backward pass: the current device's SM count and watchdog
-// word (FA2_ERR_UNSUPPORTED unless it is a compute-capability 10.3 GPU), a
+// word (FA2_ERR_UNSUPPORTED unless it is a compute-capability 10.3 GPU; the
+// capability is checked before anything that needs this library's device
+// code on the device), a
 // 128-byte-swizzled [B*H, N, D] tensor map with boxes of `rows` rows x 64
 // elements, the watchdog limit, and an address-range overlap test.
 int current_device_facts(int* sms, int** status);

@@ -15,8 +15,8 @@ namespace {
 // head dimension 128 (smaller head dimensions need less).
 constexpr int kMaxCtas = 160;
 constexpr size_t kScratchBytes = fa2::stream_k_workspace_bytes(kMaxCtas, 128);
-constexpr int kMaxDevices = 64;
 static_assert(kScratchBytes == 21465600, "the size stated in fa2.h");
+static_assert(fa2::stream_k_workspace_bytes(kMaxCtas, 256) <= kScratchBytes, "head dim 256 fits as well");
 
 // Every GPU that loads this module holds this array until the process exits.
 // In host code `g_scratch` is only a stand-in for the symbol: its device
@@ -29,7 +29,7 @@ struct Setup {
   int sms = 0;
   void* ptr = nullptr;
 };
-Setup g_setup[kMaxDevices];
+Setup g_setup[fa2::kMaxDevices];
 
 }  // namespace
 
@@ -41,21 +41,29 @@ extern "C" int fa2_fwd_noalloc(const void* Q, const void* K, const void* V, void
   if (dtype != FA2_F16 && dtype != FA2_BF16) return FA2_ERR_UNSUPPORTED;
   if (B == 0 || H == 0 || N == 0) return FA2_OK;
 
+  // The device must be one this library runs on (compute capability 10.3)
+  // before anything below touches its device code.
+  int sms = 0;
+  int* status = nullptr;
+  const int rc = fa2::current_device_facts(&sms, &status);
+  if (rc != FA2_OK) return rc;
   int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return FA2_ERR_CUDA;
-  if (dev < 0 || dev >= kMaxDevices) return FA2_ERR_UNSUPPORTED;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return fa2::record_cuda_error(e);
+  if (dev < 0 || dev >= fa2::kMaxDevices) return FA2_ERR_UNSUPPORTED;
   Setup& s = g_setup[dev];
   // Set-up on the first call on this device (with it current): the device
-  // address of the static scratch and the SM count.
+  // address of the static scratch. With lazy module loading (the CUDA 12+
+  // default) this is also when the array's memory is committed on the device.
   std::call_once(s.once, [&] {
-    cudaError_t e = cudaDeviceGetAttribute(&s.sms, cudaDevAttrMultiProcessorCount, dev);
-    if (e == cudaSuccess) e = cudaGetSymbolAddress(&s.ptr, g_scratch);
-    s.err = e;
+    s.sms = sms;
+    s.err = cudaGetSymbolAddress(&s.ptr, g_scratch);
   });
-  if (s.err != cudaSuccess || s.ptr == nullptr) return FA2_ERR_CUDA;
+  if (s.err != cudaSuccess) return fa2::record_cuda_error(s.err);
+  if (s.ptr == nullptr) return fa2::record_cuda_error(cudaErrorInvalidSymbol);
   // The scratch holds one partial result per CTA; a device with more SMs
   // than it covers is refused rather than run with a cut-down grid.
   if (s.sms > kMaxCtas) return FA2_ERR_UNSUPPORTED;
-  return fa2::launch_forward(Q, K, V, O, LSE, B, H, N, D, scale, is_causal, dtype, s.ptr, kScratchBytes,
+  return fa2::launch_forward(Q, K, V, O, LSE, B, H, N, D, scale, is_causal, dtype, s.ptr, kScratchBytes, true,
                              reinterpret_cast<cudaStream_t>(stream));
 }

@@ -9,9 +9,15 @@ inputs, already resident in HBM. Timing uses CUDA events on the launching
 stream around exactly K steps, bracketed by a barrier and a device
 synchronise; the inputs rotate over enough copies that one pass over all of
 them is larger than twice the L2 cache, so no step finds its inputs in L2
-from the step before. Under torchrun each rank runs the same workload on its
-own GPU (weak scaling, no collective on the data path) and the slowest rank's
-time is reported.
+from the step before. Under torchrun the slowest rank's time is reported,
+and the work is spread in one of two ways (--split):
+  replicas  each rank runs the whole workload on its own GPU (weak scaling;
+            the job's work grows with the number of ranks);
+  heads     rank r of W owns a contiguous slice of the workload's B*H heads
+            (attention_forward_03_gb300.partition.head_slice) and runs the
+            forward on it alone (strong scaling: the job is one workload).
+Neither puts a collective on the data path; --gather adds an all-gather of
+the head slices' O and LSE to every step of the heads split.
 
 Metric: attention forward TFLOP/s = 4*B*H*N^2*D (halved when causal) / time.
 `--pass bwd` times the backward pass (fa2_bwd) instead: 10*B*H*N^2*D
@@ -200,6 +206,22 @@ def whole_job_tflops(flops_per_step: float, steps: int, world: int, max_seconds:
     return flops_per_step * steps * world / max_seconds / 1e12
 
 
+def split_job(w: workloads.Workload, split: str, world: int, rank: int):
+    """This rank's share of the job: (local workload, first head, job FLOPs per step, parallelism label).
+
+    replicas: the whole workload on every rank (the job does `world` of them).
+    heads: flattened heads [h0, h1) of the one workload, run as a [1, h1 - h0, N, D]
+    problem (the job does the workload once)."""
+    import dataclasses
+
+    from attention_forward_03_gb300 import partition
+    if split == "replicas":
+        return w, 0, workloads.flops(w) * world, f"weak x{world} (one independent replica per GPU)"
+    h0, h1 = partition.head_slice(w.B * w.H, world, rank)
+    local = dataclasses.replace(w, name=f"{w.name}[heads {h0}:{h1}]", B=1, H=h1 - h0)
+    return local, h0, workloads.flops(w), f"heads x{world} (rank r owns a contiguous slice of the B*H heads)"
+
+
 # ------------------------------------------------------------- CPU oracle leg
 def _row_flops(w: workloads.Workload, rows):
     import numpy as np
@@ -325,13 +347,18 @@ def run_gb300(args, w, rank, world, local):
     fa2.library()
     stream = torch.cuda.current_stream(dev)
 
-    q, k, v = workloads.make_inputs(w)
+    from attention_forward_03_gb300 import partition
+    job = w
+    w, h0, job_flops, parallelism = split_job(job, args.split, world, rank)
+    q, k, v = workloads.make_inputs(job)
+    if args.split == "heads":
+        q, k, v = (partition.local_view(t, h0, h0 + w.H).contiguous() for t in (q, k, v))
     resolved_schedule = args.schedule
     if resolved_schedule == "auto":
         resolved_schedule = fa2.binding.choose_schedule(w.B, w.H, w.N, w.causal,
                                                         torch.cuda.get_device_properties(dev).multi_processor_count,
                                                         w.D)
-    set_bytes = workloads.algorithmic_bytes(w)
+    set_bytes = max(1, workloads.algorithmic_bytes(w))
     l2 = getattr(torch.cuda.get_device_properties(dev), "L2_cache_size", 128 * 2 ** 20)
     nsets = max(2, math.ceil(2 * l2 / set_bytes))
     sets = []
@@ -340,10 +367,15 @@ def run_gb300(args, w, rank, world, local):
                      torch.empty((w.B, w.H, w.N), dtype=torch.float32, device=dev)))
     torch.cuda.synchronize(dev)
 
+    gather = args.gather and args.split == "heads" and world > 1
+
     def step(i):
         qd, kd, vd, od, ld = sets[i % nsets]
         fa2.attention_forward(qd, kd, vd, scale=w.scale, is_causal=w.causal, out=od, lse=ld, stream=stream,
                               schedule=args.schedule)
+        if gather:
+            partition.gather_heads(od, job.B * job.H, world, rank)
+            partition.gather_heads(ld, job.B * job.H, world, rank)
 
     clocks = ClockSampler(local)
     clocks.start()
@@ -379,8 +411,8 @@ def run_gb300(args, w, rank, world, local):
     if status != 0:
         raise RuntimeError(f"device watchdog fired during the timed region (code {status})")
     t_max = max_over_ranks(elapsed, world, dev)
-    flops = workloads.flops(w)
-    value = whole_job_tflops(flops, args.steps, world, t_max)
+    flops = workloads.flops(w)  # this rank's launches
+    value = job_flops * args.steps / t_max / 1e12
     per_launch = elapsed / args.steps
 
     # End to end through the C ABI's host-memory entry point (fa2_fwd_host):
@@ -414,9 +446,12 @@ def run_gb300(args, w, rank, world, local):
     ev1.record(stream)
     torch.cuda.synchronize(dev)
     e2e_elapsed = max_over_ranks(ev0.elapsed_time(ev1) / 1e3, world, dev)
-    e2e_value = whole_job_tflops(flops, e2e_steps, world, e2e_elapsed)
-    h2d = 3 * q.numel() * q.element_size()
-    d2h = oh.numel() * oh.element_size() + lh.numel() * 4
+    e2e_value = job_flops * e2e_steps / e2e_elapsed / 1e12
+    # bytes of the whole job (all ranks)
+    copies = world if args.split == "replicas" else 1
+    jq = job.B * job.H * job.N * job.D * q.element_size()
+    h2d = 3 * jq * copies
+    d2h = (jq + job.B * job.H * job.N * 4) * copies
 
     if rank != 0:
         return None
@@ -426,11 +461,12 @@ def run_gb300(args, w, rank, world, local):
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": 1e3 * t_max / args.steps, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": w.dtype,
+        "scaling": "weak" if args.split == "replicas" else "strong", "vs_baseline": None, "dtype": w.dtype,
         "data": "synthetic (seeded N(0, sigma^2) inputs, cast to the workload's 16-bit dtype)",
-        "config": {"workload": w.describe(), "B": w.B, "H": w.H, "N": w.N, "D": w.D, "causal": w.causal,
-                   "scale": "1/sqrt(D)", "schedule": resolved_schedule,
-                   "parallelism": f"weak x{world} (one independent replica per GPU)",
+        "config": {"workload": job.describe(), "B": job.B, "H": job.H, "N": job.N, "D": job.D,
+                   "causal": job.causal, "scale": "1/sqrt(D)", "schedule": resolved_schedule,
+                   "parallelism": parallelism + (", O/LSE all-gathered every step" if gather else ""),
+                   "rank0_heads": [h0, h0 + w.B * w.H] if args.split == "heads" else None,
                    "l2": f"inputs rotate over {nsets} copies ({nsets * set_bytes / 2**20:.0f} MiB > 2x L2)"},
         "pct_of_peak": 100.0 * achieved / peak,
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
@@ -441,11 +477,11 @@ def run_gb300(args, w, rank, world, local):
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "path": "fa2_fwd_host (C ABI, page-locked host buffers)", "heads_per_chunk": hpc,
                 "chunk_schedule": chunk_schedule, "steps": e2e_steps},
-        "gpu_launches": args.steps,
+        "gpu_launches": args.steps if w.B * w.H > 0 else 0,
         "clocks": clock_info,
     }
     if not args.no_cpu_baseline:
-        tf, secs, rows, threads, desc = oracle_sample(w, args.cpu_seconds)
+        tf, secs, rows, threads, desc = oracle_sample(job, args.cpu_seconds)
         line["cpu_baseline"] = {"value": tf, "unit": UNIT, "cores": threads, "cpu_model": host_cpu_model(), "kind": "oracle", "sample": desc,
                                 "seconds": secs}
     return line
@@ -579,6 +615,11 @@ def main(argv=None):
                     help="forward: auto = the binding's choice, balanced = fa2_fwd_ws (equal K/V-tile steps per "
                          "SM), units = fa2_fwd; backward (--pass bwd): the same choice passed to fa2_bwd_sched "
                          "(auto = the library's)")
+    ap.add_argument("--split", default="replicas", choices=["replicas", "heads"],
+                    help="under torchrun: replicas = every rank runs the whole workload (weak scaling); heads = "
+                         "rank r owns a contiguous slice of the B*H heads (strong scaling)")
+    ap.add_argument("--gather", action="store_true",
+                    help="with --split heads: all-gather O and LSE of every step to every rank (NCCL)")
     ap.add_argument("--settle-seconds", type=float, default=1.0)
     ap.add_argument("--e2e-heads-per-chunk", type=int, default=0,
                     help="heads per chunk of the end-to-end host-memory pipeline (0 = the binding's default)")

@@ -36,10 +36,10 @@ struct CUstream_st; /* the same type as cudaStream_t / CUstream */
 #define FA2_F16 0  /* IEEE binary16 inputs and output */
 #define FA2_BF16 1 /* bfloat16 inputs and output      */
 
-/* schedule codes of fa2_bwd_sched */
+/* schedule codes of fa2_fwd_sched and fa2_bwd_sched */
 #define FA2_SCHED_AUTO 0     /* the one with less work on the busiest SM (what fa2_bwd uses) */
-#define FA2_SCHED_UNITS 1    /* whole K/V tiles dealt to the SMs in rounds */
-#define FA2_SCHED_BALANCED 2 /* equal query steps per SM; tiles cut between SMs are merged */
+#define FA2_SCHED_UNITS 1    /* whole work units dealt to the SMs in rounds */
+#define FA2_SCHED_BALANCED 2 /* equal steps per SM; units cut between SMs are merged */
 
 /* status codes (0 = success, negative = error) */
 #define FA2_OK 0
@@ -47,7 +47,7 @@ struct CUstream_st; /* the same type as cudaStream_t / CUstream */
 #define FA2_ERR_UNSUPPORTED (-2) /* head dim not supported, unknown dtype, device is not sm_103 */
 #define FA2_ERR_ALIGN (-3)       /* a tensor pointer is not 16-byte aligned */
 #define FA2_ERR_CUDA (-4)        /* a CUDA runtime/driver call failed (see fa2_last_cuda_error) */
-#define FA2_ERR_TIMEOUT (-5)     /* the device watchdog fired (reported by fa2_device_status) */
+#define FA2_ERR_TIMEOUT (-5)     /* the device watchdog fired (returned by fa2_device_status) */
 
 /*
  * fa2_fwd — enqueue the forward pass on `stream`.
@@ -120,6 +120,45 @@ int fa2_fwd_ws(const void* Q, const void* K, const void* V, void* O, float* LSE,
                void* workspace, size_t workspace_bytes, struct CUstream_st* stream);
 
 /*
+ * fa2_fwd_sched — the same operation, arguments and results as fa2_fwd, with
+ * the work schedule chosen by the caller or by the library:
+ *   FA2_SCHED_UNITS: the round schedule of fa2_fwd (whole 256-row query
+ *     units, 128-row at head dim 256, dealt to persistent CTAs in rounds;
+ *     heaviest first in a zig-zag when causal). `workspace` may be NULL.
+ *   FA2_SCHED_BALANCED: the stream-K schedule of fa2_fwd_ws; `workspace`
+ *     (as described there) is required.
+ *   FA2_SCHED_AUTO: the schedule fa2_fwd_schedule_for names for this
+ *     problem on the current device; with a NULL workspace always the round
+ *     schedule.
+ * Both schedules compute the same function; they differ in the order of the
+ * fp32 sums (outputs within rounding of each other) and each is
+ * deterministic. This is the call for a C caller who wants the faster
+ * schedule without choosing it: on a 152-SM GB300, B=1 H=8 N=8192 D=128
+ * non-causal runs balanced (its 256 units leave 48 SMs idle in the second
+ * round), B=4 H=16 N=4096 D=128 causal runs in rounds.
+ * Errors as fa2_fwd_ws, plus FA2_ERR_INVALID_ARG for an unknown schedule code
+ * or FA2_SCHED_BALANCED without a workspace.
+ */
+int fa2_fwd_sched(const void* Q, const void* K, const void* V, void* O, float* LSE,
+                  int B, int H, int N, int D, float scale, int is_causal, int dtype,
+                  void* workspace, size_t workspace_bytes, int schedule, struct CUstream_st* stream);
+
+/*
+ * fa2_fwd_schedule_for — the schedule FA2_SCHED_AUTO takes for a problem on a
+ * device with `sms` SMs (FA2_SCHED_UNITS or FA2_SCHED_BALANCED into
+ * *schedule). The cost of each is the busiest SM's work in K/V-tile steps
+ * (one query unit against one 128-key tile): the rounds take
+ * ceil(units / sms) * tiles per unit; the balanced schedule takes
+ * units * tiles per unit / sms, plus 4 steps for the write and merge of the
+ * partial results of the units it cuts. Balanced is named when it is at
+ * least 5 % cheaper, and never for causal work (the zig-zag rounds measured
+ * faster there). Host arithmetic only: needs no device.
+ * Returns FA2_OK, FA2_ERR_INVALID_ARG (NULL output, negative size, sms < 1)
+ * or FA2_ERR_UNSUPPORTED (D).
+ */
+int fa2_fwd_schedule_for(int B, int H, int N, int D, int is_causal, int sms, int* schedule);
+
+/*
  * fa2_fwd_noalloc — the same operation, arguments and results as fa2_fwd,
  * with the balanced (stream-K) schedule of fa2_fwd_ws, for callers that
  * cannot allocate device memory: code that must not call cudaMalloc, for
@@ -130,11 +169,15 @@ int fa2_fwd_ws(const void* Q, const void* K, const void* V, void* O, float* LSE,
  * have no counterpart to this entry point.
  *
  * Its scratch is one static device array of this library, 21,465,600 bytes,
- * held on every GPU that loads the library until the process exits. It
+ * held on every GPU where it has been loaded until the process exits. It
  * covers devices of up to 160 SMs at every supported head dimension; a device with
  * more SMs is refused with FA2_ERR_UNSUPPORTED.
  * The first call on each device looks up the array's device address (with
  * that device current); make that first call before any stream capture.
+ * Under lazy module loading (the default since CUDA 12) that first call is
+ * also when the 21 MB are committed on the device, so it can fail with
+ * FA2_ERR_CUDA (out of memory) if the caller's pool already holds nearly all
+ * of it: make one warm-up call at start-up, before sizing such a pool.
  * All calls share the array and it keeps the last call's contents. Nothing
  * in it has to start at zero: each launch tags its partial results with a
  * unique value, so leftovers of earlier calls are never read. Calls that
@@ -281,8 +324,10 @@ int fa2_bwd_sched(const void* Q, const void* K, const void* V, const void* O, co
  * device, synchronising `stream` first. *status receives 0 when no kernel of
  * this library has timed out waiting on one of its internal barriers since
  * the last clear, else a positive code identifying the wait that gave up.
- * If `clear` is nonzero the word is reset to 0 afterwards. Returns FA2_OK,
- * FA2_ERR_INVALID_ARG (status NULL) or FA2_ERR_CUDA.
+ * If `clear` is nonzero the word is reset to 0 afterwards. Returns FA2_OK
+ * (no timeout), FA2_ERR_TIMEOUT (a timeout was recorded; *status holds its
+ * site), FA2_ERR_INVALID_ARG (status NULL), FA2_ERR_UNSUPPORTED (not an
+ * sm_103 device) or FA2_ERR_CUDA.
  */
 int fa2_device_status(struct CUstream_st* stream, int* status, int clear);
 

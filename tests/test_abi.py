@@ -199,7 +199,8 @@ def test_product_never_imports_the_oracle():
                 assert "fa2_oracle" not in text, f
 
 
-def test_schedule_choice():
+def test_schedule_choice(lib):
+    # the binding names the choice the C cost model (fa2_fwd_schedule_for) makes
     from attention_forward_03_gb300.binding import choose_schedule
     assert choose_schedule(1, 8, 8192, False, 152) == "balanced"   # 256 units: 2 rounds of 64 vs 112 steps
     assert choose_schedule(4, 16, 8192, False, 152) == "units"     # 2048 units: 14 rounds of 64 vs 866 steps
@@ -212,6 +213,52 @@ def test_schedule_choice():
     # head dim 256: 128-row units (one sub-tile)
     assert choose_schedule(1, 8, 8192, False, 152, 256) == "balanced"  # 512 units: 4 rounds of 64 vs 220 steps
     assert choose_schedule(1, 19, 1024, False, 152, 256) == "units"    # exactly one full round
+
+
+def test_schedule_for_arguments(lib):
+    so = lib.library()
+    out = ctypes.c_int(-7)
+    assert so.fa2_fwd_schedule_for(1, 8, 8192, 128, 0, 152, None) == lib.FA2_ERR_INVALID_ARG
+    for bad in (dict(B=-1), dict(H=-1), dict(N=-1), dict(sms=0)):
+        a = dict(B=1, H=8, N=8192, sms=152, **{})
+        a.update(bad)
+        assert so.fa2_fwd_schedule_for(a["B"], a["H"], a["N"], 128, 0, a["sms"], ctypes.byref(out)) == -1
+    assert so.fa2_fwd_schedule_for(1, 8, 8192, 48, 0, 152, ctypes.byref(out)) == lib.FA2_ERR_UNSUPPORTED
+    assert out.value == -7  # untouched on error
+    assert so.fa2_fwd_schedule_for(1, 8, 8192, 128, 0, 152, ctypes.byref(out)) == lib.FA2_OK
+    assert out.value == lib.FA2_SCHED_BALANCED
+    # the cost model at the SM-count boundary: 152 units of 8 tiles fill one round exactly
+    assert lib.fa2_fwd_schedule_for(1, 38, 1024, 128, False, 152) == lib.FA2_SCHED_UNITS
+    assert lib.fa2_fwd_schedule_for(1, 39, 1024, 128, False, 152) == lib.FA2_SCHED_BALANCED
+
+
+def call_sched(lib, schedule, ws=None, nws=0, **over):
+    a = dict(GOOD)
+    a.update(over)
+    return lib.library().fa2_fwd_sched(a["Q"], a["K"], a["V"], a["O"], a["LSE"], a["B"], a["H"], a["N"], a["D"],
+                                       a["scale"], a["is_causal"], a["dtype"], ws, nws, schedule, a["stream"])
+
+
+def test_forward_schedule_codes(lib):
+    for bad in (-1, 3, 9):
+        assert call_sched(lib, bad) == lib.FA2_ERR_INVALID_ARG
+    # the balanced schedule needs a workspace (the rounds and auto do not)
+    assert call_sched(lib, lib.FA2_SCHED_BALANCED) == lib.FA2_ERR_INVALID_ARG
+    assert call_sched(lib, lib.FA2_SCHED_BALANCED, B=0) == lib.FA2_OK
+    # the usual argument checks come before any device work
+    assert call_sched(lib, lib.FA2_SCHED_AUTO, D=48) == lib.FA2_ERR_UNSUPPORTED
+    assert call_sched(lib, lib.FA2_SCHED_UNITS, Q=A + 8) == lib.FA2_ERR_ALIGN
+    assert call_sched(lib, lib.FA2_SCHED_AUTO, A * 80, 1 << 24, scale=0.0) == lib.FA2_ERR_INVALID_ARG
+
+
+@pytest.mark.skipif(torch.cuda.is_available(), reason="only meaningful on a host without a GPU")
+def test_schedule_calls_and_status_without_a_gpu_fail_loudly(lib):
+    for sched in (lib.FA2_SCHED_AUTO, lib.FA2_SCHED_UNITS):
+        assert call_sched(lib, sched) == lib.FA2_ERR_CUDA
+    assert call_sched(lib, lib.FA2_SCHED_AUTO, A * 80, 1 << 24) == lib.FA2_ERR_CUDA
+    assert call_sched(lib, lib.FA2_SCHED_BALANCED, A * 80, 1 << 24) == lib.FA2_ERR_CUDA
+    v = ctypes.c_int(0)
+    assert lib.library().fa2_device_status(None, ctypes.byref(v), 0) == lib.FA2_ERR_CUDA
 
 
 BWD = dict(Q=A, K=A * 16, V=A * 32, O=A * 48, dO=A * 64, LSE=A * 80, dQ=A * 96, dK=A * 112, dV=A * 128, B=1, H=2,

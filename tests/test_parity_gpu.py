@@ -230,3 +230,134 @@ def test_empty_problem(fa2):
     O, L = fa2.attention_forward(q, q, q)
     torch.cuda.synchronize()
     assert O.shape == (1, 2, 0, 64) and L.shape == (1, 2, 0)
+
+
+# ------------------------------------------------------- online-softmax corners
+# Inputs drawn to reach the branches i.i.d. N(0, 1) scores never reach:
+#   rising         the row maximum grows by ~17 (log2 units) per K/V tile, so
+#                  the exponent base moves and O is rescaled in TMEM on almost
+#                  every tile after a row's first (the correction step), and
+#                  partial results cut between CTAs carry very different bases;
+#   negative       every score is below -100 (natural log): a running max that
+#                  started at 0 instead of -inf would underflow every weight
+#                  (the CUDA book's -inf guard note, section 15.3);
+#   dominant_last  one key in the last, ragged K/V tile outweighs the rest by
+#                  ~20 nats: the base moves on the tile that is also masked
+#                  past N (and on the causal diagonal).
+LOG2E = 1.0 / np.log(2.0)
+RESCALE_LOG2 = 8.0  # the kernel moves a row's exponent base when its max passes the base by more than this
+
+
+def _scores(q, k, scale, causal):
+    """fp64 scores [B*H, N, N] with disallowed keys at -inf (test-side, from the exact 16-bit inputs)."""
+    qd = q.double().reshape(-1, q.shape[2], q.shape[3])
+    kd = k.double().reshape(-1, k.shape[2], k.shape[3])
+    s = torch.matmul(qd, kd.transpose(1, 2)) * scale
+    if causal:
+        n = s.shape[1]
+        s = s.masked_fill(torch.ones(n, n, dtype=torch.bool).triu(1), float("-inf"))
+    return s.numpy()
+
+
+def base_moves_after_first_tile(q, k, scale, causal, tile=128):
+    """Per row: how many K/V tiles after its first allowed one move the exponent base, with the rule the
+    kernel applies (running max in log2 units more than RESCALE_LOG2 above the base) and whole rows
+    walked tile by tile (the round schedule)."""
+    s = _scores(q, k, scale, causal) * LOG2E
+    n = s.shape[2]
+    run = np.full(s.shape[:2], -np.inf)
+    base = np.full(s.shape[:2], -np.inf)
+    moves = np.zeros(s.shape[:2], dtype=np.int64)
+    for j0 in range(0, n, tile):
+        run = np.maximum(run, s[:, :, j0:j0 + tile].max(axis=2))
+        move = np.isfinite(run) & (~np.isfinite(base) | (run - base > RESCALE_LOG2))
+        moves += (move & np.isfinite(base)).astype(np.int64)
+        base = np.where(move, run, base)
+    return moves
+
+
+CORNER_D = [32, 64, 96, 128, 256]
+
+
+@pytest.mark.parametrize("schedule", SCHEDULES)
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("dtype", ["f16", "bf16"])
+@pytest.mark.parametrize("D", CORNER_D)
+@pytest.mark.parametrize("kind", workloads.STRUCTURED_KINDS)
+def test_online_softmax_corners_every_element(fa2, oracle_mod, kind, D, dtype, causal, schedule):
+    # B1 H2 N1000: on the balanced schedule the 32-64 K/V-tile steps of the
+    # problem spread over as many CTAs, so every unit is cut and merged from
+    # partials; on the round schedule each CTA walks whole rows of 8 tiles.
+    w = workloads.custom(1, 2, 1000, D, dtype, causal, seed=D * 5 + len(kind))
+    q, k, v = workloads.make_structured_inputs(w, kind)
+    # the inputs reach the branch they are drawn for
+    if kind == "rising":
+        moves = base_moves_after_first_tile(q, k, w.scale, causal)
+        assert (moves > 0).mean() > 0.8, "rising scores must move the exponent base after the first tile"
+    elif kind == "negative":
+        s = _scores(q, k, w.scale, causal)
+        assert np.nanmax(np.where(np.isfinite(s), s, np.nan)) < -88.0, "every score must underflow exp()"
+    else:
+        js = workloads.dominant_key(w.N)
+        moves = base_moves_after_first_tile(q, k, w.scale, causal)
+        assert (moves[:, js:] > 0).mean() > 0.9, "the dominant key must move the base on the last tile"
+    O, L = run_gpu(fa2, q, k, v, w, schedule=schedule)
+    assert torch.isfinite(O).all().item() and torch.isfinite(L).all().item()
+    Oref, Lref = oracle_mod.attention_fwd(q, k, v, w.scale, w.causal)
+    err_o = float(np.abs(O.float().cpu().numpy() - Oref).max())
+    err_l = float(np.abs(L.cpu().numpy() - Lref).max())
+    assert err_o <= TOL_O[dtype], f"{kind} {w.describe()} {schedule}: max|dO| = {err_o:.3e}"
+    assert err_l <= TOL_LSE, f"{kind} {w.describe()} {schedule}: max|dLSE| = {err_l:.3e}"
+
+
+@pytest.mark.parametrize("schedule", SCHEDULES)
+@pytest.mark.parametrize("shape", [(1, 2, 2049, 128, "bf16", False), (2, 3, 1537, 64, "f16", True),
+                                   (1, 2, 2000, 256, "bf16", True), (3, 40, 700, 128, "f16", False)])
+def test_rising_scores_longer_rows_and_many_units(fa2, oracle_mod, shape, schedule):
+    # Longer rows (16-17 tiles whose base moves on each), and more units than
+    # SMs (each CTA's later units start from a base left by an earlier one).
+    B, H, N, D, dtype, causal = shape
+    w = workloads.custom(B, H, N, D, dtype, causal, seed=N + D + 3)
+    q, k, v = workloads.make_structured_inputs(w, "rising")
+    O, L = run_gpu(fa2, q, k, v, w, schedule=schedule)
+    rows = oracle_mod.sample_rows(B, H, N, 500, seed=w.seed) if B * H > 8 else None
+    Oref, Lref = oracle_mod.attention_fwd(q, k, v, w.scale, w.causal, rows=rows)
+    Og = O.float().cpu().numpy()
+    Lg = L.cpu().numpy()
+    if rows is not None:
+        Og = Og.reshape(-1, D)[rows]
+        Lg = Lg.reshape(-1)[rows]
+    assert float(np.abs(Og - Oref).max()) <= TOL_O[dtype]
+    assert float(np.abs(Lg - Lref).max()) <= TOL_LSE
+
+
+@pytest.mark.parametrize("shape", [(1, 2, 4096, 128, False), (1, 38, 1024, 128, False), (1, 39, 1024, 128, False),
+                                   (2, 3, 1000, 64, True), (1, 4, 2048, 256, False)])
+def test_auto_schedule_in_c_runs_the_named_schedule(fa2, shape):
+    # fa2_fwd_sched(FA2_SCHED_AUTO) takes the schedule fa2_fwd_schedule_for
+    # names: its output is bit-identical to that schedule's own entry point
+    # (fa2_fwd_ws for balanced, fa2_fwd for the rounds).
+    B, H, N, D, causal = shape
+    w = workloads.custom(B, H, N, D, "bf16", causal, seed=B * H + N)
+    q, k, v = (t.cuda() for t in workloads.make_inputs(w))
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    named = fa2.fa2_fwd_schedule_for(B, H, N, D, causal, sms)
+    ws = torch.empty(fa2.fa2_fwd_workspace_bytes(D), dtype=torch.uint8, device="cuda")
+    outs = []
+    for entry in ("auto", "named"):
+        o = torch.full_like(q, float("nan"))
+        lse = torch.full((B, H, N), float("nan"), dtype=torch.float32, device="cuda")
+        ptrs = (q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(), B, H, N, D, w.scale,
+                int(causal), fa2.FA2_BF16)
+        s = torch.cuda.current_stream().cuda_stream
+        if entry == "auto":
+            rc = fa2.fa2_fwd_sched(*ptrs, ws.data_ptr(), ws.numel(), fa2.FA2_SCHED_AUTO, s)
+        elif named == fa2.FA2_SCHED_BALANCED:
+            rc = fa2.fa2_fwd_ws(*ptrs, ws.data_ptr(), ws.numel(), s)
+        else:
+            rc = fa2.fa2_fwd(*ptrs, s)
+        assert rc == fa2.FA2_OK, fa2.error_text(rc)
+        torch.cuda.synchronize()
+        outs.append((o, lse))
+    assert fa2.fa2_device_status(clear=True) == 0
+    assert torch.equal(outs[0][0], outs[1][0]) and torch.equal(outs[0][1], outs[1][1])

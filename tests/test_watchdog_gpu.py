@@ -7,6 +7,8 @@ launch right after must still match the oracle.
 """
 from __future__ import annotations
 
+import ctypes
+
 import numpy as np
 import pytest
 import torch
@@ -36,9 +38,14 @@ def test_withheld_tile_times_out_and_the_context_stays_usable(fa2, oracle_mod, D
         assert lib.fa2_test_withhold_next_load(1) == fa2.FA2_OK
         fa2.attention_forward(q, k, v, scale=w.scale, schedule="units")
         torch.cuda.synchronize()  # returns: every wait in the kernel is bounded
+        # the C call reports the timeout as FA2_ERR_TIMEOUT, with the wait site in the word
+        site = ctypes.c_int(0)
+        assert lib.fa2_device_status(None, ctypes.byref(site), 0) == fa2.FA2_ERR_TIMEOUT
+        assert site.value > 0
         status = fa2.fa2_device_status(clear=True)
-        assert status != 0, "the withheld tile should have made a wait run out"
+        assert status == site.value, "the withheld tile should have made a wait run out"
         assert fa2.fa2_device_status() == 0  # cleared
+        assert lib.fa2_device_status(None, ctypes.byref(site), 0) == fa2.FA2_OK and site.value == 0
     finally:
         lib.fa2_test_withhold_next_load(0)
         fa2.fa2_set_watchdog_ns(0)

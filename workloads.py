@@ -139,3 +139,68 @@ def bwd_algorithmic_bytes(w: Workload) -> int:
     LSE (fp32) once, write dQ, dK, dV (16-bit)."""
     elems = w.B * w.H * w.N * w.D
     return 8 * elems * 2 + w.B * w.H * w.N * 4
+
+
+# ------------------------------------------------------------ structured inputs
+# Inputs shaped to reach the corners of the online softmax: the exponent base
+# moving on many K/V tiles, every score far below zero, and one dominant key
+# in a ragged last tile. They change only how Q, K, V are drawn (directions,
+# magnitudes, signs); the attention arithmetic is elsewhere.
+STRUCTURED_KINDS = ("rising", "negative", "dominant_last")
+
+RISE_NATS_PER_TILE = 12.0   # "rising": growth of the scores per 128 keys (natural-log units)
+NEGATIVE_NATS = 180.0       # "negative": typical magnitude of the (all negative) scores
+DOMINANT_NATS = 25.0        # "dominant_last": the dominant key's score above the rest
+
+
+def dominant_key(N: int) -> int:
+    """The dominant key of the "dominant_last" inputs: four keys into the last
+    128-key tile (the last key if that tile is shorter), so that under the
+    causal mask the rows from it to N-1 see it."""
+    start = 128 * ((N - 1) // 128)
+    return min(start + 4, N - 1)
+
+
+def make_structured_inputs(w: Workload, kind: str):
+    """(q, k, v) of the workload's shape and dtype, drawn to reach one corner case.
+
+    rising:        Q_i = sqrt(D) u + noise and K_j = c_j u + noise for a unit
+                   direction u per head, c_j growing by RISE_NATS_PER_TILE per
+                   128 keys, so that scale * <Q_i, K_j> is about c_j: every
+                   row's maximum rises tile after tile.
+    negative:      Q >= 0 and K <= -c elementwise, with c set so that the
+                   scores are about -NEGATIVE_NATS: every score of every row
+                   is far below zero.
+    dominant_last: Q_i = sqrt(D) u + noise, K ~ N(0, 1) except the key
+                   dominant_key(N) = DOMINANT_NATS u: one key, in the last
+                   (ragged) K/V tile, outweighs all others by about
+                   DOMINANT_NATS.
+    V ~ N(0, sigma_v^2) in every case. Draw order from the seeded CPU
+    generator: u, then the kind's noise terms, then V.
+    """
+    if kind not in STRUCTURED_KINDS:
+        raise ValueError(f"unknown kind {kind!r}")
+    g = torch.Generator(device="cpu")
+    g.manual_seed(w.seed)
+    B, H, N, D = w.B, w.H, w.N, w.D
+    shape = (B, H, N, D)
+    u = torch.randn((B, H, 1, D), dtype=torch.float64, generator=g)
+    u = u / u.norm(dim=-1, keepdim=True)
+    rd = math.sqrt(D)
+    if kind == "rising":
+        c = (torch.arange(N, dtype=torch.float64) * (RISE_NATS_PER_TILE / 128.0)).view(1, 1, N, 1)
+        q = rd * u + 0.5 * torch.randn(shape, dtype=torch.float64, generator=g)
+        k = c * u + 0.5 * torch.randn(shape, dtype=torch.float64, generator=g)
+    elif kind == "negative":
+        # E|z| = sqrt(2/pi) for z ~ N(0, 1): scores ~ -(1/sqrt(D)) * D * E|z| * (c + E|z|)
+        ez = math.sqrt(2.0 / math.pi)
+        cneg = NEGATIVE_NATS / (rd * ez) - ez
+        q = torch.randn(shape, dtype=torch.float64, generator=g).abs()
+        k = -(cneg + torch.randn(shape, dtype=torch.float64, generator=g).abs())
+    else:
+        q = rd * u + 0.5 * torch.randn(shape, dtype=torch.float64, generator=g)
+        k = torch.randn(shape, dtype=torch.float64, generator=g)
+        k[:, :, dominant_key(N), :] = DOMINANT_NATS * u[:, :, 0, :]
+    v = torch.randn(shape, dtype=torch.float64, generator=g) * w.sigma_v
+    dt = w.torch_dtype
+    return q.to(dt).contiguous(), k.to(dt).contiguous(), v.to(dt).contiguous()
