@@ -211,7 +211,7 @@ def workspace_for(device, D: int, stream=None):
     dev = torch.device(device)
     if stream is None:
         stream = torch.cuda.current_stream(dev)
-    key = (dev.index, D, int(stream.cuda_stream))
+    key = (dev.index, D, stream.cuda_stream)
     ws = _workspaces.get(key)
     if ws is None:
         with torch.cuda.device(dev):
@@ -260,52 +260,84 @@ def choose_schedule(B: int, H: int, N: int, is_causal: bool, sms: int, D: int = 
     return "balanced" if code == FA2_SCHED_BALANCED else "units"
 
 
+_DTYPE_CODES = {}
+
+
+def _dtype_code_of(dt) -> int:
+    code = _DTYPE_CODES.get(dt)
+    if code is None:
+        import torch
+        if dt == torch.float16:
+            code = FA2_F16
+        elif dt == torch.bfloat16:
+            code = FA2_BF16
+        else:
+            raise TypeError(f"unsupported dtype {dt}; expected float16 or bfloat16")
+        _DTYPE_CODES[dt] = code
+    return code
+
+
 def attention_forward(q, k, v, scale: float | None = None, is_causal: bool = False, out=None, lse=None,
                       stream=None, schedule: str = "auto", workspace=None):
     """FlashAttention-2 forward over torch CUDA tensors [B, H, N, D] (fp16/bf16).
 
     Returns (O, LSE): O like q, LSE float32 [B, H, N]. `out` / `lse` may be
     passed to write into caller-owned buffers. Runs on `stream` (a
-    torch.cuda.Stream) or the current stream.
+    torch.cuda.Stream) or the current stream of q's device.
     schedule: "auto" (the library's choice, fa2_fwd_sched with FA2_SCHED_AUTO),
     "balanced" (equal work per SM, with a workspace) or "units" (whole query
     tiles per CTA in rounds, no workspace).
     workspace: optional uint8 CUDA tensor for the balanced schedule; by default
     a cached one per (device, head dim, stream) is used, so calls on different
     streams never share one.
+    The checks here are the ones the C ABI cannot make (tensor metadata); the
+    library checks sizes, alignment and overlap itself.
     """
     import torch
     if not (q.is_cuda and k.is_cuda and v.is_cuda):
         raise ValueError("q, k, v must be CUDA tensors")
-    if q.shape != k.shape or q.shape != v.shape or q.dim() != 4:
+    shape = q.shape
+    if len(shape) != 4 or k.shape != shape or v.shape != shape:
         raise ValueError("q, k, v must share one [B, H, N, D] shape")
-    if q.dtype != k.dtype or q.dtype != v.dtype:
+    dt = q.dtype
+    if k.dtype != dt or v.dtype != dt:
         raise ValueError("q, k, v must share one dtype")
     if not (q.is_contiguous() and k.is_contiguous() and v.is_contiguous()):
         raise ValueError("q, k, v must be contiguous")
-    if schedule not in ("auto", "balanced", "units"):
+    code_sched = _SCHEDULES.get(schedule)
+    if code_sched is None:
         raise ValueError("schedule must be 'auto', 'balanced' or 'units'")
-    B, H, N, D = q.shape
+    if k.device != q.device or v.device != q.device:
+        raise ValueError("q, k, v must be on one device")
+    B, H, N, D = shape
+    dtc = _dtype_code_of(dt)
     if scale is None:
         scale = 1.0 / math.sqrt(D)
     if out is None:
         out = torch.empty_like(q)
+    elif out.shape != shape or out.dtype != dt or not out.is_contiguous() or out.device != q.device:
+        raise ValueError("out must be a contiguous tensor like q, on its device")
     if lse is None:
         lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
-    if out.shape != q.shape or out.dtype != q.dtype or not out.is_contiguous():
-        raise ValueError("out must be a contiguous tensor like q")
-    if lse.shape != (B, H, N) or lse.dtype != torch.float32 or not lse.is_contiguous():
-        raise ValueError("lse must be a contiguous float32 [B, H, N] tensor")
-    s = stream if stream is not None else torch.cuda.current_stream(q.device)
-    with torch.cuda.device(q.device):
-        if schedule == "units":
-            ws_ptr, ws_bytes = None, 0
-        else:
-            ws = workspace if workspace is not None else workspace_for(q.device, D, s)
-            ws_ptr, ws_bytes = ws.data_ptr(), ws.numel() * ws.element_size()
-        code = fa2_fwd_sched(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(),
-                             B, H, N, D, scale, int(bool(is_causal)), _dtype_code(q), ws_ptr, ws_bytes,
-                             _SCHEDULES[schedule], s.cuda_stream)
+    elif lse.shape != (B, H, N) or lse.dtype != torch.float32 or not lse.is_contiguous() or lse.device != q.device:
+        raise ValueError("lse must be a contiguous float32 [B, H, N] tensor on q's device")
+    dev = q.device
+    s = stream if stream is not None else torch.cuda.current_stream(dev)
+    if code_sched == FA2_SCHED_UNITS:
+        ws_ptr, ws_bytes = None, 0
+    else:
+        ws = workspace if workspace is not None else workspace_for(dev, D, s)
+        ws_ptr, ws_bytes = ws.data_ptr(), ws.numel() * ws.element_size()
+    lib = _lib if _lib is not None else library()
+    if torch.cuda.current_device() == dev.index:
+        code = lib.fa2_fwd_sched(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(), B, H, N,
+                                 D, scale, 1 if is_causal else 0, dtc, ws_ptr, ws_bytes, code_sched, s.cuda_stream)
+    else:
+        with torch.cuda.device(dev):
+            code = lib.fa2_fwd_sched(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), lse.data_ptr(), B, H,
+                                     N, D, scale, 1 if is_causal else 0, dtc, ws_ptr, ws_bytes, code_sched,
+                                     s.cuda_stream)
+    if code != FA2_OK:
         _check(code, "fa2_fwd_sched")
     return out, lse
 

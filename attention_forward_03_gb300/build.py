@@ -33,7 +33,9 @@ def nvcc() -> str:
 
 
 def _flags(verbose_ptxas: bool) -> list[str]:
-    f = ["-gencode", GENCODE, "-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC",
+    # hidden visibility: only the C ABI (FA2_API in fa2.h) is exported, so two
+    # copies of the library in one process never share a symbol
+    f = ["-gencode", GENCODE, "-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC,-fvisibility=hidden",
          "-I", INCLUDE, "-I", CSRC, "--expt-relaxed-constexpr"]
     if verbose_ptxas:
         f += ["-Xptxas", "-v"]

@@ -222,6 +222,48 @@ def split_job(w: workloads.Workload, split: str, world: int, rank: int):
     return local, h0, workloads.flops(w), f"heads x{world} (rank r owns a contiguous slice of the B*H heads)"
 
 
+def time_steps(step, steps: int, stream, dev, launch: str, clocks=None) -> float:
+    """Device seconds for `steps` calls of step(i, stream), on `stream`, by CUDA events.
+
+    launch="stream": the calls are made one by one inside the timed region.
+    launch="graph": the same calls (through the same API, with the same
+    arguments) are captured once into a CUDA graph on a side stream and the
+    graph is replayed once inside the timed region, so the per-launch host and
+    launch-queue costs are not in the timing; every step's kernels still run.
+    """
+    import torch
+    if launch == "graph":
+        cap = torch.cuda.Stream(device=dev)
+        cap.wait_stream(stream)
+        with torch.cuda.stream(cap):
+            step(0, cap)  # per-stream set-up (the binding's cached workspace) before the capture
+        torch.cuda.synchronize(dev)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=cap):
+            for i in range(steps):
+                step(i, cap)
+        with torch.cuda.stream(stream):
+            g.replay()  # one untimed replay: the graph's first launch pays its upload
+        torch.cuda.synchronize(dev)
+    ev0 = torch.cuda.Event(enable_timing=True)
+    ev1 = torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize(dev)
+    if clocks is not None:
+        clocks.mark_start()
+    with torch.cuda.stream(stream):
+        ev0.record(stream)
+        if launch == "graph":
+            g.replay()
+        else:
+            for i in range(steps):
+                step(i, stream)
+        ev1.record(stream)
+    torch.cuda.synchronize(dev)
+    if clocks is not None:
+        clocks.mark_stop()
+    return ev0.elapsed_time(ev1) / 1e3
+
+
 # ------------------------------------------------------------- CPU oracle leg
 def _row_flops(w: workloads.Workload, rows):
     import numpy as np
@@ -369,10 +411,12 @@ def run_gb300(args, w, rank, world, local):
 
     gather = args.gather and args.split == "heads" and world > 1
 
-    def step(i):
+    launch = "stream" if gather else args.launch
+
+    def step(i, st=None):
         qd, kd, vd, od, ld = sets[i % nsets]
-        fa2.attention_forward(qd, kd, vd, scale=w.scale, is_causal=w.causal, out=od, lse=ld, stream=stream,
-                              schedule=args.schedule)
+        fa2.attention_forward(qd, kd, vd, scale=w.scale, is_causal=w.causal, out=od, lse=ld,
+                              stream=st if st is not None else stream, schedule=args.schedule)
         if gather:
             partition.gather_heads(od, job.B * job.H, world, rank)
             partition.gather_heads(ld, job.B * job.H, world, rank)
@@ -393,24 +437,17 @@ def run_gb300(args, w, rank, world, local):
     torch.cuda.synchronize(dev)
     fa2.fa2_device_status(clear=True)
 
-    ev0 = torch.cuda.Event(enable_timing=True)
-    ev1 = torch.cuda.Event(enable_timing=True)
     barrier(world)
-    torch.cuda.synchronize(dev)
-    clocks.mark_start()
-    ev0.record(stream)
-    for i in range(args.steps):
-        step(i)
-    ev1.record(stream)
-    torch.cuda.synchronize(dev)
-    clocks.mark_stop()
+    elapsed = time_steps(step, args.steps, stream, dev, launch, clocks)
     barrier(world)
-    elapsed = ev0.elapsed_time(ev1) / 1e3
     clock_info = clocks.stop()
     status = fa2.fa2_device_status(clear=True)
     if status != 0:
         raise RuntimeError(f"device watchdog fired during the timed region (code {status})")
+    # the same steps launched one by one (reported beside the headline, not in it)
+    stream_elapsed = elapsed if launch == "stream" else time_steps(step, args.steps, stream, dev, "stream")
     t_max = max_over_ranks(elapsed, world, dev)
+    t_max_stream = max_over_ranks(stream_elapsed, world, dev)
     flops = workloads.flops(w)  # this rank's launches
     value = job_flops * args.steps / t_max / 1e12
     per_launch = elapsed / args.steps
@@ -440,6 +477,8 @@ def run_gb300(args, w, rank, world, local):
     torch.cuda.synchronize(dev)
     e2e_steps = max(3, min(args.steps, 50))
     barrier(world)
+    ev0 = torch.cuda.Event(enable_timing=True)
+    ev1 = torch.cuda.Event(enable_timing=True)
     ev0.record(stream)
     for _ in range(e2e_steps):
         e2e_step()
@@ -467,6 +506,8 @@ def run_gb300(args, w, rank, world, local):
                    "causal": job.causal, "scale": "1/sqrt(D)", "schedule": resolved_schedule,
                    "parallelism": parallelism + (", O/LSE all-gathered every step" if gather else ""),
                    "rank0_heads": [h0, h0 + w.B * w.H] if args.split == "heads" else None,
+                   "launch": ("one CUDA graph of the K steps' launches (captured through the binding and the "
+                              "C ABI), replayed once" if launch == "graph" else "K launches made one by one"),
                    "l2": f"inputs rotate over {nsets} copies ({nsets * set_bytes / 2**20:.0f} MiB > 2x L2)"},
         "pct_of_peak": 100.0 * achieved / peak,
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
@@ -479,6 +520,9 @@ def run_gb300(args, w, rank, world, local):
                 "chunk_schedule": chunk_schedule, "steps": e2e_steps},
         "gpu_launches": args.steps if w.B * w.H > 0 else 0,
         "clocks": clock_info,
+        "stream_launch": {"value": job_flops * args.steps / t_max_stream / 1e12, "unit": UNIT,
+                          "ms_per_step": 1e3 * t_max_stream / args.steps,
+                          "what": "the same K steps launched one by one from the host (per-launch costs included)"},
     }
     if not args.no_cpu_baseline:
         tf, secs, rows, threads, desc = oracle_sample(job, args.cpu_seconds)
@@ -530,10 +574,11 @@ def run_gb300_bwd(args, w, rank, world, local):
         sets.append((qd, kd, vd, od, ld, dod, outs, ws))
     torch.cuda.synchronize(dev)
 
-    def step(i):
+    def step(i, st=None):
         qd, kd, vd, od, ld, dod, outs, ws = sets[i % nsets]
         fa2.attention_backward(qd, kd, vd, od, ld, dod, scale=w.scale, is_causal=w.causal, dq=outs[0], dk=outs[1],
-                               dv=outs[2], workspace=ws, stream=stream, schedule=args.schedule)
+                               dv=outs[2], workspace=ws, stream=st if st is not None else stream,
+                               schedule=args.schedule)
 
     clocks = ClockSampler(local)
     clocks.start()
@@ -549,19 +594,9 @@ def run_gb300_bwd(args, w, rank, world, local):
             torch.cuda.synchronize(dev)
     torch.cuda.synchronize(dev)
     fa2.fa2_device_status(clear=True)
-    ev0 = torch.cuda.Event(enable_timing=True)
-    ev1 = torch.cuda.Event(enable_timing=True)
     barrier(world)
-    torch.cuda.synchronize(dev)
-    clocks.mark_start()
-    ev0.record(stream)
-    for i in range(args.steps):
-        step(i)
-    ev1.record(stream)
-    torch.cuda.synchronize(dev)
-    clocks.mark_stop()
+    elapsed = time_steps(step, args.steps, stream, dev, args.launch, clocks)
     barrier(world)
-    elapsed = ev0.elapsed_time(ev1) / 1e3
     clock_info = clocks.stop()
     status = fa2.fa2_device_status(clear=True)
     if status != 0:
@@ -585,6 +620,8 @@ def run_gb300_bwd(args, w, rank, world, local):
                    "scale": "1/sqrt(D)", "schedule": args.schedule + (" (the library's choice)"
                                                                       if args.schedule == "auto" else ""),
                    "parallelism": f"weak x{world} (one independent replica per GPU)",
+                   "launch": ("one CUDA graph of the K steps' calls, replayed once" if args.launch == "graph"
+                              else "K calls made one by one"),
                    "l2": f"inputs rotate over {nsets} copies ({nsets * set_bytes / 2**20:.0f} MiB > 2x L2)"},
         "pct_of_peak": 100.0 * achieved / peak,
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
@@ -620,6 +657,9 @@ def main(argv=None):
                          "rank r owns a contiguous slice of the B*H heads (strong scaling)")
     ap.add_argument("--gather", action="store_true",
                     help="with --split heads: all-gather O and LSE of every step to every rank (NCCL)")
+    ap.add_argument("--launch", default="graph", choices=["graph", "stream"],
+                    help="graph: the K timed steps are captured once into a CUDA graph and replayed (no per-launch "
+                         "host cost in the timing); stream: launched one by one (also reported in the line)")
     ap.add_argument("--settle-seconds", type=float, default=1.0)
     ap.add_argument("--e2e-heads-per-chunk", type=int, default=0,
                     help="heads per chunk of the end-to-end host-memory pipeline (0 = the binding's default)")

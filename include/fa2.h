@@ -32,6 +32,14 @@ extern "C" {
 
 struct CUstream_st; /* the same type as cudaStream_t / CUstream */
 
+/* The library is built with hidden symbol visibility; only the entry points
+ * below are exported. */
+#if defined(__GNUC__)
+#define FA2_API __attribute__((visibility("default")))
+#else
+#define FA2_API
+#endif
+
 /* dtype codes */
 #define FA2_F16 0  /* IEEE binary16 inputs and output */
 #define FA2_BF16 1 /* bfloat16 inputs and output      */
@@ -83,7 +91,7 @@ struct CUstream_st; /* the same type as cudaStream_t / CUstream */
  * errors are detected before anything is enqueued and leave O and LSE
  * untouched.
  */
-int fa2_fwd(const void* Q, const void* K, const void* V, void* O, float* LSE,
+FA2_API int fa2_fwd(const void* Q, const void* K, const void* V, void* O, float* LSE,
             int B, int H, int N, int D, float scale, int is_causal, int dtype,
             struct CUstream_st* stream);
 
@@ -95,7 +103,7 @@ int fa2_fwd(const void* Q, const void* K, const void* V, void* O, float* LSE,
  * not depend on B, H or N. Returns FA2_OK, FA2_ERR_INVALID_ARG (bytes NULL),
  * FA2_ERR_UNSUPPORTED (D) or FA2_ERR_CUDA.
  */
-int fa2_fwd_workspace_bytes(int D, size_t* bytes);
+FA2_API int fa2_fwd_workspace_bytes(int D, size_t* bytes);
 
 /*
  * fa2_fwd_ws — the same operation, arguments and results as fa2_fwd, with a
@@ -115,7 +123,7 @@ int fa2_fwd_workspace_bytes(int D, size_t* bytes);
  * Errors as fa2_fwd, plus FA2_ERR_INVALID_ARG for a workspace that is too
  * small or overlaps a tensor, FA2_ERR_ALIGN for a misaligned workspace.
  */
-int fa2_fwd_ws(const void* Q, const void* K, const void* V, void* O, float* LSE,
+FA2_API int fa2_fwd_ws(const void* Q, const void* K, const void* V, void* O, float* LSE,
                int B, int H, int N, int D, float scale, int is_causal, int dtype,
                void* workspace, size_t workspace_bytes, struct CUstream_st* stream);
 
@@ -139,7 +147,7 @@ int fa2_fwd_ws(const void* Q, const void* K, const void* V, void* O, float* LSE,
  * Errors as fa2_fwd_ws, plus FA2_ERR_INVALID_ARG for an unknown schedule code
  * or FA2_SCHED_BALANCED without a workspace.
  */
-int fa2_fwd_sched(const void* Q, const void* K, const void* V, void* O, float* LSE,
+FA2_API int fa2_fwd_sched(const void* Q, const void* K, const void* V, void* O, float* LSE,
                   int B, int H, int N, int D, float scale, int is_causal, int dtype,
                   void* workspace, size_t workspace_bytes, int schedule, struct CUstream_st* stream);
 
@@ -156,7 +164,7 @@ int fa2_fwd_sched(const void* Q, const void* K, const void* V, void* O, float* L
  * Returns FA2_OK, FA2_ERR_INVALID_ARG (NULL output, negative size, sms < 1)
  * or FA2_ERR_UNSUPPORTED (D).
  */
-int fa2_fwd_schedule_for(int B, int H, int N, int D, int is_causal, int sms, int* schedule);
+FA2_API int fa2_fwd_schedule_for(int B, int H, int N, int D, int is_causal, int sms, int* schedule);
 
 /*
  * fa2_fwd_noalloc — the same operation, arguments and results as fa2_fwd,
@@ -185,7 +193,7 @@ int fa2_fwd_schedule_for(int B, int H, int N, int D, int is_causal, int sms, int
  * without ordering) race on the array and must not be made.
  * Errors as fa2_fwd.
  */
-int fa2_fwd_noalloc(const void* Q, const void* K, const void* V, void* O, float* LSE,
+FA2_API int fa2_fwd_noalloc(const void* Q, const void* K, const void* V, void* O, float* LSE,
                     int B, int H, int N, int D, float scale, int is_causal, int dtype,
                     struct CUstream_st* stream);
 
@@ -198,7 +206,7 @@ int fa2_fwd_noalloc(const void* Q, const void* K, const void* V, void* O, float*
  * FA2_ERR_INVALID_ARG (bytes NULL, negative size, B*H above INT32_MAX),
  * FA2_ERR_UNSUPPORTED (D) or FA2_ERR_CUDA (no usable device).
  */
-int fa2_fwd_host_buffer_bytes(int B, int H, int N, int D, size_t* bytes);
+FA2_API int fa2_fwd_host_buffer_bytes(int B, int H, int N, int D, size_t* bytes);
 
 /*
  * fa2_fwd_host — the same operation and results as fa2_fwd, from and to HOST
@@ -240,7 +248,7 @@ int fa2_fwd_host_buffer_bytes(int B, int H, int N, int D, size_t* bytes);
  * (an internal lock); calls that share a dev_buffer must be ordered by the
  * caller.
  */
-int fa2_fwd_host(const void* Q, const void* K, const void* V, void* O, float* LSE,
+FA2_API int fa2_fwd_host(const void* Q, const void* K, const void* V, void* O, float* LSE,
                  int B, int H, int N, int D, float scale, int is_causal, int dtype,
                  int heads_per_chunk, int balanced, void* dev_buffer, size_t dev_bytes,
                  struct CUstream_st* stream);
@@ -254,7 +262,7 @@ int fa2_fwd_host(const void* Q, const void* K, const void* V, void* O, float* LS
  * Returns FA2_OK, FA2_ERR_INVALID_ARG (bytes NULL or a negative size) or
  * FA2_ERR_UNSUPPORTED (D not 32, 64, 96 or 128). Needs no device.
  */
-int fa2_bwd_workspace_bytes(int B, int H, int N, int D, size_t* bytes);
+FA2_API int fa2_bwd_workspace_bytes(int B, int H, int N, int D, size_t* bytes);
 
 /*
  * fa2_bwd — enqueue the backward pass (the gradient of fa2_fwd's O with
@@ -291,7 +299,7 @@ int fa2_bwd_workspace_bytes(int B, int H, int N, int D, size_t* bytes);
  * plus FA2_ERR_INVALID_ARG for a missing or too small workspace and
  * FA2_ERR_ALIGN for a misaligned one. The library allocates nothing.
  */
-int fa2_bwd(const void* Q, const void* K, const void* V, const void* O, const void* dO,
+FA2_API int fa2_bwd(const void* Q, const void* K, const void* V, const void* O, const void* dO,
             const float* LSE, void* dQ, void* dK, void* dV,
             int B, int H, int N, int D, float scale, int is_causal, int dtype,
             void* workspace, size_t workspace_bytes, struct CUstream_st* stream);
@@ -314,7 +322,7 @@ int fa2_bwd(const void* Q, const void* K, const void* V, const void* O, const vo
  * deterministic for dK and dV. Errors as fa2_bwd, plus FA2_ERR_INVALID_ARG
  * for an unknown schedule code.
  */
-int fa2_bwd_sched(const void* Q, const void* K, const void* V, const void* O, const void* dO,
+FA2_API int fa2_bwd_sched(const void* Q, const void* K, const void* V, const void* O, const void* dO,
                   const float* LSE, void* dQ, void* dK, void* dV,
                   int B, int H, int N, int D, float scale, int is_causal, int dtype,
                   void* workspace, size_t workspace_bytes, int schedule, struct CUstream_st* stream);
@@ -329,7 +337,7 @@ int fa2_bwd_sched(const void* Q, const void* K, const void* V, const void* O, co
  * site), FA2_ERR_INVALID_ARG (status NULL), FA2_ERR_UNSUPPORTED (not an
  * sm_103 device) or FA2_ERR_CUDA.
  */
-int fa2_device_status(struct CUstream_st* stream, int* status, int clear);
+FA2_API int fa2_device_status(struct CUstream_st* stream, int* status, int clear);
 
 /*
  * fa2_set_watchdog_ns — set the time (in nanoseconds) a kernel waits on any
@@ -337,7 +345,7 @@ int fa2_device_status(struct CUstream_st* stream, int* status, int clear);
  * winds down. Applies to launches made after the call, process-wide. 0
  * restores the default (1 s). Returns FA2_OK.
  */
-int fa2_set_watchdog_ns(unsigned long long ns);
+FA2_API int fa2_set_watchdog_ns(unsigned long long ns);
 
 /*
  * fa2_test_withhold_next_load — test hook for the watchdog. When enable is
@@ -348,17 +356,17 @@ int fa2_set_watchdog_ns(unsigned long long ns);
  * work in flight, and its outputs (O/LSE, or dQ/dK/dV) are left unspecified.
  * No GPU fault, trap or hang is involved. Returns FA2_OK.
  */
-int fa2_test_withhold_next_load(int enable);
+FA2_API int fa2_test_withhold_next_load(int enable);
 
 /* Human-readable text for a status code (static storage, never NULL). */
-const char* fa2_error_string(int code);
+FA2_API const char* fa2_error_string(int code);
 
 /* Text of the last CUDA error seen by this library on the calling thread
  * (static thread-local storage, never NULL; "" if none). */
-const char* fa2_last_cuda_error(void);
+FA2_API const char* fa2_last_cuda_error(void);
 
 /* Library ABI version: (major << 16) | minor. */
-int fa2_version(void);
+FA2_API int fa2_version(void);
 
 #ifdef __cplusplus
 }
