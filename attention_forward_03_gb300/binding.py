@@ -236,8 +236,8 @@ KV_TILE = 128    # keys per K/V tile
 
 
 def unit_rows(D: int = 128) -> int:
-    """Query rows per work unit: 256 (two 128-row sub-tiles), or 128 at head dim 256."""
-    return KV_TILE if D == 256 else UNIT_ROWS
+    """Query rows per work unit: 256 (two 128-row sub-tiles), or 128 at head dims from 256."""
+    return KV_TILE if D >= 256 else UNIT_ROWS
 
 
 def steps_per_head(N: int, is_causal: bool, D: int = 128) -> int:

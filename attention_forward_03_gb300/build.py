@@ -20,7 +20,8 @@ BUILD_DIR = os.path.join(PKG, "_build")
 LIB_NAME = "libfa2_gb300.so"
 LIB_PATH = os.path.join(PKG, LIB_NAME)
 SOURCES = ["fa2_api.cu", "fa2_noalloc.cu", "fa2_host.cu", "fa2_fwd_d32.cu", "fa2_fwd_d64.cu", "fa2_fwd_d96.cu",
-           "fa2_fwd_d128.cu", "fa2_fwd_d256.cu", "fa2_bwd_api.cu",
+           "fa2_fwd_d128.cu", "fa2_fwd_d256.cu",
+           "fa2_fwd_d512.cu", "fa2_fwd_d1024.cu", "fa2_bwd_api.cu",
            "fa2_bwd_d32.cu", "fa2_bwd_d64.cu", "fa2_bwd_d96.cu", "fa2_bwd_d128.cu"]
 GENCODE = "arch=compute_103a,code=sm_103a"
 

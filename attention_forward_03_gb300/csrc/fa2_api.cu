@@ -192,6 +192,12 @@ LaunchFn pick(int d, int dtype, int causal) {
     case 64: return pick_d<64>(bf, c);
     case 96: return pick_d<96>(bf, c);
     case 128: return pick_d<128>(bf, c);
+    case 512:
+      if (bf) return c ? launch_fwd_dtile<512, true, true> : launch_fwd_dtile<512, true, false>;
+      return c ? launch_fwd_dtile<512, false, true> : launch_fwd_dtile<512, false, false>;
+    case 1024:
+      if (bf) return c ? launch_fwd_dtile<1024, true, true> : launch_fwd_dtile<1024, true, false>;
+      return c ? launch_fwd_dtile<1024, false, true> : launch_fwd_dtile<1024, false, false>;
     default:
       if (bf) return c ? launch_fwd_wide<256, true, true> : launch_fwd_wide<256, true, false>;
       return c ? launch_fwd_wide<256, false, true> : launch_fwd_wide<256, false, false>;
@@ -240,7 +246,8 @@ int launch(const void* Q, const void* K, const void* V, void* O, float* LSE, int
   const int64_t bh = static_cast<int64_t>(B) * H;
   const int unit_rows = fwd_unit_rows(D), unit_subtiles = fwd_unit_subtiles(D);
   const int64_t n_qt = (static_cast<int64_t>(N) + unit_rows - 1) / unit_rows;
-  if (bh > INT32_MAX || bh * n_qt > INT32_MAX) return FA2_ERR_INVALID_ARG;
+  const int64_t bh_sched = bh * fwd_out_chunks(D);  // heads as the scheduler sees them
+  if (bh > INT32_MAX || bh_sched * n_qt > INT32_MAX) return FA2_ERR_INVALID_ARG;
   const uintptr_t mis = reinterpret_cast<uintptr_t>(Q) | reinterpret_cast<uintptr_t>(K) |
                         reinterpret_cast<uintptr_t>(V) | reinterpret_cast<uintptr_t>(O) |
                         reinterpret_cast<uintptr_t>(LSE) | reinterpret_cast<uintptr_t>(workspace);
@@ -263,12 +270,14 @@ int launch(const void* Q, const void* K, const void* V, void* O, float* LSE, int
   if (schedule == FA2_SCHED_AUTO && workspace &&
       fwd_auto_schedule(B, H, N, D, is_causal, info->sms) != FA2_SCHED_BALANCED)
     workspace = nullptr;  // the rounds win: run them, the workspace unused
+  if (fwd_dtiled(D)) workspace = nullptr;  // head dims 512, 1024: round schedule only
 
   CUtensorMap mq, mk, mv, mo;
-  // V boxes: 128 rows, or at head dim 256 64 rows (the kernel streams V in
-  // halves of 64 keys there); O: the kernel stores it through a map at D >= 96
+  // V boxes: 128 rows, or at head dims from 256 64 rows (the kernels stream V
+  // in halves of 64 keys there); O: the kernel stores it through a map at
+  // D = 96, 128
   if (!make_map(&mq, Q, (int)bh, N, D, dtype) || !make_map(&mk, K, (int)bh, N, D, dtype) ||
-      !make_rows_map(&mv, V, (int)bh, N, D, dtype, D == 256 ? 64u : 128u) || !make_map(&mo, O, (int)bh, N, D, dtype)) {
+      !make_rows_map(&mv, V, (int)bh, N, D, dtype, D >= 256 ? 64u : 128u) || !make_map(&mo, O, (int)bh, N, D, dtype)) {
     std::snprintf(t_last_cuda_error, sizeof(t_last_cuda_error), "cuTensorMapEncodeTiled failed");
     return FA2_ERR_CUDA;
   }
@@ -278,9 +287,9 @@ int launch(const void* Q, const void* K, const void* V, void* O, float* LSE, int
   p.status = info->status;
   p.watchdog_ns = g_watchdog_ns.load(std::memory_order_relaxed);
   p.N = N;
-  p.BH = (int)bh;
+  p.BH = (int)bh_sched;
   p.n_qt = (int)n_qt;
-  p.num_units = (int)(bh * n_qt);
+  p.num_units = (int)(bh_sched * n_qt);
   p.nkv_full = (N + kKeys - 1) / kKeys;
   p.scale_log2 = scale * 1.4426950408889634f;
   p.test_withhold = g_test_withhold.exchange(0, std::memory_order_relaxed);
@@ -294,7 +303,7 @@ int launch(const void* Q, const void* K, const void* V, void* O, float* LSE, int
     per_head = n_qt * static_cast<long long>(p.nkv_full);
   }
   p.steps_per_head = per_head;
-  p.total_steps = per_head * bh;
+  p.total_steps = per_head * bh_sched;
   int grid;
   if (workspace) {
     p.stream_k = 1;
@@ -373,7 +382,7 @@ int fwd_auto_schedule(long long B, long long H, long long N, int D, int is_causa
   constexpr double kSplitCostSteps = 4.0;
   const long long rows = fwd_unit_rows(D);
   const long long units = B * H * ((N + rows - 1) / rows);
-  if (is_causal || units <= 0 || sms <= 0) return FA2_SCHED_UNITS;
+  if (is_causal || units <= 0 || sms <= 0 || fwd_dtiled(D)) return FA2_SCHED_UNITS;
   const long long nkv = (N + kKeys - 1) / kKeys;
   const double rounds_cost = static_cast<double>((units + sms - 1) / sms) * static_cast<double>(nkv);
   const double balanced_cost = static_cast<double>(units) * static_cast<double>(nkv) / sms + kSplitCostSteps;

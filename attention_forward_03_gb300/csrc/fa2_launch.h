@@ -42,10 +42,17 @@ constexpr int kKeys = 128;          // keys per K/V tile
 // Q/K/V tile read as zeros (the copy engine's out-of-bounds fill), so they
 // add nothing to Q.K^T and P.V. 256 has a kernel of its own with one
 // 128-row query sub-tile per work unit (its O accumulator takes half of the
-// tensor memory).
-constexpr bool fwd_head_dim_ok(int d) { return d == 32 || d == 64 || d == 96 || d == 128 || d == 256; }
-constexpr int fwd_unit_subtiles(int d) { return d == 256 ? 1 : kSubTiles; }
+// tensor memory). 512 and 1024 tile the output's head dimension: a work unit
+// is 128 query rows and one 256-column chunk of O (fa2_kernel_dtile.cuh).
+constexpr int kDtileOutCols = 256;  // output columns per work unit at head dims 512 and 1024
+constexpr bool fwd_head_dim_ok(int d) {
+  return d == 32 || d == 64 || d == 96 || d == 128 || d == 256 || d == 512 || d == 1024;
+}
+constexpr bool fwd_dtiled(int d) { return d >= 512; }
+constexpr int fwd_unit_subtiles(int d) { return d >= 256 ? 1 : kSubTiles; }
 constexpr int fwd_unit_rows(int d) { return kRows * fwd_unit_subtiles(d); }
+// Output chunks per query tile: the units of one query tile.
+constexpr int fwd_out_chunks(int d) { return fwd_dtiled(d) ? d / kDtileOutCols : 1; }
 
 struct Params {
   void* o;                  // [B,H,N,D] 16-bit
@@ -53,7 +60,8 @@ struct Params {
   int* status;              // device watchdog word
   unsigned long long watchdog_ns;
   int N;
-  int BH;
+  int BH;                   // heads B*H; at head dims 512 and 1024 B*H times the output chunks (each
+                            // (head, chunk) pair is scheduled as a head of its own)
   int n_qt;                 // query work units per head = ceil(N / unit rows)
   int num_units;            // BH * n_qt
   int nkv_full;             // K/V tiles of a full row = ceil(N / 128)
@@ -114,11 +122,14 @@ struct BwdParams {
 // part of the caller's workspace, which is sized without a device).
 constexpr int kBwdMaxCtas = 160;
 
-// Bytes of stream-K workspace for `grid` CTAs at head dimension d.
+// Bytes of stream-K workspace for `grid` CTAs at head dimension d (none at
+// head dims 512 and 1024, which run on the round schedule only).
 constexpr size_t stream_k_workspace_bytes(int grid, int d) {
-  return (static_cast<size_t>(grid) * fwd_unit_subtiles(d) * ((static_cast<size_t>(d) * 128 + 3 * 128) * sizeof(float)) +
-          255) / 256 * 256 +
-         static_cast<size_t>(grid) * fwd_unit_subtiles(d) * 8;
+  return fwd_dtiled(d) ? 0
+                       : (static_cast<size_t>(grid) * fwd_unit_subtiles(d) *
+                              ((static_cast<size_t>(d) * 128 + 3 * 128) * sizeof(float)) +
+                          255) / 256 * 256 +
+                             static_cast<size_t>(grid) * fwd_unit_subtiles(d) * 8;
 }
 
 // The full forward call (validation, tensor maps, launch) with an optional
@@ -172,5 +183,11 @@ cudaError_t launch_fwd(const CUtensorMap& q, const CUtensorMap& k, const CUtenso
 template <int D, bool kBf16, bool kCausal>
 cudaError_t launch_fwd_wide(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v, const CUtensorMap& o,
                             const Params& p, int grid, cudaStream_t stream);
+
+// Head dims 512 and 1024 (fa2_kernel_dtile.cuh, instantiated in
+// fa2_fwd_d512.cu and fa2_fwd_d1024.cu); round schedule only.
+template <int D, bool kBf16, bool kCausal>
+cudaError_t launch_fwd_dtile(const CUtensorMap& q, const CUtensorMap& k, const CUtensorMap& v, const CUtensorMap& o,
+                             const Params& p, int grid, cudaStream_t stream);
 
 }  // namespace fa2

@@ -59,12 +59,17 @@ KERNEL_FILES = ("fa2_kernel.cuh", "fa2_fwd_common.cuh", "fa2_launch.h", "sm103_p
 # the head-dim-256 forward kernel
 WIDE_KERNEL_FILES = ("fa2_kernel_wide.cuh", "fa2_fwd_common.cuh", "fa2_launch.h", "sm103_ptx.cuh", "tmem_io.cuh",
                      "fa2_fwd_d256.cu", "fa2_api.cu")
+# the d-tiled forward kernel (head dims 512 and 1024)
+DTILE_KERNEL_FILES = ("fa2_kernel_dtile.cuh", "fa2_fwd_common.cuh", "fa2_launch.h", "sm103_ptx.cuh", "tmem_io.cuh",
+                      "fa2_fwd_d512.cu", "fa2_fwd_d1024.cu", "fa2_api.cu")
 # the same for the backward pass (its three kernels and their launch)
 BWD_KERNEL_FILES = ("fa2_bwd_kernel.cuh", "fa2_kernel.cuh", "fa2_fwd_common.cuh", "fa2_launch.h", "sm103_ptx.cuh",
                     "tmem_io.cuh", "fa2_bwd_d64.cu", "fa2_bwd_d128.cu", "fa2_bwd_api.cu", "fa2_api.cu")
 
 
 def fwd_kernel_files(D: int):
+    if D >= 512:
+        return DTILE_KERNEL_FILES
     return WIDE_KERNEL_FILES if D == 256 else KERNEL_FILES
 
 

@@ -70,7 +70,8 @@ def call(lib, **over):
 
 @pytest.mark.parametrize("over,code", [
     (dict(B=-1), -1), (dict(H=-3), -1), (dict(N=-1), -1),
-    (dict(D=48), -2), (dict(D=512), -2), (dict(D=0), -2), (dict(D=16), -2), (dict(D=160), -2), (dict(D=192), -2),
+    (dict(D=48), -2), (dict(D=768), -2), (dict(D=2048), -2), (dict(D=0), -2), (dict(D=16), -2), (dict(D=160), -2),
+    (dict(D=192), -2), (dict(D=384), -2),
     (dict(dtype=2), -2), (dict(dtype=-1), -2),
     (dict(scale=0.0), -1), (dict(scale=-0.5), -1), (dict(scale=float("nan")), -1), (dict(scale=float("inf")), -1),
     (dict(Q=None), -1), (dict(K=None), -1), (dict(V=None), -1), (dict(O=None), -1), (dict(LSE=None), -1),
@@ -96,7 +97,7 @@ def test_workspace_variant_checks_its_arguments(lib):
     assert call_ws(lib, A * 80, 1 << 20, D=48) == lib.FA2_ERR_UNSUPPORTED
     assert call_ws(lib, None, 0, B=0) == lib.FA2_OK
     n = ctypes.c_size_t(0)
-    assert lib.library().fa2_fwd_workspace_bytes(512, ctypes.byref(n)) == lib.FA2_ERR_UNSUPPORTED
+    assert lib.library().fa2_fwd_workspace_bytes(768, ctypes.byref(n)) == lib.FA2_ERR_UNSUPPORTED
     assert lib.library().fa2_fwd_workspace_bytes(64, None) == lib.FA2_ERR_INVALID_ARG
 
 
@@ -167,7 +168,7 @@ def test_empty_problem_is_a_no_op(lib, over):
 def test_valid_call_without_a_gpu_fails_loudly(lib):
     assert call(lib) == lib.FA2_ERR_CUDA
     # every supported head dimension passes the argument checks and reaches the device query
-    for d in (32, 64, 96, 128, 256):
+    for d in (32, 64, 96, 128, 256, 512, 1024):
         assert call(lib, D=d) == lib.FA2_ERR_CUDA
         assert call_ws(lib, A * 80, 1 << 24, D=d) == lib.FA2_ERR_CUDA
     assert lib.library().fa2_last_cuda_error().decode() != ""

@@ -98,7 +98,7 @@ def test_padded_head_dims_every_element(fa2, oracle_mod, N, D, dtype, causal, sc
 
 
 @pytest.mark.parametrize("schedule", SCHEDULES)
-@pytest.mark.parametrize("name", ["pages_d32", "target_d96", "target_d256"])
+@pytest.mark.parametrize("name", ["pages_d32", "target_d96", "target_d256", "target_d512", "target_d1024"])
 def test_other_head_dim_workloads_full_size(fa2, oracle_mod, name, schedule):
     compare(fa2, oracle_mod, workloads.WORKLOADS[name], sample=600, schedule=schedule)
 
@@ -139,6 +139,37 @@ def test_head_dim_256_peaked_logits(fa2, oracle_mod, schedule):
     # Q/K ~ N(0, 3^2) as in the ragged workload: sharply peaked rows in fp16.
     w = workloads.custom(2, 2, 1000, 256, "f16", False, seed=63, sigma_qk=3.0)
     compare(fa2, oracle_mod, w, schedule=schedule)
+
+
+EDGE_N_DTILE = [1, 63, 128, 129, 255, 257, 700]
+
+
+@pytest.mark.parametrize("N", EDGE_N_DTILE)
+@pytest.mark.parametrize("D", [512, 1024])
+@pytest.mark.parametrize("dtype", ["f16", "bf16"])
+@pytest.mark.parametrize("causal", [False, True])
+def test_d_tiled_head_dims_every_element(fa2, oracle_mod, N, D, dtype, causal):
+    # Head dims 512 and 1024: units of 128 query rows and one 256-column
+    # chunk of O, each recomputing the full S over all of D; Q and K stream
+    # through the ring in 128-column chunks, V in 64-key halves of the
+    # unit's columns (round schedule only: "balanced" runs the rounds).
+    w = workloads.custom(2, 2, N, D, dtype, causal, seed=N * 17 + D)
+    compare(fa2, oracle_mod, w, schedule="units")
+
+
+@pytest.mark.parametrize("D", [512, 1024])
+def test_d_tiled_many_units_per_cta_and_balanced_request(fa2, oracle_mod, D):
+    # More units than SMs (each CTA walks several (query tile, output chunk)
+    # units, the ring and barriers carrying over); a balanced request runs the
+    # rounds and gives the same output bit for bit.
+    w = workloads.custom(2, 20, 1024, D, "bf16", False, seed=D + 5)
+    q, k, v = workloads.make_inputs(w)
+    O1, L1 = run_gpu(fa2, q, k, v, w, schedule="units")
+    O2, L2 = run_gpu(fa2, q, k, v, w, schedule="balanced")
+    assert torch.equal(O1, O2) and torch.equal(L1, L2)
+    compare(fa2, oracle_mod, w, sample=300, schedule="units")
+    wc = workloads.custom(1, 12, 1500, D, "f16", True, seed=D + 6)
+    compare(fa2, oracle_mod, wc, sample=300, schedule="units")
 
 
 @pytest.mark.parametrize("schedule", SCHEDULES)
@@ -276,7 +307,7 @@ def base_moves_after_first_tile(q, k, scale, causal, tile=128):
     return moves
 
 
-CORNER_D = [32, 64, 96, 128, 256]
+CORNER_D = [32, 64, 96, 128, 256, 512, 1024]
 
 
 @pytest.mark.parametrize("schedule", SCHEDULES)

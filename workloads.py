@@ -25,6 +25,8 @@ Q/K/V i.i.d. normal, cast to the 16-bit type with round-to-nearest-even):
               head dimension 96)
   target_d256 B=1 H=8 N=8192 D=256 bf16 non-causal, seed 9 (the target shape at
               the first head dimension of the tiling_qk page's d-tiled range)
+  target_d512, target_d1024  the same at head dimensions 512 (seed 10) and
+              1024 (seed 11), the largest the tiling_qk page's launcher takes
 
 Scale is 1/sqrt(D) everywhere. Draw order: Q, then K, then V, each
 ``torch.randn(shape, dtype=float32, generator=g) * sigma`` from a CPU
@@ -76,6 +78,8 @@ WORKLOADS = {
     "pages_d32": Workload("pages_d32", 1, 8, 8192, 32, "f16", False, 7),
     "target_d96": Workload("target_d96", 1, 8, 8192, 96, "bf16", False, 8),
     "target_d256": Workload("target_d256", 1, 8, 8192, 256, "bf16", False, 9),
+    "target_d512": Workload("target_d512", 1, 8, 8192, 512, "bf16", False, 10),
+    "target_d1024": Workload("target_d1024", 1, 8, 8192, 1024, "bf16", False, 11),
 }
 
 # The five workloads the parity contract names, in their stated order.
