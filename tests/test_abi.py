@@ -135,7 +135,7 @@ def test_host_entry_point_checks_arguments_first(lib):
     assert host(B=0) == lib.FA2_OK and host(N=0, Q=None, buf=None) == lib.FA2_OK
     n = ctypes.c_size_t(0)
     assert so.fa2_fwd_host_buffer_bytes(1, 2, 64, 64, None) == lib.FA2_ERR_INVALID_ARG
-    assert so.fa2_fwd_host_buffer_bytes(1, 2, 64, 512, ctypes.byref(n)) == lib.FA2_ERR_UNSUPPORTED
+    assert so.fa2_fwd_host_buffer_bytes(1, 2, 64, 768, ctypes.byref(n)) == lib.FA2_ERR_UNSUPPORTED
     assert so.fa2_fwd_host_buffer_bytes(-1, 2, 64, 64, ctypes.byref(n)) == lib.FA2_ERR_INVALID_ARG
 
 
@@ -214,6 +214,9 @@ def test_schedule_choice(lib):
     # head dim 256: 128-row units (one sub-tile)
     assert choose_schedule(1, 8, 8192, False, 152, 256) == "balanced"  # 512 units: 4 rounds of 64 vs 220 steps
     assert choose_schedule(1, 19, 1024, False, 152, 256) == "units"    # exactly one full round
+    # head dims 512 and 1024 run on the round schedule only
+    assert choose_schedule(1, 8, 8192, False, 152, 512) == "units"
+    assert choose_schedule(1, 1, 8192, False, 152, 1024) == "units"
 
 
 def test_schedule_for_arguments(lib):

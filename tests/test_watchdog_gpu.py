@@ -28,7 +28,7 @@ def fa2():
     return m
 
 
-@pytest.mark.parametrize("D", [128, 256])
+@pytest.mark.parametrize("D", [128, 256, 512])
 def test_withheld_tile_times_out_and_the_context_stays_usable(fa2, oracle_mod, D):
     w = workloads.custom(1, 4, 512, D, "bf16", False, seed=77)
     q, k, v = (t.cuda() for t in workloads.make_inputs(w))
