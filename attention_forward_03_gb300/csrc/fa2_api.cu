@@ -408,7 +408,10 @@ extern "C" int fa2_fwd_sched(const void* Q, const void* K, const void* V, void* 
                              int schedule, struct CUstream_st* stream) {
   if (schedule != FA2_SCHED_AUTO && schedule != FA2_SCHED_UNITS && schedule != FA2_SCHED_BALANCED)
     return FA2_ERR_INVALID_ARG;
-  if (schedule == FA2_SCHED_BALANCED && !workspace && B > 0 && H > 0 && N > 0) return FA2_ERR_INVALID_ARG;
+  // the balanced schedule needs a workspace (none at head dims 512 and 1024,
+  // which run the rounds)
+  if (schedule == FA2_SCHED_BALANCED && !workspace && B > 0 && H > 0 && N > 0 && !fwd_dtiled(D))
+    return FA2_ERR_INVALID_ARG;
   return launch(Q, K, V, O, LSE, B, H, N, D, scale, is_causal, dtype, workspace, workspace_bytes, schedule,
                 reinterpret_cast<cudaStream_t>(stream));
 }

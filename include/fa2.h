@@ -134,7 +134,8 @@ FA2_API int fa2_fwd_ws(const void* Q, const void* K, const void* V, void* O, flo
  *     units, 128-row at head dim 256, dealt to persistent CTAs in rounds;
  *     heaviest first in a zig-zag when causal). `workspace` may be NULL.
  *   FA2_SCHED_BALANCED: the stream-K schedule of fa2_fwd_ws; `workspace`
- *     (as described there) is required.
+ *     (as described there) is required, except at head dims 512 and 1024,
+ *     which always run the round schedule and need none.
  *   FA2_SCHED_AUTO: the schedule fa2_fwd_schedule_for names for this
  *     problem on the current device; with a NULL workspace always the round
  *     schedule.

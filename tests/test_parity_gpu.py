@@ -310,6 +310,20 @@ def base_moves_after_first_tile(q, k, scale, causal, tile=128):
 CORNER_D = [32, 64, 96, 128, 256, 512, 1024]
 
 
+def lse_tolerance(q, k, w):
+    """TOL_LSE plus the fp32 accumulation bound of the scores: the tensor core
+    sums D/16 K-steps of 16 products into an fp32 accumulator, each step
+    rounding it by at most one ulp (2^-23 relative) of a partial sum no larger
+    than sum_d |q_d k_d|; the LSE, a smooth maximum of the scores, moves by at
+    most the largest score error. Small for ordinary inputs (about 1e-5
+    at D = 128 for N(0, 1) data); it matters only where every score has a
+    huge raw magnitude (the all-negative inputs at D = 1024: sum |q k| ~ 5e3)."""
+    qa = q.double().abs().reshape(-1, q.shape[2], q.shape[3])
+    ka = k.double().abs().reshape(-1, k.shape[2], k.shape[3])
+    l1 = float(torch.matmul(qa, ka.transpose(1, 2)).max())
+    return TOL_LSE + w.scale * (w.D / 16) * 2.0 ** -23 * l1
+
+
 @pytest.mark.parametrize("schedule", SCHEDULES)
 @pytest.mark.parametrize("causal", [False, True])
 @pytest.mark.parametrize("dtype", ["f16", "bf16"])
@@ -337,8 +351,9 @@ def test_online_softmax_corners_every_element(fa2, oracle_mod, kind, D, dtype, c
     Oref, Lref = oracle_mod.attention_fwd(q, k, v, w.scale, w.causal)
     err_o = float(np.abs(O.float().cpu().numpy() - Oref).max())
     err_l = float(np.abs(L.cpu().numpy() - Lref).max())
+    tol_l = lse_tolerance(q, k, w)
     assert err_o <= TOL_O[dtype], f"{kind} {w.describe()} {schedule}: max|dO| = {err_o:.3e}"
-    assert err_l <= TOL_LSE, f"{kind} {w.describe()} {schedule}: max|dLSE| = {err_l:.3e}"
+    assert err_l <= tol_l, f"{kind} {w.describe()} {schedule}: max|dLSE| = {err_l:.3e} (bound {tol_l:.3e})"
 
 
 @pytest.mark.parametrize("schedule", SCHEDULES)
