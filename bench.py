@@ -227,7 +227,7 @@ def split_job(w: workloads.Workload, split: str, world: int, rank: int):
     return local, h0, workloads.flops(w), f"heads x{world} (rank r owns a contiguous slice of the B*H heads)"
 
 
-def time_steps(step, steps: int, stream, dev, launch: str, clocks=None) -> float:
+def time_steps(step, steps: int, stream, dev, launch: str, clocks=None, resettle_s: float = 0.5) -> float:
     """Device seconds for `steps` calls of step(i, stream), on `stream`, by CUDA events.
 
     launch="stream": the calls are made one by one inside the timed region.
@@ -247,9 +247,16 @@ def time_steps(step, steps: int, stream, dev, launch: str, clocks=None) -> float
         with torch.cuda.graph(g, stream=cap):
             for i in range(steps):
                 step(i, cap)
-        with torch.cuda.stream(stream):
-            g.replay()  # one untimed replay: the graph's first launch pays its upload
-        torch.cuda.synchronize(dev)
+        # untimed replays: the first pays the graph's upload, and the clocks,
+        # which drop while the GPU idles during the capture, ramp back up
+        # (a timed replay straight after the capture measured 5-8 % low)
+        t0 = time.perf_counter()
+        while True:
+            with torch.cuda.stream(stream):
+                g.replay()
+            torch.cuda.synchronize(dev)
+            if time.perf_counter() - t0 >= resettle_s:
+                break
     ev0 = torch.cuda.Event(enable_timing=True)
     ev1 = torch.cuda.Event(enable_timing=True)
     torch.cuda.synchronize(dev)
