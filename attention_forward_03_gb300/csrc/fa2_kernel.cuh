@@ -94,6 +94,18 @@ struct Layout {
   static_assert(kSmemBytes <= 232448, "shared memory budget");
 };
 
+// End of sub-tile 0's K/V range in a segment [b, e). Under the causal mask
+// a unit of 256 query rows at q0 = 256 qt needs tiles [0, 2 qt + 2), but
+// its first 128 rows see no key of tile 2 qt + 1: when the segment holds
+// that tile and at least one other, sub-tile 0 stops one tile early (its S,
+// softmax pass and P.V there would only add zeros).
+template <bool kCausal>
+__device__ __forceinline__ int sub0_end(const Segment& w) {
+  if (!kCausal) return w.kv_end;
+  const bool skip = w.kv_end == w.nkv && w.nkv == 2 * (w.q0 / (2 * kRows)) + 2 && w.kv_end - 1 > w.kv_begin;
+  return skip ? w.kv_end - 1 : w.kv_end;
+}
+
 template <int D, bool kBf16, bool kCausal>
 __global__ void __launch_bounds__(kThreads, 1)
     fa2_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
@@ -370,7 +382,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int t = me;
           uint32_t q_round = 0, s_free_ph = 0, p_full_ph = 0;
           bool s_out = false;
+          bool skip_s = false;  // the S of the tile being taken is skipped (sub-tile 0, masked tile)
           auto next_s = [&](int slot_k) -> bool {
+            if (skip_s) {  // a tile sub-tile 0 skips: release the K slot, no product
+              mma_commit(bar_empty(slot_k));
+              return true;
+            }
             if (s_out) {
               if (!wait_bounded(bar_s_free0 + 8 * t, s_free_ph, wd, kSiteMmaSFree, true, kNapNs)) return false;
               s_free_ph ^= 1u;
@@ -384,25 +401,30 @@ __global__ void __launch_bounds__(kThreads, 1)
           };
           while (ok && next_segment<kCausal>(cur, w, p)) {
             const int b = w.kv_begin, e = w.kv_end;
+            const int et = t == 0 ? sub0_end<kCausal>(w) : e;  // this sub-tile's end
             if (!wait_bounded(bar_q_full, q_round & 1u, wd, kSiteMmaQFull, true, kNapNs)) { ok = false; break; }
             ++q_round;
             int slot_k = take(base_idx + k_index(b, b), 0u);
+            skip_s = false;
             if (slot_k < 0 || !next_s(slot_k)) { ok = false; break; }
             if (e - b == 1) mma_commit(bar_q_empty);
             for (int j = b; j < e && ok; ++j) {
               if (j + 1 < e) {
                 slot_k = take(base_idx + k_index(j + 1, b), 0u);
+                skip_s = j + 1 >= et;
                 if (slot_k < 0 || !next_s(slot_k)) { ok = false; break; }
                 if (j + 2 == e) mma_commit(bar_q_empty);
               }
               const int slot_v = take(base_idx + v_index(j, b, e), 1u);
               if (slot_v < 0) { ok = false; break; }
-              if (!wait_bounded(bar_p_full0 + 8 * t, p_full_ph, wd, kSiteMmaPFull, true, kNapNs)) { ok = false; break; }
-              p_full_ph ^= 1u;
-              tc_fence_after_sync();
-              issue_pv(t, slot_v, j > b);
-              mma_commit(bar_p_free0 + 8 * t);
-              if (j == e - 1) mma_commit(bar_o_full0 + 8 * t);
+              if (j < et) {
+                if (!wait_bounded(bar_p_full0 + 8 * t, p_full_ph, wd, kSiteMmaPFull, true, kNapNs)) { ok = false; break; }
+                p_full_ph ^= 1u;
+                tc_fence_after_sync();
+                issue_pv(t, slot_v, j > b);
+                mma_commit(bar_p_free0 + 8 * t);
+                if (j == et - 1) mma_commit(bar_o_full0 + 8 * t);
+              }
               mma_commit(bar_empty(slot_v));
             }
             base_idx += 2u * static_cast<uint32_t>(e - b);
@@ -460,7 +482,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       float base = -CUDART_INF_F;   // exponent base (log2 units) that l and O are relative to
       float l = 0.f;    // sum of p (unrounded): LSE
       float l_o = 0.f;  // normaliser of O (see below)
-      for (int j = w.kv_begin; j < w.kv_end; ++j) {
+      // sub-tile 0 skips its fully masked last tile where each sub-tile has
+      // its own MMA issuer (D <= 64; with the issuers split by type the two
+      // sub-tiles must stay in step)
+      const int e_t = (t == 0 && L::kPInTmem) ? sub0_end<kCausal>(w) : w.kv_end;
+      for (int j = w.kv_begin; j < e_t; ++j) {
         bool got = wait_bounded(bar_s, s_phase, wd, kSiteSoftmaxSFull);
         got = __all_sync(0xffffffffu, got);
         if (!got) { ok = false; break; }
