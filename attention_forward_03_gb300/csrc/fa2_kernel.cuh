@@ -176,6 +176,25 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     *abort_flag = 0;
     mbar_init_fence();
+    // The first segment's Q and first K tile are requested here, before the
+    // TMEM allocation, the CTA barrier and the register hand-off, so that
+    // their load latency overlaps that set-up; the producer carries on after
+    // them (ring slot 0).
+    SegCursor c0 = first_cursor(p);
+    Segment w0;
+    if (next_segment<kCausal>(c0, w0, p)) {
+      mbar_arrive_expect_tx(bar_q_full, L::kQBytes);
+      for (int t = 0; t < kSubTiles; ++t)
+        for (int pn = 0; pn < L::kPanels; ++pn)
+          tma_load_3d_hint(sQ + t * L::kTileBytes + pn * kPanelBytes, &tmQ, bar_q_full, pn * 64, w0.q0 + t * kRows,
+                           w0.bh, l2_policy_evict_first());
+      if (!p.test_withhold) {  // test hook: the first tile never arrives
+        mbar_arrive_expect_tx(bar_full(0, 0u), L::kTileBytes);
+        for (int pn = 0; pn < L::kPanels; ++pn)
+          tma_load_3d_hint(sRing + pn * kPanelBytes, &tmK, bar_full(0, 0u), pn * 64, w0.kv_begin * kKeys, w0.bh,
+                           l2_policy_evict_last());
+      }
+    }
   }
   if (warp == kMmaWarp) {
     tmem_alloc(smem_addr(tmem_slot), kTmemCols);
@@ -230,17 +249,26 @@ __global__ void __launch_bounds__(kThreads, 1)
           return true;
         };
         while (ok && next_segment<kCausal>(cur, w, p)) {
-          if (q_round > 0 && !wait_bounded(bar_q_empty, (q_round - 1) & 1u, wd, kSiteLoadQEmpty, true, kNapNs)) {
-            ok = false;
-            break;
+          if (q_round == 0) {
+            // Q and K_b of the first segment were requested at kernel entry
+            // (into ring slot 0): account for them as loads of this thread.
+            q_round = 1;
+            kbits ^= 1u;
+            ++issued;
+            slot = 1;
+          } else {
+            if (!wait_bounded(bar_q_empty, (q_round - 1) & 1u, wd, kSiteLoadQEmpty, true, kNapNs)) {
+              ok = false;
+              break;
+            }
+            mbar_arrive_expect_tx(bar_q_full, L::kQBytes);
+            for (int t = 0; t < kSubTiles; ++t)
+              for (int pn = 0; pn < L::kPanels; ++pn)
+                tma_load_3d_hint(sQ + t * L::kTileBytes + pn * kPanelBytes, &tmQ, bar_q_full, pn * 64,
+                                 w.q0 + t * kRows, w.bh, stream_once);
+            ++q_round;
+            ok = load_tile(&tmK, w.kv_begin, 0u);
           }
-          mbar_arrive_expect_tx(bar_q_full, L::kQBytes);
-          for (int t = 0; t < kSubTiles; ++t)
-            for (int pn = 0; pn < L::kPanels; ++pn)
-              tma_load_3d_hint(sQ + t * L::kTileBytes + pn * kPanelBytes, &tmQ, bar_q_full, pn * 64,
-                               w.q0 + t * kRows, w.bh, stream_once);
-          ++q_round;
-          ok = load_tile(&tmK, w.kv_begin, 0u);
           for (int j = w.kv_begin; j < w.kv_end && ok; ++j) {
             if (j + 1 < w.kv_end) ok = load_tile(&tmK, j + 1, 0u);
             if (ok) ok = load_tile(&tmV, j, 1u);
