@@ -405,6 +405,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     }
     __syncwarp();
   } else if (warp == kBwdMmaWarp || (kTwoIssuers && warp == kBwdGradWarp)) {
+    // The issuers poll their barriers without sleeping: each step is a chain
+    // of hand-offs between them and the compute warpgroups, and a sleeping
+    // waiter wakes late (measured: 0 to +2.3 % across the backward workloads).
     // --------------------------------------------------------- MMA issuers
     if (lane == 0) {
       constexpr uint32_t idesc_s = make_idesc_f16(kBf16, L::kSR, false);              // S^T, dP^T: N = SR
@@ -488,17 +491,17 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         BwdSegment sg;
         while (ok && bwd_next_segment<kCausal, L::kR>(cur, sg, p)) {
           const int n_steps = sg.i_end - sg.i_begin;
-          if (!wait_bounded(bar_kv_full, units & 1u, wd, kSiteBwdKvFull, true, kNapNs)) {
+          if (!wait_bounded(bar_kv_full, units & 1u, wd, kSiteBwdKvFull, true, 0u)) {
             ok = false;
             break;
           }
           for (int t = 0; t < n_steps; ++t, ++g) {
-            if (!wait_bounded(bar_stage_full(slot), ph, wd, kSiteBwdStageFull, true, kNapNs)) {
+            if (!wait_bounded(bar_stage_full(slot), ph, wd, kSiteBwdStageFull, true, 0u)) {
               ok = false;
               break;
             }
             if (scores) {
-              if (g > 0 && !wait_bounded(bar_s_free, (g - 1) & 1u, wd, kSiteBwdSFree, true, kNapNs)) {
+              if (g > 0 && !wait_bounded(bar_s_free, (g - 1) & 1u, wd, kSiteBwdSFree, true, 0u)) {
                 ok = false;
                 break;
               }
@@ -507,19 +510,19 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
               mma_commit(bar_s_full);
               mma_commit(bar_stage_empty(slot));
             } else {
-              if (!wait_bounded(bar_p_full, g & 1u, wd, kSiteBwdPFull, true, kNapNs)) {
+              if (!wait_bounded(bar_p_full, g & 1u, wd, kSiteBwdPFull, true, 0u)) {
                 ok = false;
                 break;
               }
               if (t == 0 && units > 0 &&
-                  !wait_bounded(bar_acc_free, (units - 1) & 1u, wd, kSiteBwdAccFree, true, kNapNs)) {
+                  !wait_bounded(bar_acc_free, (units - 1) & 1u, wd, kSiteBwdAccFree, true, 0u)) {
                 ok = false;
                 break;
               }
               tc_fence_after_sync();
               issue_grads(slot, t > 0);
               mma_commit(bar_stage_empty(slot));
-              if (g > 0 && !wait_bounded(bar_dq_free, (g - 1) & 1u, wd, kSiteBwdDqFree, true, kNapNs)) {
+              if (g > 0 && !wait_bounded(bar_dq_free, (g - 1) & 1u, wd, kSiteBwdDqFree, true, 0u)) {
                 ok = false;
                 break;
               }
@@ -548,8 +551,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         // threads hold the previous step's S^T / dP^T, issues this step's.
         auto start_step = [&](uint32_t step) -> int {
           const int s = slot;
-          if (!wait_bounded(bar_stage_full(s), ph, wd, kSiteBwdStageFull, true, kNapNs)) return -1;
-          if (step > 0 && !wait_bounded(bar_s_free, (step - 1) & 1u, wd, kSiteBwdSFree, true, kNapNs)) return -1;
+          if (!wait_bounded(bar_stage_full(s), ph, wd, kSiteBwdStageFull, true, 0u)) return -1;
+          if (step > 0 && !wait_bounded(bar_s_free, (step - 1) & 1u, wd, kSiteBwdSFree, true, 0u)) return -1;
           tc_fence_after_sync();
           issue_sdp(s);
           mma_commit(bar_s_full);
@@ -563,7 +566,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         BwdSegment sg;
         while (ok && bwd_next_segment<kCausal, L::kR>(wcur, sg, p)) {
           const int n_steps = sg.i_end - sg.i_begin;
-          if (!wait_bounded(bar_kv_full, units & 1u, wd, kSiteBwdKvFull, true, kNapNs)) {
+          if (!wait_bounded(bar_kv_full, units & 1u, wd, kSiteBwdKvFull, true, 0u)) {
             ok = false;
             break;
           }
@@ -583,20 +586,20 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 break;
               }
             }
-            if (!wait_bounded(bar_p_full, g & 1u, wd, kSiteBwdPFull, true, kNapNs)) {
+            if (!wait_bounded(bar_p_full, g & 1u, wd, kSiteBwdPFull, true, 0u)) {
               ok = false;
               break;
             }
             // the unit's first accumulation overwrites dV / dK: the previous
             // unit's epilogue must have loaded them
-            if (t == 0 && units > 0 && !wait_bounded(bar_acc_free, (units - 1) & 1u, wd, kSiteBwdAccFree, true, kNapNs)) {
+            if (t == 0 && units > 0 && !wait_bounded(bar_acc_free, (units - 1) & 1u, wd, kSiteBwdAccFree, true, 0u)) {
               ok = false;
               break;
             }
             tc_fence_after_sync();
             issue_grads(cur, t > 0);
             mma_commit(bar_stage_empty(cur));
-            if (g > 0 && !wait_bounded(bar_dq_free, (g - 1) & 1u, wd, kSiteBwdDqFree, true, kNapNs)) {
+            if (g > 0 && !wait_bounded(bar_dq_free, (g - 1) & 1u, wd, kSiteBwdDqFree, true, 0u)) {
               ok = false;
               break;
             }
