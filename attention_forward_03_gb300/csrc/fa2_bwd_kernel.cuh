@@ -24,13 +24,15 @@
 //              g takes query columns [32g, 32g+32) of every step (and, in
 //              the epilogue, the dK / dV row's 32-column chunks: the first
 //              half of them, rounded up, for g = 0, the rest for g = 1)
-//   warp  8    tcgen05 MMA issuer (one thread), owns the TMEM allocation
-//   warp  9    non-causal launches: a second issuer. Warp 8 then issues the
-//              score products S^T, dP^T and warp 9 the gradient products dV,
-//              dK, dQ^T (measured 9 % faster on long non-causal rows; causal
-//              launches, whose units are short and start on the masked
-//              diagonal, keep one issuer that computes the next step's
-//              scores before the current step's gradients)
+//   warp  8    tcgen05 MMA issuer (one thread) of the score products S^T,
+//              dP^T; owns the TMEM allocation
+//   warp  9    tcgen05 MMA issuer (one thread) of the gradient products dV,
+//              dK, dQ^T. Both issuers poll their barriers without sleeping;
+//              with that, two issuers also pay on causal launches (long
+//              causal rows +19.5 %, B4 H16 N4096 causal +13.5 % over one
+//              issuer that computed the next step's scores before the
+//              current step's gradients), where with sleeping waits they had
+//              measured 1 % slower.
 //   warp  10   TMA producer (one thread)
 // Head dims 32 and 96 run in the tiles of 64 and 128 (Dp below): their
 // columns past D arrive as zeros from the copy engine, so they add nothing.
@@ -65,7 +67,7 @@ namespace fa2 {
 
 constexpr int kBwdThreads = 352;    // 11 warps
 constexpr int kBwdMmaWarp = 8;      // MMA issuer (all products, or S^T / dP^T); owns the TMEM allocation
-constexpr int kBwdGradWarp = 9;     // second MMA issuer (dV, dK, dQ^T) of non-causal launches
+constexpr int kBwdGradWarp = 9;     // second MMA issuer (dV, dK, dQ^T)
 constexpr int kBwdLoadWarp = 10;
 constexpr int kBwdComputeThreads = 256;
 
@@ -143,10 +145,10 @@ struct BwdLayout {
   // step's P^T and dS^T as packed 16-bit pairs: the A operands of dV += P^T
   // dO and dK += dS^T Q then come from tensor memory (the faster form of the
   // MMA, and no shared-memory operand reads for them). dS^T also goes to
-  // shared memory, where dQ^T = K^T dS^T reads it as its B operand. Used by
-  // non-causal launches only (the kernel's kATmem): measured +1.8 % (target)
-  // and +2.5 % (B4 H16 N8192 D128) there, but -2.4 % on long causal rows,
-  // whose single issuer waits on the compute threads' extra TMEM stores.
+  // shared memory, where dQ^T = K^T dS^T reads it as its B operand. Measured
+  // +1.8 % (target) and +2.5 % (B4 H16 N8192 D128) non-causal, and, with two
+  // non-sleeping issuers, +1 to +2 % on causal launches too (with one
+  // issuer it had been -2.4 % on long causal rows).
   static constexpr bool kGradATmem = (kSR == 64);
   static constexpr uint32_t kColPT = kColDQ + kSR;
   static constexpr uint32_t kColDST = kColPT + kSR / 2;
@@ -262,8 +264,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                    const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmDO,
                    const __grid_constant__ CUtensorMap tmDQ, const BwdParams p) {
   using L = BwdLayout<D>;
-  constexpr bool kTwoIssuers = !kCausal;
-  constexpr bool kATmem = L::kGradATmem && !kCausal;  // P^T, dS^T in TMEM for dV, dK
+  constexpr bool kTwoIssuers = true;
+  constexpr bool kATmem = L::kGradATmem;  // P^T, dS^T in TMEM for dV, dK
   constexpr uint32_t kReaders = kTwoIssuers ? 2 : 1;  // issuer threads reading a ring slot and K/V
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   const uint32_t raw = smem_addr(smem_raw);
