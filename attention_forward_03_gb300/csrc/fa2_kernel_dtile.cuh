@@ -28,13 +28,15 @@
 // Tensor memory: [0,128) S, [128,384) O (this unit's 256 columns), [384,448)
 // P (16-bit pairs). One S buffer: the softmax copies S into registers and
 // releases it at once, so S(j+1) is computed during the softmax of tile j.
-// Shared memory: a ring of seven 32 KB slots and nothing else (Q is not
-// resident: 128 KB at D = 512 and 256 KB at 1024 leave no room for a ring).
-// Slot contents: a chunk of Q or of K (128 rows x 128 head-dim columns, two
-// 64-column panels), or half a V tile (64 keys x the unit's 256 columns,
-// four panels of 64 rows); all 128-byte swizzled. Load order per segment
-// [b, e): the S operands of tile b (Q_0, K_{b,0}, Q_1, K_{b,1}, ...), then for
-// each j: those of tile j+1 (if any), V_j's two halves.
+// Shared memory at D = 512: the unit's Q (128 KB, resident for the segment)
+// and a ring of three 32 KB slots; at D = 1024 (a resident Q would be 256 KB)
+// a ring of seven slots and nothing else, Q streaming through the ring with
+// K. Slot contents: a chunk of K (or, at D = 1024, of Q): 128 rows x 128
+// head-dim columns, two 64-column panels; or half a V tile (64 keys x the
+// unit's 256 columns, four panels of 64 rows); all 128-byte swizzled. Load
+// order per segment [b, e): Q (D = 512), the S operands of tile b (K_{b,0},
+// K_{b,1}, ...; at D = 1024 Q_0, K_{b,0}, Q_1, K_{b,1}, ...), then for each j:
+// those of tile j+1 (if any), V_j's two halves.
 // Only the round schedule runs here (whole units dealt to the CTAs); the
 // host never asks for stream-K at these head dims.
 #pragma once
@@ -49,13 +51,17 @@ struct DtileLayout {
   static constexpr int kOutChunks = D / kDtileOutCols;      // output chunks per query tile
   static constexpr int kSlotBytes = 2 * kPanelBytes;        // 32 KB
   static constexpr int kVPanelBytes = kSlotBytes / 4;       // V half: 64 rows x 64 columns per panel
-  static constexpr int kStages = 7;
-  static constexpr int kItemsS = 2 * kChunks;               // ring items of one S: Q_c, K_c for each chunk
-  static constexpr int kRingOffset = 0;
+  // Q resident in shared memory (D = 512: 128 rows x 512 = 128 KB) or
+  // streamed through the ring with K (D = 1024)
+  static constexpr bool kQRes = (D == 512);
+  static constexpr int kQBytes = kQRes ? kRows * D * 2 : 0;
+  static constexpr int kStages = kQRes ? 3 : 7;
+  static constexpr int kItemsS = kQRes ? kChunks : 2 * kChunks;  // ring items of one S: K_c (and Q_c) per chunk
+  static constexpr int kRingOffset = kQBytes;
   static constexpr int kBarOffset = kRingOffset + kStages * kSlotBytes;
   // barriers: ring full (S operand)[S], ring full (V half)[S], ring empty[S], s_full, s_free, p_full, p_free,
-  // o_full, drain[2]
-  static constexpr int kNumBars = 3 * kStages + 7;
+  // o_full, drain[2], q_full, q_empty
+  static constexpr int kNumBars = 3 * kStages + 9;
   static constexpr int kMiscOffset = kBarOffset + kNumBars * 8;
   static constexpr int kSmemBytes = kMiscOffset + 16 + 1024;  // + slack for 1 KB alignment
   static constexpr uint32_t kColO = kKeys;                      // O at 128
@@ -77,6 +83,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t base = (raw + 1023u) & ~1023u;
   uint8_t* smem = smem_raw + (base - raw);
 
+  const uint32_t sQ = base;  // D = 512: the resident Q
   const uint32_t sRing = base + L::kRingOffset;
   const uint32_t bars = base + L::kBarOffset;
   // Per slot one "full" barrier per item type (0: S operand, 1: V half; each
@@ -90,6 +97,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t bar_p_free = bar_p_full + 8;
   const uint32_t bar_o_full = bar_p_free + 8;
   const uint32_t bar_drain = bar_o_full + 8;  // [issuer]
+  const uint32_t bar_q_full = bar_drain + 16;  // D = 512: the resident Q has landed
+  const uint32_t bar_q_empty = bar_q_full + 8;  // D = 512: the segment's last S has read it
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kMiscOffset);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kMiscOffset + 4);
 
@@ -109,6 +118,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(bar_o_full, 1);
     mbar_init(bar_drain, 1);
     mbar_init(bar_drain + 8, 1);
+    mbar_init(bar_q_full, 1);
+    mbar_init(bar_q_empty, 1);
     *abort_flag = 0;
     mbar_init_fence();
   }
@@ -144,7 +155,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tma_prefetch_map(&tmV);
         const uint64_t keep = l2_policy_evict_last();  // Q, K, V: each re-read by several units
         int slot = 0;
-        uint32_t ring_ph = 0, issued = 0;
+        uint32_t ring_ph = 0, issued = 0, q_round = 0;
         uint32_t types = 0, sbits = 0, vbits = 0;  // per slot: latest item's type; next S / V full parity
         bool ok = true;
         SegCursor cur = first_cursor(p);
@@ -171,9 +182,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         };
         while (ok && next_segment<kCausal, kR>(cur, w, p)) {
           const int bh = w.bh / kNO, oc = w.bh % kNO;
+          if constexpr (L::kQRes) {
+            // the unit's Q, once the previous segment's last S has read it
+            if (q_round > 0 && !wait_bounded(bar_q_empty, (q_round - 1) & 1u, wd, kSiteLoadQEmpty, true, kNapNs)) {
+              ok = false;
+              break;
+            }
+            mbar_arrive_expect_tx(bar_q_full, L::kQBytes);
+            for (int pn = 0; pn < D / 64; ++pn)
+              tma_load_3d_hint(sQ + pn * kPanelBytes, &tmQ, bar_q_full, 64 * pn, w.q0, bh, keep);
+            ++q_round;
+          }
           auto load_s = [&](int j) -> bool {
             for (int c = 0; c < kNC && ok; ++c) {
-              if (!load_item(&tmQ, 128 * c, w.q0, bh, 2, kPanelBytes, 0u)) return false;
+              if (!L::kQRes && !load_item(&tmQ, 128 * c, w.q0, bh, 2, kPanelBytes, 0u)) return false;
               if (!load_item(&tmK, 128 * c, j * kKeys, bh, 2, kPanelBytes, 0u)) return false;
             }
             return true;
@@ -197,6 +219,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t par = (((is_v ? vbits : sbits) >> s) & 1u) ^ 1u;
           wait_bounded(bar_full(s, is_v), par, wd, kSiteDrain, false, kNapNs);
         }
+        if (L::kQRes && q_round > 0) wait_bounded(bar_q_full, (q_round - 1) & 1u, wd, kSiteDrain, false, kNapNs);
       }
       __syncwarp();
     } else if (warp < kMmaWarp + kIssuers) {
@@ -221,34 +244,43 @@ __global__ void __launch_bounds__(kThreads, 1)
           // S(j) = sum_c Q_c K_{j,c}^T: 8 K-steps per chunk, A = Q chunk and
           // B = K chunk (both K-major, two 64-column panels). The S buffer
           // is overwritten only once the softmax has copied the previous S.
-          uint32_t s_free_ph = 0;
+          uint32_t s_free_ph = 0, q_round = 0;
           bool s_out = false;
           while (ok && next_segment<kCausal, kR>(cur, w, p)) {
             const int b = w.kv_begin, e = w.kv_end;
+            if (L::kQRes) {
+              if (!wait_bounded(bar_q_full, q_round & 1u, wd, kSiteMmaQFull, true, kNapNs)) { ok = false; break; }
+              ++q_round;
+            }
             for (int j = b; j < e && ok; ++j) {
               const uint32_t i0 = base_idx + static_cast<uint32_t>(s_pos(j, b));
               for (int c = 0; c < kNC; ++c) {
-                const int slot_q = take(i0 + 2 * c, 0u);
-                const int slot_k = slot_q < 0 ? -1 : take(i0 + 2 * c + 1, 0u);
+                // A: the Q chunk (resident at D = 512, else the ring item
+                // before K's); B: the K chunk
+                const int slot_q = L::kQRes ? 0 : take(i0 + 2 * c, 0u);
+                const int slot_k = slot_q < 0 ? -1 : take(L::kQRes ? i0 + c : i0 + 2 * c + 1, 0u);
                 if (slot_k < 0) { ok = false; break; }
                 if (c == 0 && s_out) {
                   if (!wait_bounded(bar_s_free, s_free_ph, wd, kSiteMmaSFree, true, kNapNs)) { ok = false; break; }
                   s_free_ph ^= 1u;
                 }
                 tc_fence_after_sync();
-                const uint32_t qa = desc_lo_sw128(sRing, 16) + static_cast<uint32_t>(slot_q * (L::kSlotBytes >> 4));
+                const uint32_t qa =
+                    L::kQRes ? desc_lo_sw128(sQ, 16) + static_cast<uint32_t>(c * (L::kSlotBytes >> 4))
+                             : desc_lo_sw128(sRing, 16) + static_cast<uint32_t>(slot_q * (L::kSlotBytes >> 4));
                 const uint32_t ka = desc_lo_sw128(sRing, 16) + static_cast<uint32_t>(slot_k * (L::kSlotBytes >> 4));
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk) {
                   const uint32_t off = static_cast<uint32_t>(((kk >> 2) * kPanelBytes + (kk & 3) * 32) >> 4);
                   mma_ss_w(tmem, qa + off, kHi, ka + off, kHi, idesc_s, (c > 0 || kk > 0) ? 1u : 0u);
                 }
-                mma_commit(bar_empty(slot_q));
+                if (!L::kQRes) mma_commit(bar_empty(slot_q));
                 mma_commit(bar_empty(slot_k));
               }
               if (!ok) break;
               mma_commit(bar_s_full);
               s_out = true;
+              if (L::kQRes && j == e - 1) mma_commit(bar_q_empty);
             }
             base_idx += static_cast<uint32_t>(seg_items(b, e));
           }
