@@ -378,7 +378,7 @@ def test_rising_scores_longer_rows_and_many_units(fa2, oracle_mod, shape, schedu
 
 
 @pytest.mark.parametrize("shape", [(1, 2, 4096, 128, False), (1, 38, 1024, 128, False), (1, 39, 1024, 128, False),
-                                   (2, 3, 1000, 64, True), (1, 4, 2048, 256, False)])
+                                   (2, 3, 1000, 64, True), (1, 4, 2048, 256, False), (1, 2, 1500, 512, False)])
 def test_auto_schedule_in_c_runs_the_named_schedule(fa2, shape):
     # fa2_fwd_sched(FA2_SCHED_AUTO) takes the schedule fa2_fwd_schedule_for
     # names: its output is bit-identical to that schedule's own entry point
@@ -407,3 +407,17 @@ def test_auto_schedule_in_c_runs_the_named_schedule(fa2, shape):
         outs.append((o, lse))
     assert fa2.fa2_device_status(clear=True) == 0
     assert torch.equal(outs[0][0], outs[1][0]) and torch.equal(outs[0][1], outs[1][1])
+    # with no workspace the library's choice is always the rounds (fa2_fwd)
+    o = torch.full_like(q, float("nan"))
+    lse = torch.full((B, H, N), float("nan"), dtype=torch.float32, device="cuda")
+    rc = fa2.fa2_fwd_sched(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(), B, H, N, D,
+                           w.scale, int(causal), fa2.FA2_BF16, None, 0, fa2.FA2_SCHED_AUTO,
+                           torch.cuda.current_stream().cuda_stream)
+    assert rc == fa2.FA2_OK, fa2.error_text(rc)
+    o_u = torch.empty_like(q)
+    l_u = torch.empty((B, H, N), dtype=torch.float32, device="cuda")
+    rc = fa2.fa2_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o_u.data_ptr(), l_u.data_ptr(), B, H, N, D, w.scale,
+                     int(causal), fa2.FA2_BF16, torch.cuda.current_stream().cuda_stream)
+    assert rc == fa2.FA2_OK, fa2.error_text(rc)
+    torch.cuda.synchronize()
+    assert torch.equal(o, o_u) and torch.equal(lse, l_u)

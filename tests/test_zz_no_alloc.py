@@ -41,7 +41,7 @@ def _ptrs(*ts):
 
 @pytest.mark.parametrize("shape", [(1, 8, 2048, 128, "bf16", False), (2, 3, 1000, 64, "f16", True),
                                    (1, 2, 3000, 128, "f16", True), (1, 3, 777, 96, "bf16", False),
-                                   (1, 4, 1500, 256, "f16", True)])
+                                   (1, 4, 1500, 256, "f16", True), (1, 2, 700, 512, "bf16", True)])
 def test_no_alloc_matches_the_workspace_entry_point(lib, shape):
     B, H, N, D, dtype, causal = shape
     code = lib.FA2_BF16 if dtype == "bf16" else lib.FA2_F16
