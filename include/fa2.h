@@ -71,13 +71,17 @@ struct CUstream_st; /* the same type as cudaStream_t / CUstream */
  * B, H, N : batch, heads, sequence length (queries and keys), each >= 0. If
  *           any is 0 the call does nothing and returns FA2_OK (pointers may
  *           then be NULL).
- * D       : head dimension; 32, 64, 96, 128 or 256. 64 and 128 are the
- *           native tile widths; 32 and 96 run in the tiles of 64 and 128,
- *           whose columns past D the kernel reads as zeros. These four are
- *           the head dims the split-Q launcher of "FlashAttention-2 MMA
- *           代码学习" dispatches (its host function at the end of the page);
- *           256, the first of the tiling_qk page's larger ones, runs on a
- *           kernel of its own with 128-row work units.
+ * D       : head dimension; 32, 64, 96, 128, 256, 512 or 1024. 64 and 128
+ *           are the native tile widths; 32 and 96 run in the tiles of 64 and
+ *           128, whose columns past D the kernel reads as zeros. These four
+ *           are the head dims the split-Q launcher of "FlashAttention-2 MMA
+ *           代码学习" dispatches (its host function at the end of the page).
+ *           256, 512 and 1024 are the tiling_qk page's larger ones: 256 runs
+ *           on a kernel of its own with 128-row work units; 512 and 1024 tile
+ *           the output's head dimension, a work unit being 128 query rows and
+ *           one 256-column chunk of O, each recomputing the scores over all
+ *           of D (the tensor cores do 1.5x / 2.5x the FLOPs of the
+ *           definition). 512 and 1024 always run the round schedule.
  * scale   : multiplier on Q.K; finite and > 0 (the usual value is 1/sqrt(D)).
  * is_causal: nonzero keeps only keys j <= i for query i.
  * dtype   : FA2_F16 or FA2_BF16.
@@ -97,10 +101,10 @@ FA2_API int fa2_fwd(const void* Q, const void* K, const void* V, void* O, float*
 
 /*
  * fa2_fwd_workspace_bytes — bytes of device workspace fa2_fwd_ws needs on the
- * current device for head dimension D (32, 64, 96, 128 or 256): one fp32
- * partial result of a work unit per SM (256 rows, or 128 at head dim 256)
- * plus one 8-byte flag per 128-row sub-tile. It does
- * not depend on B, H or N. Returns FA2_OK, FA2_ERR_INVALID_ARG (bytes NULL),
+ * current device for head dimension D (32, 64, 96, 128, 256, 512 or 1024):
+ * one fp32 partial result of a work unit per SM (256 rows, or 128 at head
+ * dim 256) plus one 8-byte flag per 128-row sub-tile; 0 at head dims 512 and
+ * 1024, which run the round schedule only. It does not depend on B, H or N. Returns FA2_OK, FA2_ERR_INVALID_ARG (bytes NULL),
  * FA2_ERR_UNSUPPORTED (D) or FA2_ERR_CUDA.
  */
 FA2_API int fa2_fwd_workspace_bytes(int D, size_t* bytes);
@@ -112,7 +116,8 @@ FA2_API int fa2_fwd_workspace_bytes(int D, size_t* bytes);
  * (query tile, K/V tile) steps, and a query tile whose K/V range is cut
  * between CTAs is finished by merging fp32 partial results with the online
  * (m, l) rule of "FlashAttention-2 MMA 代码学习", step 1 (the merge the
- * pages apply across K/V blocks, here applied across CTAs).
+ * pages apply across K/V blocks, here applied across CTAs). At head dims
+ * 512 and 1024 it runs the round schedule of fa2_fwd (the workspace unused).
  *
  * workspace: NULL (then this is exactly fa2_fwd), or a 16-byte aligned
  *   device buffer of at least fa2_fwd_workspace_bytes(D) bytes that overlaps
@@ -131,7 +136,7 @@ FA2_API int fa2_fwd_ws(const void* Q, const void* K, const void* V, void* O, flo
  * fa2_fwd_sched — the same operation, arguments and results as fa2_fwd, with
  * the work schedule chosen by the caller or by the library:
  *   FA2_SCHED_UNITS: the round schedule of fa2_fwd (whole 256-row query
- *     units, 128-row at head dim 256, dealt to persistent CTAs in rounds;
+ *     units, 128-row from head dim 256, dealt to persistent CTAs in rounds;
  *     heaviest first in a zig-zag when causal). `workspace` may be NULL.
  *   FA2_SCHED_BALANCED: the stream-K schedule of fa2_fwd_ws; `workspace`
  *     (as described there) is required, except at head dims 512 and 1024,
