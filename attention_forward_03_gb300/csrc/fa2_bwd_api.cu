@@ -24,7 +24,7 @@ constexpr int kElemBlocksPerSm = 8;
 
 size_t round256(size_t x) { return (x + 255) / 256 * 256; }
 
-// Workspace: dQ accumulator | LSE*log2(e) | Delta (rows padded to a multiple
+// Workspace: dQ accumulator | -LSE*log2(e) | Delta (rows padded to a multiple
 // of the step rows) | stream-K partial dV, dK
 // (one [2][D][128] fp32 slot per CTA, kBwdMaxCtas slots) | their flags.
 struct BwdWorkspace {
@@ -95,7 +95,8 @@ __device__ __forceinline__ uint32_t pack_pair(float lo, float hi, bool bf16) {
 }
 
 // Per row (b, h, i) of the padded [B*H, Npad] grid: Delta_i = <dO_i, O_i>
-// and LSE_i * log2(e) (rows >= N: 0 and +inf, so the main kernel's P is 0
+// and -LSE_i * log2(e), the offset the main kernel adds to S * scale*log2(e)
+// with one packed FMA per two scores (rows >= N: 0 and -inf, so that P is 0
 // there), and zeroes the row of the fp32 dQ accumulator. D/8 threads per
 // row, 8 elements (16 bytes) each, in groups of kLanes (D/8 rounded up to a
 // power of two: the shuffle reduction's width; the extra lanes add zero);
@@ -104,7 +105,7 @@ template <int D, bool kBf16>
 __global__ void __launch_bounds__(kElemThreads) fa2_bwd_prologue(const uint4* __restrict__ O,
                                                                  const uint4* __restrict__ dO,
                                                                  const float* __restrict__ LSE,
-                                                                 float* __restrict__ dq_acc, float* __restrict__ lse2,
+                                                                 float* __restrict__ dq_acc, float* __restrict__ neg_lse2,
                                                                  float* __restrict__ delta, int N, int Npad,
                                                                  long long rows) {
   constexpr int kPer = D / 8;  // threads with data per row
@@ -137,7 +138,7 @@ __global__ void __launch_bounds__(kElemThreads) fa2_bwd_prologue(const uint4* __
     if (live && part == 0) {
       const bool in_range = i < N;
       delta[row] = in_range ? acc : 0.f;
-      lse2[row] = in_range ? LSE[bh * N + i] * 1.4426950408889634f : CUDART_INF_F;
+      neg_lse2[row] = in_range ? -(LSE[bh * N + i] * 1.4426950408889634f) : -CUDART_INF_F;
     }
   }
 }
@@ -175,14 +176,14 @@ BwdLaunchFn pick_bwd(int d, int dtype, int causal) {
 }
 
 template <int D>
-cudaError_t launch_prologue(bool bf16, const void* O, const void* dO, const float* LSE, float* dq_acc, float* lse2,
+cudaError_t launch_prologue(bool bf16, const void* O, const void* dO, const float* LSE, float* dq_acc, float* neg_lse2,
                             float* delta, int N, int Npad, long long rows, int grid, cudaStream_t s) {
   const uint4* o = static_cast<const uint4*>(O);
   const uint4* g = static_cast<const uint4*>(dO);
   if (bf16)
-    fa2_bwd_prologue<D, true><<<grid, kElemThreads, 0, s>>>(o, g, LSE, dq_acc, lse2, delta, N, Npad, rows);
+    fa2_bwd_prologue<D, true><<<grid, kElemThreads, 0, s>>>(o, g, LSE, dq_acc, neg_lse2, delta, N, Npad, rows);
   else
-    fa2_bwd_prologue<D, false><<<grid, kElemThreads, 0, s>>>(o, g, LSE, dq_acc, lse2, delta, N, Npad, rows);
+    fa2_bwd_prologue<D, false><<<grid, kElemThreads, 0, s>>>(o, g, LSE, dq_acc, neg_lse2, delta, N, Npad, rows);
   return cudaGetLastError();
 }
 
@@ -259,7 +260,7 @@ extern "C" int fa2_bwd_sched(const void* Q, const void* K, const void* V, const 
   float* dq_acc = reinterpret_cast<float*>(ws);
   CUtensorMap mdq;  // the kernel adds blocks of 32 rows of dQ into the accumulator
   if (!encode_f32_rows_map(&mdq, dq_acc, (int)bh, N, D, 32)) return record_cuda_error(cudaErrorInvalidValue);
-  float* lse2 = reinterpret_cast<float*>(ws + wl.dq_bytes);
+  float* neg_lse2 = reinterpret_cast<float*>(ws + wl.dq_bytes);
   float* delta = reinterpret_cast<float*>(ws + wl.dq_bytes + wl.stat_bytes);
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   const bool bf = dtype == FA2_BF16;
@@ -268,10 +269,10 @@ extern "C" int fa2_bwd_sched(const void* Q, const void* K, const void* V, const 
   const int pgrid = grid_for(rows * (D / 8), sms);
   cudaError_t e;
   switch (D) {
-    case 32: e = launch_prologue<32>(bf, O, dO, LSE, dq_acc, lse2, delta, N, npad, rows, pgrid, s); break;
-    case 64: e = launch_prologue<64>(bf, O, dO, LSE, dq_acc, lse2, delta, N, npad, rows, pgrid, s); break;
-    case 96: e = launch_prologue<96>(bf, O, dO, LSE, dq_acc, lse2, delta, N, npad, rows, pgrid, s); break;
-    default: e = launch_prologue<128>(bf, O, dO, LSE, dq_acc, lse2, delta, N, npad, rows, pgrid, s); break;
+    case 32: e = launch_prologue<32>(bf, O, dO, LSE, dq_acc, neg_lse2, delta, N, npad, rows, pgrid, s); break;
+    case 64: e = launch_prologue<64>(bf, O, dO, LSE, dq_acc, neg_lse2, delta, N, npad, rows, pgrid, s); break;
+    case 96: e = launch_prologue<96>(bf, O, dO, LSE, dq_acc, neg_lse2, delta, N, npad, rows, pgrid, s); break;
+    default: e = launch_prologue<128>(bf, O, dO, LSE, dq_acc, neg_lse2, delta, N, npad, rows, pgrid, s); break;
   }
   if (e != cudaSuccess) return record_cuda_error(e);
 
@@ -279,7 +280,7 @@ extern "C" int fa2_bwd_sched(const void* Q, const void* K, const void* V, const 
   p.dk = dK;
   p.dv = dV;
   p.dq_acc = dq_acc;
-  p.lse2 = lse2;
+  p.neg_lse2 = neg_lse2;
   p.delta = delta;
   p.status = status;
   p.watchdog_ns = watchdog_limit_ns();

@@ -43,7 +43,7 @@
 //                   runs with M = 128 and the lanes from D on are discarded)
 // Shared memory (128-byte swizzled, 64-element panels): K and V of the tile
 // (resident for the unit), a ring of query steps (Q_i, dO_i, and the 64
-// LSE*log2(e) and Delta values), the 16-bit P^T and dS^T of the step
+// -LSE*log2(e) and Delta values), the 16-bit P^T and dS^T of the step
 // (written by the compute threads, read by the tensor core), and an fp32
 // staging tile for dQ (64 rows x D) that TMA reduce-adds into the global
 // accumulator, 32 rows per compute warpgroup.
@@ -114,7 +114,7 @@ struct BwdLayout {
   static constexpr int kQPanelBytes = kSR * 128;              // SR rows x 64 16-bit elements
   static constexpr int kQBytes = kPanels * kQPanelBytes;      // Q or dO step: SR rows x Dp
   static constexpr int kPTileBytes = (kSR / 64) * kPanelBytes;  // P^T or dS^T: 128 keys x SR queries
-  static constexpr int kStatBytes = 2 * kSR * 4;              // LSE*log2(e) and Delta of one step
+  static constexpr int kStatBytes = 2 * kSR * 4;              // -LSE*log2(e) and Delta of one step
   static constexpr int kStages = (kSR == 128) ? 2 : (kPanels == 2 ? 3 : 6);
   // Epilogue: a key row's D columns in chunks of 32, the first kChunksWg for
   // compute warpgroup 0 and the rest for warpgroup 1.
@@ -347,7 +347,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
   if (warp == kBwdLoadWarp) {
     // ------------------------------------------------------------ producer
     // Per unit: K and V of the tile once, then every query step (Q_i, dO_i
-    // and their 64 LSE*log2(e) / Delta values) through the ring.
+    // and their 64 -LSE*log2(e) / Delta values) through the ring.
     if (lane == 0) {
       tma_prefetch_map(&tmK);
       tma_prefetch_map(&tmV);
@@ -389,7 +389,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           }
           const size_t off = static_cast<size_t>(bh) * p.Npad + static_cast<size_t>(i) * L::kSR;
           const uint32_t sst = sStats + static_cast<uint32_t>(slot * L::kStatBytes);
-          bulk_load(sst, p.lse2 + off, L::kSR * 4, full);
+          bulk_load(sst, p.neg_lse2 + off, L::kSR * 4, full);
           bulk_load(sst + L::kSR * 4, p.delta + off, L::kSR * 4, full);
           ++loads;
           if (++slot == L::kStages) {
@@ -721,37 +721,46 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
           break;
         }
         tc_fence_after_sync();
-        const float* lse2_step = stats + slot * (L::kStatBytes / 4) + L::kCW * wg;
-        const float* delta_step = lse2_step + L::kSR;
+        const float* neg_lse2_step = stats + slot * (L::kStatBytes / 4) + L::kCW * wg;
+        const float* delta_step = neg_lse2_step + L::kSR;
         bool fr = true;
 #pragma unroll
         for (int h = 0; h < L::kHalves; ++h) {
           uint32_t sr[32], dpr[32];
-          tmem_ld32x32_wait(tS + 32u * h, sr);
-          tmem_ld32x32_wait(tDP + 32u * h, dpr);
+          tmem_ld32x32_nowait(tS + 32u * h, sr);
+          tmem_ld32x32_nowait(tDP + 32u * h, dpr);
+          tmem_wait_ld2(sr, dpr);
           if (h == L::kHalves - 1) {
             // S^T and dP^T are in registers: the issuer may compute the next ones.
             tc_fence_before_sync();
             mbar_arrive(bar_s_free);
           }
-          const float* lse2 = lse2_step + 32 * h;
-          const float* delta = delta_step + 32 * h;
+          // the step's -LSE*log2(e) and Delta values of these 32 query columns
+          const float4* nl4 = reinterpret_cast<const float4*>(neg_lse2_step + 32 * h);
+          const float4* dl4 = reinterpret_cast<const float4*>(delta_step + 32 * h);
           const int q0 = i * L::kSR + L::kCW * wg + 32 * h;  // query row of this thread's first column
           // masked: keys past N (ragged last tile) and, causal, keys after the query
           const bool masked = !key_ok || (kCausal && key > q0);
           uint32_t pk[16], dk[16];
 #pragma unroll
-          for (int j = 0; j < 32; j += 2) {
-            float p0 = ex2_approx(__uint_as_float(sr[j]) * c - lse2[j]);
-            float p1 = ex2_approx(__uint_as_float(sr[j + 1]) * c - lse2[j + 1]);
-            if (masked) {
-              if (!key_ok || key > q0 + j) p0 = 0.f;
-              if (!key_ok || key > q0 + j + 1) p1 = 0.f;
+          for (int j = 0; j < 32; j += 4) {
+            const float4 nl = nl4[j / 4];
+            const float4 dl = dl4[j / 4];
+            float e[4], pr[4], ds[4];
+            ffma2(e[0], e[1], __uint_as_float(sr[j]), __uint_as_float(sr[j + 1]), c, nl.x, nl.y);
+            ffma2(e[2], e[3], __uint_as_float(sr[j + 2]), __uint_as_float(sr[j + 3]), c, nl.z, nl.w);
+#pragma unroll
+            for (int t = 0; t < 4; ++t) {
+              pr[t] = ex2_approx(e[t]);
+              if (masked && (!key_ok || key > q0 + j + t)) pr[t] = 0.f;
             }
-            const float d0 = p0 * (__uint_as_float(dpr[j]) - delta[j]);
-            const float d1 = p1 * (__uint_as_float(dpr[j + 1]) - delta[j + 1]);
-            pk[j / 2] = pack2(p0, p1, kBf16);
-            dk[j / 2] = pack2(d0, d1, kBf16);
+            fmul_sub2(ds[0], ds[1], pr[0], pr[1], __uint_as_float(dpr[j]), __uint_as_float(dpr[j + 1]), dl.x, dl.y);
+            fmul_sub2(ds[2], ds[3], pr[2], pr[3], __uint_as_float(dpr[j + 2]), __uint_as_float(dpr[j + 3]), dl.z,
+                      dl.w);
+            pk[j / 2] = pack2(pr[0], pr[1], kBf16);
+            pk[j / 2 + 1] = pack2(pr[2], pr[3], kBf16);
+            dk[j / 2] = pack2(ds[0], ds[1], kBf16);
+            dk[j / 2 + 1] = pack2(ds[2], ds[3], kBf16);
           }
           // the previous step's P^T / dS^T must have been read by the tensor core
           if (h == 0 && g > 0) {

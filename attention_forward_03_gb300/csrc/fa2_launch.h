@@ -92,7 +92,7 @@ struct BwdParams {
   void* dv;
   float* dq_acc;            // [B,H,N,D] fp32 dQ accumulator (zeroed by the prologue kernel; the
                             // kernel adds into it through a tensor map)
-  const float* lse2;        // [B*H, Npad] LSE * log2(e); +inf for rows >= N
+  const float* neg_lse2;    // [B*H, Npad] -LSE * log2(e) (the exponent's offset); -inf for rows >= N
   const float* delta;       // [B*H, Npad] <dO_i, O_i>; 0 for rows >= N
   int* status;              // device watchdog word
   unsigned long long watchdog_ns;

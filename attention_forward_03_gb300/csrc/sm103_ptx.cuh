@@ -251,6 +251,37 @@ __device__ __forceinline__ void ffma2_bcast(float& d0, float& d1, float a0, floa
       : "f"(a0), "f"(a1), "f"(b), "f"(c));
 }
 
+// (d0, d1) = (a0, a1) * (b, b) + (c0, c1) as one packed f32x2 FMA
+__device__ __forceinline__ void ffma2(float& d0, float& d1, float a0, float a1, float b, float c0, float c1) {
+  asm("{\n"
+      ".reg .b64 A, B, C, D;\n"
+      "mov.b64 A, {%2, %3};\n"
+      "mov.b64 B, {%4, %4};\n"
+      "mov.b64 C, {%5, %6};\n"
+      "fma.rn.f32x2 D, A, B, C;\n"
+      "mov.b64 {%0, %1}, D;\n"
+      "}\n"
+      : "=f"(d0), "=f"(d1)
+      : "f"(a0), "f"(a1), "f"(b), "f"(c0), "f"(c1));
+}
+
+// (d0, d1) = (p0, p1) * ((x0, x1) - (y0, y1)): a packed f32x2 subtract,
+// then a packed multiply
+__device__ __forceinline__ void fmul_sub2(float& d0, float& d1, float p0, float p1, float x0, float x1, float y0,
+                                          float y1) {
+  asm("{\n"
+      ".reg .b64 P, X, Y, D;\n"
+      "mov.b64 P, {%2, %3};\n"
+      "mov.b64 X, {%4, %5};\n"
+      "mov.b64 Y, {%6, %7};\n"
+      "sub.rn.f32x2 D, X, Y;\n"
+      "mul.rn.f32x2 D, P, D;\n"
+      "mov.b64 {%0, %1}, D;\n"
+      "}\n"
+      : "=f"(d0), "=f"(d1)
+      : "f"(p0), "f"(p1), "f"(x0), "f"(x1), "f"(y0), "f"(y1));
+}
+
 // (s0, s1) += (a0, a1) as one packed f32x2 add
 __device__ __forceinline__ void fadd2_acc(float& s0, float& s1, float a0, float a1) {
   asm("{\n"
