@@ -374,7 +374,9 @@ def attention_forward_host(q, k, v, scale: float | None = None, is_causal: bool 
     forward pass runs there and O, LSE are copied back into `out` / `lse`
     (allocated in page-locked memory when not given), chunk by chunk so that
     the copies overlap the kernels. Page-locked inputs are needed for the
-    copies to overlap. With synchronize=False the call returns once the work
+    copies to overlap. Q, K, V given as the three slices of one packed
+    [3, B, H, N, D] buffer take one copy per chunk instead of three, and a
+    page-locked `lse` is written by the kernels in place (no copy). With synchronize=False the call returns once the work
     is enqueued on `stream`; the results are valid after that stream is
     synchronised.
     schedule: "auto" (choose_schedule applied to one chunk), "balanced" or "units".

@@ -227,6 +227,15 @@ FA2_API int fa2_fwd_host_buffer_bytes(int B, int H, int N, int D, size_t* bytes)
  *           other. Page-locked memory (cudaHostAlloc / cudaHostRegister) is
  *           needed for the copies to overlap anything; pageable memory works
  *           but the copies then run one after another.
+ * Copies  : each copy costs the copy engine a few microseconds besides its
+ *           bytes, so the call makes as few as the layout allows. When K
+ *           and V follow Q at one fixed spacing (three slices of one packed
+ *           [3, B, H, N, D] buffer, for one), each chunk's Q, K and V move in
+ *           one two-dimensional copy, else in three. When the device can
+ *           address LSE directly (page-locked memory under unified
+ *           addressing; cudaPointerGetAttributes gives its device pointer)
+ *           and N is a multiple of 4, the kernels write LSE there and no LSE
+ *           copy is made. Either way the results are the same.
  * B, H, N, D, scale, is_causal, dtype: as fa2_fwd.
  * heads_per_chunk: heads (of the flattened B*H) per chunk; 0 = ceil(B*H / 4).
  *           The first chunk holds half as many (rounded down, at least one)

@@ -76,6 +76,32 @@ def test_round_schedule_equals_device_entry_point_bit_for_bit(fa2):
         assert torch.equal(O, Od.cpu()) and torch.equal(L, Ld.cpu()), f"heads_per_chunk={hpc}"
 
 
+@pytest.mark.parametrize("N", [300, 301])
+def test_packed_qkv_and_direct_lse_equal_the_copy_path(fa2, oracle_mod, N):
+    # Q, K, V as slices of one page-locked [3, B, H, N, D] buffer take one 2-D
+    # copy per chunk; page-locked LSE with N % 4 == 0 is written by the
+    # kernels in place. The reference run uses unequally spaced inputs (slices
+    # 0, 1 and 3 of a 4-slice buffer) and pageable LSE, the copy path. Same
+    # kernels on the same chunks: equal bit for bit.
+    w = workloads.custom(2, 3, N, 128, "bf16", False, seed=45)
+    q, k, v = workloads.make_inputs(w)
+    packed = torch.empty((3, *q.shape), dtype=q.dtype).pin_memory()
+    spread = torch.empty((4, *q.shape), dtype=q.dtype).pin_memory()
+    for i, t in enumerate((q, k, v)):
+        packed[i].copy_(t)
+        spread[(0, 1, 3)[i]].copy_(t)
+    for hpc in (1, 2, None):
+        lse_pinned = torch.empty((w.B, w.H, w.N), dtype=torch.float32).pin_memory()
+        O1, L1 = fa2.attention_forward_host(packed[0], packed[1], packed[2], scale=w.scale, lse=lse_pinned,
+                                            heads_per_chunk=hpc, schedule="units")
+        lse_pageable = torch.empty((w.B, w.H, w.N), dtype=torch.float32)
+        O2, L2 = fa2.attention_forward_host(spread[0], spread[1], spread[3], scale=w.scale, lse=lse_pageable,
+                                            heads_per_chunk=hpc, schedule="units")
+        assert fa2.fa2_device_status(clear=True) == 0
+        assert torch.equal(O1, O2) and torch.equal(L1, L2), f"heads_per_chunk={hpc}"
+    check_against_oracle(oracle_mod, w, q, k, v, O1, L1)
+
+
 def test_pageable_host_memory_and_side_stream(fa2, oracle_mod):
     w = workloads.custom(1, 3, 257, 64, "bf16", False, seed=44)
     q, k, v = workloads.make_inputs(w)  # pageable
