@@ -34,6 +34,8 @@
 //              current step's gradients), where with sleeping waits they had
 //              measured 1 % slower.
 //   warp  10   TMA producer (one thread)
+//   warp  11   (D = 96, 128) two threads that add the compute warpgroups'
+//              staged dQ^T rows into the accumulator with TMA reduce-adds
 // Head dims 32 and 96 run in the tiles of 64 and 128 (Dp below): their
 // columns past D arrive as zeros from the copy engine, so they add nothing.
 // Tensor memory (fp32 columns x 128 lanes):
@@ -65,10 +67,17 @@
 
 namespace fa2 {
 
-constexpr int kBwdThreads = 352;    // 11 warps
+// 11 warps, and at D = 96, 128 a twelfth (see kBwdDqWarp)
+constexpr int bwd_threads(int d) { return d > 64 ? 384 : 352; }
 constexpr int kBwdMmaWarp = 8;      // MMA issuer (all products, or S^T / dP^T); owns the TMEM allocation
 constexpr int kBwdGradWarp = 9;     // second MMA issuer (dV, dK, dQ^T)
 constexpr int kBwdLoadWarp = 10;
+// D = 96, 128: two lanes of this warp add the compute warpgroups' staged
+// dQ^T rows into the accumulator (a TMA reduce-add per 32 rows) and give
+// the rows back once the copy engine has read them. At D <= 64 each
+// warpgroup's first thread does it (measured: the extra warp is +1 to +6 %
+// at D = 96, 128 and -2 % at D = 64).
+constexpr int kBwdDqWarp = 11;
 constexpr int kBwdComputeThreads = 256;
 
 enum : int {
@@ -259,13 +268,14 @@ __device__ __forceinline__ bool bwd_next_segment(BwdCursor& c, BwdSegment& s, co
 }
 
 template <int D, bool kBf16, bool kCausal>
-__global__ void __launch_bounds__(kBwdThreads, 1)
+__global__ void __launch_bounds__(bwd_threads(D), 1)
     fa2_bwd_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                    const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmDO,
                    const __grid_constant__ CUtensorMap tmDQ, const BwdParams p) {
   using L = BwdLayout<D>;
   constexpr bool kTwoIssuers = true;
   constexpr bool kATmem = L::kGradATmem;  // P^T, dS^T in TMEM for dV, dK
+  constexpr bool kDqWarp = bwd_threads(D) > 352;  // staged dQ^T added by warp kBwdDqWarp
   constexpr uint32_t kReaders = kTwoIssuers ? 2 : 1;  // issuer threads reading a ring slot and K/V
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   const uint32_t raw = smem_addr(smem_raw);
@@ -646,10 +656,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     // dQ^T of global step `step` (head pend_bh, rows pend_q0 + kCW*wg +
     // [0, kCW)) from TMEM into the fp32 accumulator: this thread holds
     // head-dim index rr of those query rows. The warpgroup writes them into
-    // its kCW x D staging rows (row-major, the accumulator's layout) and its
-    // leader thread adds each block of 32 rows into global memory with one
-    // TMA reduce-add; the staging rows are rewritten once those TMAs have
-    // read them.
+    // its kCW x D staging rows (row-major, the accumulator's layout); each
+    // block of 32 rows is added into global memory by one TMA reduce-add,
+    // issued by the warpgroup's first thread (D <= 64) or by a lane of warp
+    // kBwdDqWarp (D = 96, 128); the staging rows are rewritten once those
+    // TMAs have read them.
     const bool leader = (threadIdx.x & 127) == 0;
     const uint32_t stage_rows = sDQS + static_cast<uint32_t>(wg * L::kCW * D * 4);
     uint32_t drains = 0;
@@ -668,7 +679,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       mbar_arrive(bar_dq_free);
       // the staging rows must have been read by the previous step's TMAs
       if (drains > 0) {
-        if (leader) {
+        if (!kDqWarp && leader) {
           bulk_wait_read_all();
           mbar_arrive(bar_dqs_free(wg));
         }
@@ -688,6 +699,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
       }
       fence_proxy_async_shared();
       mbar_arrive(bar_dqs_ready(wg));
+      if constexpr (kDqWarp) {
+        ++drains;
+        return true;
+      }
       if (quarter == 0) {  // the leader's warp waits as a whole, so its lanes agree on the outcome
         bool rd = wait_bounded(bar_dqs_ready(wg), drains & 1u, wd, kSiteBwdDqsReady);
         rd = __all_sync(0xffffffffu, rd);
@@ -935,7 +950,40 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     // the last step's dQ^T; the staged blocks must be read (and added)
     // before the CTA's shared memory goes away
     if (ok && g > 0) drain_dq(g - 1);
-    if (leader) bulk_wait_all();
+    if (!kDqWarp && leader) bulk_wait_all();
+  } else if (kDqWarp && warp == kBwdDqWarp) {
+    // ------------------------------------------------------------- dQ adds
+    // Lane w serves compute warpgroup w, walking the steps in the order
+    // every role does: once the warpgroup has staged a step's dQ^T rows, one
+    // TMA reduce-add per 32 rows into the fp32 accumulator; once the copy
+    // engine has read them, the rows are given back. It polls without
+    // sleeping.
+    if (lane < 2) {
+      const int w = lane;
+      const uint32_t rows = sDQS + static_cast<uint32_t>(w * L::kCW * D * 4);
+      uint32_t k = 0;  // steps whose rows were added
+      bool ok = true;
+      BwdCursor cur = bwd_first_cursor(p);
+      BwdSegment sg;
+      while (ok && bwd_next_segment<kCausal, L::kR>(cur, sg, p)) {
+        for (int i = sg.i_begin; i < sg.i_end; ++i, ++k) {
+          ok = wait_bounded(bar_dqs_ready(w), k & 1u, wd, kSiteBwdDqsReady, true, 0u);
+          if (!ok) break;
+#pragma unroll
+          for (int h = 0; h < L::kHalves; ++h) {
+            const int q0 = i * L::kSR + L::kCW * w + 32 * h;
+            if (q0 < p.N)  // rows past N are outside the map and skipped
+              tma_reduce_add_3d(&tmDQ, rows + static_cast<uint32_t>(32 * h * D * 4), 0, q0, sg.bh);
+          }
+          bulk_commit_group();
+          bulk_wait_read_all();
+          mbar_arrive(bar_dqs_free(w));
+        }
+      }
+      // the adds in flight complete before the CTA's shared memory goes away
+      bulk_wait_all();
+    }
+    __syncwarp();
   }
 
   tc_fence_before_sync();
@@ -960,7 +1008,7 @@ cudaError_t launch_bwd(const CUtensorMap& k, const CUtensorMap& v, const CUtenso
   // (the whole grid resident at once, or the launch fails).
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
-  cfg.blockDim = dim3(kBwdThreads);
+  cfg.blockDim = dim3(bwd_threads(D));
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
