@@ -200,7 +200,7 @@ extern "C" int fa2_fwd_host(const void* Q, const void* K, const void* V, void* O
     if (packed) {
       // rows Q, K, V of the chunk: host pitch = their spacing, device pitch = L.k
       e = cudaMemcpy2DAsync(dq + off, L.k, hq + off, uk - uq, n, 3, cudaMemcpyHostToDevice, pp.in);
-      if (e == cudaErrorInvalidValue) {
+      if (e == cudaErrorInvalidValue || e == cudaErrorInvalidPitchValue) {
         cudaGetLastError();
         packed = false;
       }
