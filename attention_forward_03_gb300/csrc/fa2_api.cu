@@ -346,6 +346,21 @@ bool encode_tile_map(CUtensorMap* map, const void* ptr, int bh, int n, int d, in
   return make_rows_map(map, ptr, bh, n, d, dtype, rows);
 }
 
+bool encode_f32_cols_map_sw128(CUtensorMap* map, float* ptr, int bh, int n, int d, unsigned rows) {
+  return cached_map(map, MapKey{ptr, bh, n, d, 17, rows}, [&](CUtensorMap* m) {
+    EncodeTiledFn enc = encode_fn();
+    if (!enc) return false;
+    cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)n, (cuuint64_t)bh};
+    cuuint64_t strides[2] = {(cuuint64_t)d * 4, (cuuint64_t)n * d * 4};
+    cuuint32_t box[3] = {32, rows, 1};
+    cuuint32_t estride[3] = {1, 1, 1};
+    CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, ptr, dims, strides, box, estride,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+  });
+}
+
 bool encode_f32_rows_map(CUtensorMap* map, float* ptr, int bh, int n, int d, unsigned rows) {
   return cached_map(map, MapKey{ptr, bh, n, d, 16, rows}, [&](CUtensorMap* m) {
     EncodeTiledFn enc = encode_fn();

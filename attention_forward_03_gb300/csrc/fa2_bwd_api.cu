@@ -259,7 +259,9 @@ extern "C" int fa2_bwd_sched(const void* Q, const void* K, const void* V, const 
   char* ws = static_cast<char*>(workspace);
   float* dq_acc = reinterpret_cast<float*>(ws);
   CUtensorMap mdq;  // the kernel adds blocks of 32 rows of dQ into the accumulator
-  if (!encode_f32_rows_map(&mdq, dq_acc, (int)bh, N, D, 32)) return record_cuda_error(cudaErrorInvalidValue);
+  const bool mapped = D <= 64 ? encode_f32_cols_map_sw128(&mdq, dq_acc, (int)bh, N, D, 128)
+                              : encode_f32_rows_map(&mdq, dq_acc, (int)bh, N, D, 32);
+  if (!mapped) return record_cuda_error(cudaErrorInvalidValue);
   float* neg_lse2 = reinterpret_cast<float*>(ws + wl.dq_bytes);
   float* delta = reinterpret_cast<float*>(ws + wl.dq_bytes + wl.stat_bytes);
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);

@@ -40,15 +40,18 @@
 // columns past D arrive as zeros from the copy engine, so they add nothing.
 // Tensor memory (fp32 columns x 128 lanes):
 //   [0, D)          dV accumulator        [Dp, Dp+D)     dK accumulator
-//   [2Dp, 2Dp+64)   S^T of the step       [2Dp+64, 2Dp+128) dP^T of the step
-//   [2Dp+128, 2Dp+192) dQ^T of the step (lane = head-dim index; the MMA
-//                   runs with M = 128 and the lanes from D on are discarded)
+//   [2Dp, 2Dp+SR)   S^T of the step       [2Dp+SR, 2Dp+2SR) dP^T of the step
+//   [2Dp+2SR, ...)  Dp = 128: dQ^T of the step (lane = head-dim index; the
+//                   MMA runs with M = 128 and the lanes from D on are
+//                   discarded); Dp = 64: dQ of the step, untransposed (lane =
+//                   query row, 64 columns)
 // Shared memory (128-byte swizzled, 64-element panels): K and V of the tile
 // (resident for the unit), a ring of query steps (Q_i, dO_i, and the 64
 // -LSE*log2(e) and Delta values), the 16-bit P^T and dS^T of the step
 // (written by the compute threads, read by the tensor core), and an fp32
-// staging tile for dQ (64 rows x D) that TMA reduce-adds into the global
-// accumulator, 32 rows per compute warpgroup.
+// staging tile for dQ that TMA reduce-adds into the global accumulator: at
+// Dp = 128 SR rows x D, 32 rows per compute warpgroup and reduce-add; at
+// Dp = 64 SR rows x 32 columns per warpgroup, 128-byte swizzled.
 //
 // Schedules: whole units dealt to the CTAs in rounds (zig-zag when causal),
 // or stream-K: every CTA takes an equal share of all query steps, so a unit
@@ -159,6 +162,14 @@ struct BwdLayout {
   // non-sleeping issuers, +1 to +2 % on causal launches too (with one
   // issuer it had been -2.4 % on long causal rows).
   static constexpr bool kGradATmem = (kSR == 64);
+  // At Dp = 64 the step's dQ is computed untransposed, dQ = dS K (M = the
+  // 128 query rows, N = 64): the rows fill all 128 TMEM lanes, so every
+  // compute warp stages a share (32 columns per warpgroup, 16-byte stores
+  // into 128-byte-swizzled rows that one TMA reduce-add per warpgroup reads),
+  // and an N = 64 product takes 8 x ~47 cycles against 8 x 64 for dQ^T's
+  // N = 128. dQ^T (lanes = head-dim index) puts only D of the 128 lanes to
+  // use, so half the warps staged everything.
+  static constexpr bool kDqRows = (kDp == 64);
   static constexpr uint32_t kColPT = kColDQ + kSR;
   static constexpr uint32_t kColDST = kColPT + kSR / 2;
   static_assert(!kGradATmem || kColDST + kSR / 2 <= kTmemCols, "TMEM budget");
@@ -425,6 +436,7 @@ __global__ void __launch_bounds__(bwd_threads(D), 1)
       constexpr uint32_t idesc_s = make_idesc_f16(kBf16, L::kSR, false);              // S^T, dP^T: N = SR
       constexpr uint32_t idesc_acc = make_idesc_f16(kBf16, L::kNacc, true);           // dV, dK: N = D (64 at D = 32)
       constexpr uint32_t idesc_dq = make_idesc_f16_ab(kBf16, L::kSR, true, true);     // dQ^T: N = SR
+      constexpr uint32_t idesc_dqr = make_idesc_f16_ab(kBf16, L::kNacc, true, true);  // dQ (Dp = 64): N = 64
       constexpr uint32_t kHi = desc_hi_sw128(1024);  // 8-row (K-major) / 8-row-of-K (MN-major) groups 1 KB apart
       // S^T = K Q_i^T and dP^T = V dO_i^T: A = K / V (K-major, 128-row
       // panels), B = Q_i / dO_i (K-major, SR-row panels), N = SR, D/16 steps.
@@ -485,7 +497,10 @@ __global__ void __launch_bounds__(bwd_threads(D), 1)
 #pragma unroll
         for (int kk = 0; kk < kBwdKeys / 16; ++kk) {
           const uint32_t off = static_cast<uint32_t>((kk * 16 * 128) >> 4);
-          mma_ss_w(tmem + L::kColDQ, kt_lo + off, kHi, ds_mn + off, kHi, idesc_dq, kk > 0 ? 1u : 0u);
+          if constexpr (L::kDqRows)  // dQ = dS K: A = dS^T's rows read MN-major (M = queries), B = K MN-major
+            mma_ss_w(tmem + L::kColDQ, ds_mn + off, kHi, kt_lo + off, kHi, idesc_dqr, kk > 0 ? 1u : 0u);
+          else
+            mma_ss_w(tmem + L::kColDQ, kt_lo + off, kHi, ds_mn + off, kHi, idesc_dq, kk > 0 ? 1u : 0u);
         }
       };
 
@@ -669,6 +684,46 @@ __global__ void __launch_bounds__(bwd_threads(D), 1)
       got = __all_sync(0xffffffffu, got);
       if (!got) return false;
       tc_fence_after_sync();
+      if constexpr (L::kDqRows) {
+        // this thread's query row (TMEM lane rr) of dQ, columns [32 wg, 32 wg + 32)
+        uint32_t v[32];
+        tmem_ld32x32_wait(tmem + lane_off + L::kColDQ + 32u * wg, v);
+        tc_fence_before_sync();
+        mbar_arrive(bar_dq_free);
+        if (drains > 0) {
+          if (leader) {
+            bulk_wait_read_all();
+            mbar_arrive(bar_dqs_free(wg));
+          }
+          bool fr = wait_bounded(bar_dqs_free(wg), (drains - 1) & 1u, wd, kSiteBwdDqsFree);
+          fr = __all_sync(0xffffffffu, fr);
+          if (!fr) return false;
+        }
+        const bool has_cols = 32 * wg < D;  // warpgroup-uniform: at D = 32 the second half is padding
+        const uint32_t box = sDQS + static_cast<uint32_t>(wg * 128 * 32 * 4);
+        if (has_cols) {
+          // 8 chunks of 4 columns into this row of the box, 128-byte swizzled
+          const uint32_t row = box + static_cast<uint32_t>(rr * 128);
+#pragma unroll
+          for (int ch = 0; ch < 8; ++ch)
+            st_shared_v4(row + ((static_cast<uint32_t>(ch) ^ xr) << 4), v[4 * ch], v[4 * ch + 1], v[4 * ch + 2],
+                         v[4 * ch + 3]);
+        }
+        fence_proxy_async_shared();
+        mbar_arrive(bar_dqs_ready(wg));
+        if (quarter == 0) {  // the leader's warp waits as a whole, so its lanes agree on the outcome
+          bool rd = wait_bounded(bar_dqs_ready(wg), drains & 1u, wd, kSiteBwdDqsReady);
+          rd = __all_sync(0xffffffffu, rd);
+          if (!rd) return false;
+        }
+        if (leader) {
+          if (has_cols && pend_q0 < p.N)  // rows past N are outside the map and skipped
+            tma_reduce_add_3d(&tmDQ, box, 32 * wg, pend_q0, pend_bh);
+          bulk_commit_group();
+        }
+        ++drains;
+        return true;
+      }
       uint32_t v[L::kHalves][32];
       // every warp loads (lanes from D on hold the discarded rows; a load
       // guarded by dq_rows made the compiler spill at D = 32 and 96), only

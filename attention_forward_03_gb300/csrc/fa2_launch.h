@@ -167,6 +167,9 @@ bool encode_tile_map(CUtensorMap* map, const void* ptr, int bh, int n, int d, in
 unsigned long long watchdog_limit_ns();
 // fp32 [B*H, N, D] map with boxes of `rows` whole rows (D elements), no swizzle.
 bool encode_f32_rows_map(CUtensorMap* map, float* ptr, int bh, int n, int d, unsigned rows);
+// fp32 [bh][n][d] in boxes of 32 columns x `rows` rows, 128-byte swizzled in
+// shared memory (the backward's dQ staging at head dims up to 64).
+bool encode_f32_cols_map_sw128(CUtensorMap* map, float* ptr, int bh, int n, int d, unsigned rows);
 bool ranges_overlap(const void* a, size_t na, const void* b, size_t nb);
 
 template <int D, bool kBf16, bool kCausal>
