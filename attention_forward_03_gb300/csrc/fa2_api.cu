@@ -105,7 +105,7 @@ EncodeTiledFn encode_fn() {
 // guarded by one lock.
 struct MapKey {
   const void* ptr;
-  int bh, n, d, kind;  // kind: the 16-bit dtype code, or 16 for fp32 rows
+  int bh, n, d, kind;  // kind: the 16-bit dtype code, 16 for fp32 rows, 17 for fp32 swizzled column boxes
   unsigned rows;
   bool operator==(const MapKey& o) const {
     return ptr == o.ptr && bh == o.bh && n == o.n && d == o.d && kind == o.kind && rows == o.rows;
