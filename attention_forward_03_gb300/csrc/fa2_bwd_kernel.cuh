@@ -43,12 +43,14 @@
 //   [2Dp, 2Dp+SR)   S^T of the step       [2Dp+SR, 2Dp+2SR) dP^T of the step
 //   [2Dp+2SR, ...)  Dp = 128: dQ^T of the step (lane = head-dim index; the
 //                   MMA runs with M = 128 and the lanes from D on are
-//                   discarded); Dp = 64: dQ of the step, untransposed (lane =
-//                   query row, 64 columns)
+//                   discarded), then P^T and dS^T of the step (SR/2 packed
+//                   columns each); Dp = 64: dQ of the step, untransposed
+//                   (lane = query row, 64 columns), then P^T (64 packed
+//                   columns)
 // Shared memory (128-byte swizzled, 64-element panels): K and V of the tile
-// (resident for the unit), a ring of query steps (Q_i, dO_i, and the 64
-// -LSE*log2(e) and Delta values), the 16-bit P^T and dS^T of the step
-// (written by the compute threads, read by the tensor core), and an fp32
+// (resident for the unit), a ring of query steps (Q_i, dO_i, and their
+// -LSE*log2(e) and Delta values), the 16-bit dS^T of the step (written by
+// the compute threads, read by the tensor core), and an fp32
 // staging tile for dQ that TMA reduce-adds into the global accumulator: at
 // Dp = 128 SR rows x D, 32 rows per compute warpgroup and reduce-add; at
 // Dp = 64 SR rows x 32 columns per warpgroup, 128-byte swizzled.
@@ -125,9 +127,9 @@ struct BwdLayout {
   static constexpr int kKVBytes = kPanels * kPanelBytes;      // K or V tile: 128 rows x Dp
   static constexpr int kQPanelBytes = kSR * 128;              // SR rows x 64 16-bit elements
   static constexpr int kQBytes = kPanels * kQPanelBytes;      // Q or dO step: SR rows x Dp
-  static constexpr int kPTileBytes = (kSR / 64) * kPanelBytes;  // P^T or dS^T: 128 keys x SR queries
+  static constexpr int kPTileBytes = (kSR / 64) * kPanelBytes;  // dS^T: 128 keys x SR queries
   static constexpr int kStatBytes = 2 * kSR * 4;              // -LSE*log2(e) and Delta of one step
-  static constexpr int kStages = (kSR == 128) ? 2 : (kPanels == 2 ? 3 : 6);
+  static constexpr int kStages = (kSR == 128) ? 3 : (kPanels == 2 ? 3 : 6);
   // Epilogue: a key row's D columns in chunks of 32, the first kChunksWg for
   // compute warpgroup 0 and the rest for warpgroup 1.
   static constexpr int kChunks = D / 32;
@@ -137,8 +139,7 @@ struct BwdLayout {
   static constexpr int kK = 0;
   static constexpr int kV = kKVBytes;
   static constexpr int kRing = 2 * kKVBytes;
-  static constexpr int kP = kRing + kStages * kStageBytes;
-  static constexpr int kDS = kP + kPTileBytes;
+  static constexpr int kDS = kRing + kStages * kStageBytes;  // dS^T (P^T lives in tensor memory)
   static constexpr int kDQS = kDS + kPTileBytes;              // dQ staging: SR rows x D fp32
   static constexpr int kStats = kDQS + kSR * D * 4;
   static constexpr int kBars = kStats + kStages * kStatBytes;
@@ -153,14 +154,14 @@ struct BwdLayout {
   static constexpr uint32_t kColDP = 2 * kDp + kSR;
   static constexpr uint32_t kColDQ = 2 * kDp + 2 * kSR;
   static_assert(kColDQ + kSR <= kTmemCols, "TMEM budget");
-  // With 64-row steps (Dp = 128) the 64 columns past dQ^T can hold the
-  // step's P^T and dS^T as packed 16-bit pairs: the A operands of dV += P^T
-  // dO and dK += dS^T Q then come from tensor memory (the faster form of the
-  // MMA, and no shared-memory operand reads for them). dS^T also goes to
-  // shared memory, where dQ^T = K^T dS^T reads it as its B operand. Measured
-  // +1.8 % (target) and +2.5 % (B4 H16 N8192 D128) non-causal, and, with two
-  // non-sleeping issuers, +1 to +2 % on causal launches too (with one
-  // issuer it had been -2.4 % on long causal rows).
+  // With 64-row steps (Dp = 128) the 64 columns past dQ^T hold the step's
+  // P^T and dS^T as packed 16-bit pairs: the A operands of dV += P^T dO and
+  // dK += dS^T Q then come from tensor memory (the faster form of the MMA,
+  // and no shared-memory operand reads for them). dS^T also goes to shared
+  // memory, where dQ^T = K^T dS^T reads it as its B operand. Measured +1.8 %
+  // (target) and +2.5 % (B4 H16 N8192 D128) non-causal, and, with two
+  // non-sleeping issuers, +1 to +2 % on causal launches too (with one issuer
+  // it had been -2.4 % on long causal rows).
   static constexpr bool kGradATmem = (kSR == 64);
   // At Dp = 64 the step's dQ is computed untransposed, dQ = dS K (M = the
   // 128 query rows, N = 64): the rows fill all 128 TMEM lanes, so every
@@ -170,11 +171,18 @@ struct BwdLayout {
   // N = 128. dQ^T (lanes = head-dim index) puts only D of the 128 lanes to
   // use, so half the warps staged everything.
   static constexpr bool kDqRows = (kDp == 64);
-  static constexpr uint32_t kColPT = kColDQ + kSR;
+  // At Dp = 64 the untransposed dQ takes 64 of its region's 128 columns;
+  // the other 64 hold the step's P^T (128 query columns as packed pairs), so
+  // dV += P^T dO reads A from tensor memory at every head dimension (at Dp =
+  // 64 measured +5 to +11 % over P^T in shared memory, bit-identical). dS^T
+  // stays in shared memory only there: dK and dQ both read it from there.
+  static constexpr uint32_t kColPT = kDqRows ? kColDQ + kDp : kColDQ + kSR;
   static constexpr uint32_t kColDST = kColPT + kSR / 2;
+  static_assert(kGradATmem || kDqRows, "P^T has tensor-memory columns at every step height");
+  static_assert(kColPT + kSR / 2 <= kTmemCols, "TMEM budget");
   static_assert(!kGradATmem || kColDST + kSR / 2 <= kTmemCols, "TMEM budget");
   static_assert(kSmemBytes <= 232448, "shared memory budget");
-  static_assert(kRing % 1024 == 0 && kP % 1024 == 0 && kDS % 1024 == 0, "swizzled tiles need 1 KB alignment");
+  static_assert(kRing % 1024 == 0 && kDS % 1024 == 0, "swizzled tiles need 1 KB alignment");
 };
 
 // Work unit u -> (head, K/V tile). Non-causal: the tiles of a head are
@@ -285,7 +293,7 @@ __global__ void __launch_bounds__(bwd_threads(D), 1)
                    const __grid_constant__ CUtensorMap tmDQ, const BwdParams p) {
   using L = BwdLayout<D>;
   constexpr bool kTwoIssuers = true;
-  constexpr bool kATmem = L::kGradATmem;  // P^T, dS^T in TMEM for dV, dK
+  constexpr bool kATmem = L::kGradATmem;  // dS^T in TMEM for dK (P^T is there for dV at every D)
   constexpr bool kDqWarp = bwd_threads(D) > 352;  // staged dQ^T added by warp kBwdDqWarp
   constexpr uint32_t kReaders = kTwoIssuers ? 2 : 1;  // issuer threads reading a ring slot and K/V
   extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -296,7 +304,6 @@ __global__ void __launch_bounds__(bwd_threads(D), 1)
   const uint32_t sK = base + L::kK;
   const uint32_t sV = base + L::kV;
   const uint32_t sRing = base + L::kRing;
-  const uint32_t sP = base + L::kP;
   const uint32_t sDS = base + L::kDS;
   const uint32_t sStats = base + L::kStats;
   const float* stats = reinterpret_cast<const float*>(smem + L::kStats);
@@ -307,7 +314,7 @@ __global__ void __launch_bounds__(bwd_threads(D), 1)
   auto bar_stage_empty = [&](int s) { return bars + 16 + 8u * (L::kStages + s); };
   const uint32_t bar_s_full = bars + 16 + 16u * L::kStages;  // S^T, dP^T of a step in TMEM
   const uint32_t bar_s_free = bar_s_full + 8;                 // ... loaded by the compute threads
-  const uint32_t bar_p_full = bar_s_full + 16;                // P^T, dS^T of a step in shared memory
+  const uint32_t bar_p_full = bar_s_full + 16;                // P^T, dS^T of a step written
   const uint32_t bar_p_free = bar_s_full + 24;                // ... read by the tensor core
   const uint32_t bar_dq_full = bar_s_full + 32;               // dQ^T of a step in TMEM
   const uint32_t bar_dq_free = bar_s_full + 40;               // ... loaded by the compute threads
@@ -457,24 +464,22 @@ __global__ void __launch_bounds__(bwd_threads(D), 1)
           mma_ss_w(tmem + L::kColDP, v_lo + a, kHi, do_lo + b, kHi, idesc_s, kk > 0 ? 1u : 0u);
         }
       };
-      // dV += P^T dO_i and dK += dS^T Q_i: A = P^T / dS^T (K-major, panels
-      // of 64 query columns 16 KB apart), B = dO_i / Q_i (MN-major: rows are
-      // the contraction index, 64-column panels of SR rows), SR/16 steps of
-      // 16 rows.
+      // dV += P^T dO_i and dK += dS^T Q_i: A = P^T from tensor memory, dS^T
+      // from tensor memory (Dp = 128) or shared memory (K-major, panels of 64
+      // query columns 16 KB apart), B = dO_i / Q_i (MN-major: rows are the
+      // contraction index, 64-column panels of SR rows), SR/16 steps of 16
+      // rows.
       auto issue_grads = [&](int slot, bool acc) {
         const uint32_t st = sRing + static_cast<uint32_t>(slot * L::kStageBytes);
-        const uint32_t p_lo = desc_lo_sw128(sP, 16), ds_lo = desc_lo_sw128(sDS, 16);
+        const uint32_t ds_lo = desc_lo_sw128(sDS, 16);
         const uint32_t q_mn = desc_lo_sw128(st, L::kQPanelBytes);
         const uint32_t do_mn = desc_lo_sw128(st + L::kQBytes, L::kQPanelBytes);
 #pragma unroll
         for (int kk = 0; kk < L::kSR / 16; ++kk) {
-          const uint32_t a = static_cast<uint32_t>(((kk >> 2) * kPanelBytes + (kk & 3) * 32) >> 4);
           const uint32_t b = static_cast<uint32_t>((kk * 16 * 128) >> 4);
           const uint32_t acc_kk = (acc || kk > 0) ? 1u : 0u;
-          if constexpr (kATmem)  // A = P^T in TMEM: 16 query columns = 8 packed columns per K-step
-            mma_ts_w(tmem + L::kColDV, tmem + L::kColPT + 8u * kk, do_mn + b, kHi, idesc_acc, acc_kk);
-          else
-            mma_ss_w(tmem + L::kColDV, p_lo + a, kHi, do_mn + b, kHi, idesc_acc, acc_kk);
+          // A = P^T in TMEM: 16 query columns = 8 packed columns per K-step
+          mma_ts_w(tmem + L::kColDV, tmem + L::kColPT + 8u * kk, do_mn + b, kHi, idesc_acc, acc_kk);
         }
 #pragma unroll
         for (int kk = 0; kk < L::kSR / 16; ++kk) {
@@ -658,7 +663,6 @@ __global__ void __launch_bounds__(bwd_threads(D), 1)
     const uint32_t tS = tmem + lane_off + L::kColS + static_cast<uint32_t>(L::kCW * wg);
     const uint32_t tDP = tmem + lane_off + L::kColDP + static_cast<uint32_t>(L::kCW * wg);
     const uint32_t tDQ = tmem + lane_off + L::kColDQ + static_cast<uint32_t>(L::kCW * wg);
-    const uint32_t p_row = sP + static_cast<uint32_t>(rr * 128);
     const uint32_t ds_row = sDS + static_cast<uint32_t>(rr * 128);
     const uint32_t xr = static_cast<uint32_t>(rr & 7);
     const bool dq_rows = quarter * 32 < D;    // warp-uniform: lanes >= D of dQ^T are discarded
@@ -842,17 +846,13 @@ __global__ void __launch_bounds__(bwd_threads(D), 1)
           // the 64-column panel that holds them
           const int qc = L::kCW * wg + 32 * h;  // first query column of this half in the step
           const uint32_t panel = static_cast<uint32_t>((qc >> 6) * kPanelBytes);
-          if constexpr (kATmem) {
-            // P^T and dS^T of these 32 query columns into this thread's TMEM
-            // lane (16 packed columns per warpgroup)
-            tmem_st32x16(tmem + lane_off + L::kColPT + static_cast<uint32_t>(qc / 2), pk);
-            tmem_st32x16(tmem + lane_off + L::kColDST + static_cast<uint32_t>(qc / 2), dk);
-          }
+          // P^T (and, at 64-row steps, dS^T) of these 32 query columns into
+          // this thread's TMEM lane: 16 packed columns
+          tmem_st32x16(tmem + lane_off + L::kColPT + static_cast<uint32_t>(qc / 2), pk);
+          if constexpr (kATmem) tmem_st32x16(tmem + lane_off + L::kColDST + static_cast<uint32_t>(qc / 2), dk);
 #pragma unroll
           for (int ch = 0; ch < 4; ++ch) {
             const uint32_t col = panel + ((static_cast<uint32_t>(((qc & 63) >> 3) + ch) ^ xr) << 4);
-            if constexpr (!kATmem)
-              st_shared_v4(p_row + col, pk[4 * ch], pk[4 * ch + 1], pk[4 * ch + 2], pk[4 * ch + 3]);
             st_shared_v4(ds_row + col, dk[4 * ch], dk[4 * ch + 1], dk[4 * ch + 2], dk[4 * ch + 3]);
           }
         }
@@ -860,7 +860,7 @@ __global__ void __launch_bounds__(bwd_threads(D), 1)
           ok = false;
           break;
         }
-        if constexpr (kATmem) tmem_wait_st();
+        tmem_wait_st();
         fence_proxy_async_shared();
         tc_fence_before_sync();
         mbar_arrive(bar_p_full);
