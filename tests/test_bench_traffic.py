@@ -43,3 +43,20 @@ def test_hash_covers_every_listed_source():
         for f in files:
             assert os.path.exists(os.path.join(bench.KERNEL_SOURCES, f)), f
         assert bench.kernel_source_hash(files) != bench.kernel_source_hash(files[1:])
+
+
+def test_committed_figures_were_taken_on_the_kernels_as_they_stand():
+    # every entry in the committed file still matches its kernel's sources, so
+    # the bench reports each figure; reads + writes add up to the total
+    with open(bench.PROFILE_TRAFFIC) as f:
+        table = json.load(f)
+    entries = {k: v for k, v in table.items() if isinstance(v, dict)}
+    assert {"target", "bwd:target"} <= set(entries)
+    for name, e in entries.items():
+        if name.startswith("bwd:"):
+            files = bench.BWD_KERNEL_FILES
+        else:
+            files = bench.fwd_kernel_files(bench.workloads.WORKLOADS[name].D)
+        assert e["kernel_source_hash"] == bench.kernel_source_hash(files), name
+        assert e["dram_bytes_per_launch"] == e["dram_bytes_read_per_launch"] + e["dram_bytes_write_per_launch"], name
+        assert bench.traffic_per_launch(name, files) == e["dram_bytes_per_launch"], name
